@@ -1,0 +1,328 @@
+"""Seeded synthetic inputs for the KDA prefill forward.
+
+This module holds input recipes only -- no step of the method's arithmetic.  It
+is the one piece shared by the oracle tests, the GPU parity tests and the
+benchmark.  Every recipe is seeded by ``(name, seed, salt)``; a fresh salt per
+run follows "NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section
+04 HARDENING (every scoring run draws a fresh random seed, and distributions and
+layouts vary), and the extreme-value probes follow the same section's stress
+probes (deep decays, saturated gates, boundary lengths, repeated keys).
+
+Layouts: q, k, g ``[B, T, H, dk]``; v ``[B, T, H, dv]``; beta ``[B, T, H]``;
+h0 ``[N, H, dk, dv]`` fp32; cu_seqlens int32 ``[N + 1]`` for packed varlen (B = 1).
+"""
+from __future__ import annotations
+
+import hashlib
+import math
+import os
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+import torch
+
+LN_1E4 = math.log(1e-4)
+LN_1E6 = math.log(1e-6)
+
+
+def fresh_salt() -> int:
+    env = os.environ.get("KDA_SALT")
+    if env is not None:
+        return int(env)
+    return int.from_bytes(os.urandom(4), "little")
+
+
+def _rng(name: str, seed: int, salt: int) -> np.random.Generator:
+    h = hashlib.sha256(f"{name}|{seed}|{salt}".encode()).digest()
+    return np.random.default_rng(int.from_bytes(h[:8], "little"))
+
+
+@dataclass
+class KdaInputs:
+    name: str
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    g: torch.Tensor
+    beta: torch.Tensor
+    h0: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]
+    scale: float
+    seed: int = 0
+    salt: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self):
+        return self.q.shape[0]
+
+    @property
+    def T(self):
+        return self.q.shape[1]
+
+    @property
+    def H(self):
+        return self.q.shape[2]
+
+    @property
+    def dk(self):
+        return self.q.shape[3]
+
+    @property
+    def dv(self):
+        return self.v.shape[3]
+
+    @property
+    def num_seqs(self):
+        return self.cu_seqlens.numel() - 1 if self.cu_seqlens is not None else self.B
+
+    @property
+    def tokens(self):
+        return self.B * self.T
+
+    def seq_lens(self):
+        if self.cu_seqlens is None:
+            return [self.T] * self.B
+        cu = self.cu_seqlens.tolist()
+        return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+
+    def tensors(self):
+        return dict(q=self.q, k=self.k, v=self.v, g=self.g, beta=self.beta, h0=self.h0,
+                    cu_seqlens=self.cu_seqlens, scale=self.scale)
+
+    def to(self, device):
+        mv = lambda t: None if t is None else t.to(device)  # noqa: E731
+        return KdaInputs(self.name, mv(self.q), mv(self.k), mv(self.v), mv(self.g),
+                         mv(self.beta), mv(self.h0), mv(self.cu_seqlens), self.scale,
+                         self.seed, self.salt, dict(self.meta))
+
+
+# --------------------------------------------------------------------------- pieces
+
+def _t(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dtype)
+
+
+def _softplus(x: np.ndarray) -> np.ndarray:
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def _student_t_mixture(rng, shape, H):
+    """Student-t(nu=4) draws times a per-head scale s ~ U[0.1, 3] (one per tensor)."""
+    s = rng.uniform(0.1, 3.0, size=H).astype(np.float32)
+    x = rng.standard_t(4.0, size=shape).astype(np.float32)
+    return x * s[None, None, :, None]
+
+
+def _gate_cfg2(rng, shape):
+    x = rng.normal(-1.0, 2.0, size=shape).astype(np.float32)
+    g = -_softplus(x)
+    return np.maximum(g, LN_1E4).astype(np.float32)
+
+
+def _cu(lengths) -> torch.Tensor:
+    return torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+
+
+def uniform_split(rng, total: int, n: int, max_len: int = 4000) -> np.ndarray:
+    """n lengths summing to total: one of length 1, the rest from uniform cut points,
+    every length <= max_len, at least one length with L mod 64 != 0."""
+    assert n >= 2
+    for _ in range(10000):
+        rest = total - 1
+        cuts = np.sort(rng.choice(np.arange(1, rest), size=n - 2, replace=False))
+        parts = np.diff(np.concatenate([[0], cuts, [rest]]))
+        if parts.min() < 2 or parts.max() > max_len:
+            continue
+        if not np.any(parts % 64 != 0):
+            continue
+        pos = int(rng.integers(0, n))
+        lens = np.insert(parts, pos, 1)
+        return lens.astype(np.int64)
+    raise RuntimeError("could not draw a valid split")
+
+
+def skewed_split(rng, total: int, n: int, dominant: int = 5000, sigma: float = 1.5):
+    """Log-normal(sigma) lengths with one dominant sequence of about `dominant` tokens."""
+    dom = int(round(dominant * rng.uniform(0.95, 1.05)))
+    w = rng.lognormal(0.0, sigma, size=n - 1)
+    rest = total - dom
+    lens = np.maximum(1, np.floor(w / w.sum() * rest)).astype(np.int64)
+    # fix the sum exactly, keeping every length >= 1 and below the dominant one
+    diff = rest - lens.sum()
+    order = np.argsort(-lens)
+    i = 0
+    while diff != 0:
+        j = order[i % len(order)]
+        if diff > 0:
+            lens[j] += 1
+            diff -= 1
+        elif lens[j] > 1:
+            lens[j] -= 1
+            diff += 1
+        i += 1
+    assert lens.max() < dom
+    pos = int(rng.integers(0, n))
+    return np.insert(lens, pos, dom).astype(np.int64)
+
+
+# --------------------------------------------------------------------------- recipes
+
+def make_cfg1(seed: int = 0, salt: int = 0, T: int = 256, H: int = 2, d: int = 64,
+              B: int = 1, dtype=torch.float32) -> KdaInputs:
+    """Tiny fixed length: q, k, v ~ N(0,1) (fp32); g = -softplus(N(0,1));
+    beta = sigmoid(N(0,1)); h0 = 0; scale = dk^-0.5."""
+    rng = _rng("cfg1", seed, salt)
+    q = rng.normal(size=(B, T, H, d))
+    k = rng.normal(size=(B, T, H, d))
+    v = rng.normal(size=(B, T, H, d))
+    g = -_softplus(rng.normal(size=(B, T, H, d)))
+    beta = 1.0 / (1.0 + np.exp(-rng.normal(size=(B, T, H))))
+    h0 = torch.zeros(B, H, d, d, dtype=torch.float32)
+    return KdaInputs("cfg1", _t(q, dtype), _t(k, dtype), _t(v, dtype), _t(g, torch.float32),
+                     _t(beta, torch.float32), h0, None, d ** -0.5, seed, salt)
+
+
+def _cfg2_like(rng, B, T, H, dk, dv, N, dtype):
+    q = _student_t_mixture(rng, (B, T, H, dk), H)
+    k = _student_t_mixture(rng, (B, T, H, dk), H)
+    v = _student_t_mixture(rng, (B, T, H, dv), H)
+    g = _gate_cfg2(rng, (B, T, H, dk))
+    beta = 1.0 / (1.0 + np.exp(-rng.normal(0.0, 1.5, size=(B, T, H))))
+    h0 = rng.normal(0.0, 0.1, size=(N, H, dk, dv)).astype(np.float32)
+    return (_t(q, dtype), _t(k, dtype), _t(v, dtype), _t(g, torch.float32),
+            _t(beta, torch.float32), torch.from_numpy(h0))
+
+
+def make_cfg2(seed: int = 0, salt: int = 0, T: int = 8192, H: int = 32, d: int = 128,
+              B: int = 1, dtype=torch.bfloat16) -> KdaInputs:
+    """Fixed length: Student-t(4) mixture with per-head scale in [0.1, 3] for q, k, v
+    (bf16); g = -softplus(N(-1, 2)) clamped to alpha >= 1e-4; beta = sigmoid(N(0, 1.5));
+    h0 ~ N(0, 0.1) fp32."""
+    rng = _rng("cfg2", seed, salt)
+    q, k, v, g, beta, h0 = _cfg2_like(rng, B, T, H, d, d, B, dtype)
+    return KdaInputs("cfg2", q, k, v, g, beta, h0, None, d ** -0.5, seed, salt)
+
+
+def make_cfg3(seed: int = 0, salt: int = 0, total: int = 8192, n: int = 8, H: int = 32,
+              d: int = 128, dtype=torch.bfloat16, max_len: int = 4000) -> KdaInputs:
+    """Varlen: a seeded uniform split into n sequences (one of length 1, lengths up to
+    max_len, some with L mod 64 != 0); per-sequence h0; distributions as cfg2."""
+    rng = _rng("cfg3", seed, salt)
+    lens = uniform_split(rng, total, n, max_len=max_len)
+    q, k, v, g, beta, h0 = _cfg2_like(rng, 1, total, H, d, d, n, dtype)
+    return KdaInputs("cfg3", q, k, v, g, beta, h0, _cu(lens), d ** -0.5, seed, salt,
+                     {"lens": lens.tolist()})
+
+
+def _rows_with_norms(rng, shape, lo=1e-3, hi=1e3):
+    x = rng.standard_t(4.0, size=shape)
+    x = x / np.maximum(np.linalg.norm(x, axis=-1, keepdims=True), 1e-30)
+    nrm = 10.0 ** rng.uniform(math.log10(lo), math.log10(hi), size=shape[:-1] + (1,))
+    return (x * nrm).astype(np.float32)
+
+
+def make_cfg4(seed: int = 0, salt: int = 0, total: int = 8192, n: int = 32, H: int = 32,
+              d: int = 128, dtype=torch.bfloat16, dominant: int = 5000) -> KdaInputs:
+    """Varlen skewed: log-normal(1.5) lengths with one ~5000-token sequence.  Probes:
+    g = -1e-6 on a random half of the key channels of each head, g = ln(1e-6) on the
+    rest; beta spikes (0 or 1 with probability 0.1 each); q/k row norms log-uniform in
+    [1e-3, 1e3]."""
+    rng = _rng("cfg4", seed, salt)
+    lens = skewed_split(rng, total, n, dominant=dominant)
+    q = _rows_with_norms(rng, (1, total, H, d))
+    k = _rows_with_norms(rng, (1, total, H, d))
+    v = _student_t_mixture(rng, (1, total, H, d), H)
+    slow = np.zeros((H, d), dtype=bool)
+    for h in range(H):
+        slow[h, rng.permutation(d)[: d // 2]] = True
+    g = np.where(slow[None, None], np.float32(-1e-6), np.float32(LN_1E6))
+    g = np.broadcast_to(g, (1, total, H, d)).astype(np.float32)
+    beta = 1.0 / (1.0 + np.exp(-rng.normal(0.0, 1.5, size=(1, total, H))))
+    u = rng.uniform(size=(1, total, H))
+    beta = np.where(u < 0.1, 0.0, np.where(u < 0.2, 1.0, beta))
+    h0 = rng.normal(0.0, 0.1, size=(n, H, d, d)).astype(np.float32)
+    return KdaInputs("cfg4", _t(q, dtype), _t(k, dtype), _t(v, dtype), _t(g, torch.float32),
+                     _t(beta, torch.float32), torch.from_numpy(h0), _cu(lens), d ** -0.5,
+                     seed, salt, {"lens": lens.tolist()})
+
+
+def make_cfg5(H: int, total: int, varlen: bool, seed: int = 0, salt: int = 0,
+              d: int = 128, dtype=torch.bfloat16) -> KdaInputs:
+    """Throughput sweep row: fixed = total/8192 sequences of 8192 tokens; varlen = the
+    cfg3 recipe with total/1024 sequences."""
+    if varlen:
+        n = max(2, total // 1024)
+        x = make_cfg3(seed, salt, total=total, n=n, H=H, d=d, dtype=dtype,
+                      max_len=max(4000, total // 2))
+        x.name = f"cfg5-varlen-H{H}-{total}"
+        return x
+    B = total // 8192
+    x = make_cfg2(seed, salt, T=8192, H=H, d=d, B=B, dtype=dtype)
+    x.name = f"cfg5-fixed-H{H}-{total}"
+    return x
+
+
+def make_lengths(lengths, seed: int = 0, salt: int = 0, H: int = 2, d: int = 64,
+                 dk: Optional[int] = None, dv: Optional[int] = None,
+                 dtype=torch.bfloat16, h0: bool = True, name: str = "lengths") -> KdaInputs:
+    """cfg2-style distributions on an explicit list of sequence lengths (packed varlen;
+    zero-length sequences allowed)."""
+    dk = dk or d
+    dv = dv or d
+    rng = _rng(name + "|" + ",".join(map(str, lengths)), seed, salt)
+    lens = np.asarray(lengths, dtype=np.int64)
+    total = int(lens.sum())
+    q, k, v, g, beta, h0t = _cfg2_like(rng, 1, total, H, dk, dv, len(lens), dtype)
+    return KdaInputs(name, q, k, v, g, beta, h0t if h0 else None, _cu(lens), dk ** -0.5,
+                     seed, salt, {"lens": lens.tolist()})
+
+
+def make_probe(kind: str, seed: int = 0, salt: int = 0, T: int = 200, H: int = 2,
+               d: int = 64, dtype=torch.bfloat16) -> KdaInputs:
+    """Stress probes: 'deep' (g ~ -6.5 per token, ~600 bits per 64 tokens),
+    'abyss' (g = -60: every step forgets almost all), 'saturated' (g = 0, alpha = 1),
+    'repeated_keys' (one key reused across the sequence), 'beta01' (beta in {0, 1}),
+    'beta0' (beta = 0: pure decay), 'zero_rows' (some q/k rows exactly zero),
+    'long_memory' (g = -softplus(N(-10, 1)), alpha ~ 0.99995, and small writes
+    beta = sigmoid(N(-4.5, 1)): an error in the state persists for thousands of tokens
+    instead of being forgotten or overwritten)."""
+    rng = _rng("probe-" + kind, seed, salt)
+    q, k, v, g, beta, h0 = _cfg2_like(rng, 1, T, H, d, d, 1, dtype)
+    g = g.numpy()
+    beta = beta.numpy()
+    if kind == "deep":
+        g = (-6.5 * rng.uniform(0.8, 1.2, size=g.shape)).astype(np.float32)
+    elif kind == "abyss":
+        g = np.full(g.shape, -60.0, dtype=np.float32)
+    elif kind == "long_memory":
+        x = rng.normal(-10.0, 1.0, size=g.shape).astype(np.float32)
+        g = (-_softplus(x)).astype(np.float32)
+        beta = (1.0 / (1.0 + np.exp(-rng.normal(-4.5, 1.0, size=beta.shape)))).astype(np.float32)
+    elif kind == "saturated":
+        g = np.zeros(g.shape, dtype=np.float32)
+    elif kind == "repeated_keys":
+        kk = k.float().numpy()
+        kk[:, :, :, :] = kk[:, :1, :, :]
+        k = _t(kk, dtype)
+    elif kind == "beta01":
+        beta = (rng.uniform(size=beta.shape) < 0.5).astype(np.float32)
+    elif kind == "beta0":
+        beta = np.zeros(beta.shape, dtype=np.float32)
+    elif kind == "zero_rows":
+        qq, kk = q.float().numpy(), k.float().numpy()
+        zq = rng.uniform(size=qq.shape[:3]) < 0.1
+        zk = rng.uniform(size=kk.shape[:3]) < 0.1
+        qq[zq] = 0.0
+        kk[zk] = 0.0
+        q, k = _t(qq, dtype), _t(kk, dtype)
+    else:
+        raise ValueError(kind)
+    return KdaInputs("probe-" + kind, q, k, v, torch.from_numpy(np.ascontiguousarray(g)),
+                     torch.from_numpy(np.ascontiguousarray(beta)), h0, None, d ** -0.5,
+                     seed, salt)
+
+
+PROBES = ("deep", "abyss", "saturated", "repeated_keys", "beta01", "beta0", "zero_rows",
+          "long_memory")
