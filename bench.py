@@ -1,0 +1,369 @@
+"""Benchmark: KDA prefill forward tokens/s on one GB300 (or N replicas).
+
+Workload: fixed length B=1, T=8192, H=32, dk=dv=128, bf16 q/k/v, fp32 g/beta/h0
+(the Student-t / deep-gate recipe of tests/gen.py, fresh salt per run).  A step is
+one kda_fwd over the whole batch: schedule, per-chunk factors, state recurrence.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` = tokens/s over all ranks with inputs resident in
+HBM; `e2e` = the same metric through the public binding with pinned host buffers,
+host-to-device inputs and device-to-host outputs inside the timed region;
+`roofline` = the dominant kernel's algorithmic bytes per launch over its
+CUDA-event duration, against the measured HBM copy bandwidth.  The per-step input
+(336 MB) and factor workspace (~300 MB) exceed the 129 MB L2, so no L2 flush is
+inserted between steps.  `--impl reference` times the fp64 CPU oracle on this
+host's cores on the same workload (a bounded number of heads per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from tests import gen  # noqa: E402
+
+METRIC = "KDA fwd tokens/s at H=32,d=128,8192 tok; % tensor-pipe/HBM roofline"
+WORKLOAD = "fixed-length B=1 T=8192 H=32 dk=dv=128 bf16 q/k/v, fp32 g/beta/h0 (Student-t mixture, g=-softplus(N(-1,2)) clamped)"
+B, T, H, D = 1, 8192, 32, 128
+KERNEL_NAMES = ["schedule", "factors", "state_recurrence"]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _algorithmic_bytes(kernel: str, tokens: int, heads: int, dk: int, dv: int, nseq: int):
+    """Algorithmic HBM bytes one launch of `kernel` must move (bf16 q/k/v/o, fp32 g/beta/states)."""
+    th = tokens * heads
+    if kernel == "factors":       # reads q, k, v, g, beta
+        return th * (2 * dk * 2 + dv * 2 + dk * 4 + 4)
+    if kernel == "state_recurrence":  # writes o; reads h0, writes hT
+        return th * dv * 2 + 2 * nseq * heads * dk * dv * 4
+    return 0
+
+
+def _path_bytes(tokens, heads, dk, dv, nseq):
+    return tokens * heads * (2 * dk * 2 + 2 * dv * 2 + dk * 4 + 4) + 2 * nseq * heads * dk * dv * 4
+
+
+class ClockSampler:
+    """nvidia-smi samples while the timed region runs (median SM clock, throttle reasons)."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic_for(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel's source is
+    unchanged since it was captured (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    ent = j.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "gated_delta_rule_25_gb300", "csrc", ent["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if h == ent["sha"] else None
+
+
+def _oracle_sample(x, heads: int, nthreads: int = 0):
+    import oracle
+    t = x.tensors()
+    for key in ("q", "k", "v", "g", "beta"):
+        t[key] = t[key][:, :, :heads].contiguous()
+    if t["h0"] is not None:
+        t["h0"] = t["h0"][:, :heads].contiguous()
+    t0 = time.perf_counter()
+    oracle.kda_recurrence_fp64(**t, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x, budget_s: float = 12.0):
+    """The fp64 oracle, as it stands, on this host's cores: whole heads of the same
+    workload until ~budget_s of work; tokens/s scaled to all H heads."""
+    import oracle
+    cores = oracle.max_threads()
+    heads = min(H, max(1, cores))
+    dt = _oracle_sample(x, heads)
+    reps = 1
+    total = dt
+    while total < budget_s and reps < 8:
+        total += _oracle_sample(x, heads)
+        reps += 1
+    per_run = total / reps
+    tok_s = (x.tokens * heads / H) / per_run
+    return {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} of {H} heads x {x.tokens} tokens, {reps} runs, fp64 C recurrence; "
+                      "tokens/s scaled to all heads"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    x = gen.make_cfg2(seed=0, salt=gen.fresh_salt())
+    cores = oracle.max_threads()
+    heads = min(H, max(1, cores))
+    for _ in range(args.warmup):
+        _oracle_sample(x, max(1, heads // 4))
+    times = [_oracle_sample(x, heads) for _ in range(args.steps)]
+    per = sum(times) / len(times)
+    tok_s = (x.tokens * heads / H) / per
+    line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3 * H / heads, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": x.tokens},
+            "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {heads} of {H} heads x {x.tokens} tokens "
+                                       "(fp64 token recurrence); tokens/s scaled to all heads"},
+            "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_delta_rule_25_gb300 as kda
+
+    salt = gen.fresh_salt() + rank
+    x = gen.make_cfg2(seed=0, salt=salt)
+    xd = x.to(dev)
+    nseq = x.num_seqs
+    o = torch.empty_like(xd.v)
+    hT = torch.empty_like(xd.h0)
+    ws = torch.empty(kda.workspace_size(B, T, H, D, D, nseq) + 256, dtype=torch.uint8, device=dev)
+    nl = kda.launch_count(B, T, H, D, D, nseq)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        kda.fwd(**xd.tensors(), o=o, hT=hT, workspace=ws, events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # per-launch boundary events for every timed step (kernel timing on the launching stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_kernel = [0.0] * nl
+    for row in evs:
+        for j in range(nl):
+            per_kernel[j] += row[j].elapsed_time(row[j + 1])
+    per_kernel = [t / args.steps for t in per_kernel]
+
+    t_max = torch.tensor([elapsed_ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    ms_step = float(t_max.item()) / args.steps
+    value = world * x.tokens / (ms_step * 1e-3)
+
+    # parity after timing, on fresh inputs through the same buffers (sampled heads)
+    x2 = gen.make_cfg2(seed=1, salt=salt + 7919)
+    for name in ("q", "k", "v", "g", "beta", "h0"):
+        getattr(xd, name).copy_(getattr(x2, name).to(dev))
+    step()
+    torch.cuda.synchronize(dev)
+    parity = None
+    if rank == 0:
+        import oracle
+        from tests.metrics import rel_rmse
+        hs = [0, 17]
+        t = x2.tensors()
+        for key in ("q", "k", "v", "g", "beta"):
+            t[key] = t[key][:, :, hs].contiguous()
+        t["h0"] = t["h0"][:, hs].contiguous()
+        o_ref, h_ref = oracle.kda_recurrence_fp64(**t)
+        parity = {"heads": hs, "o_rel_rmse": rel_rmse(o.cpu()[:, :, hs], o_ref),
+                  "hT_rel_rmse": rel_rmse(hT.cpu()[:, hs], h_ref), "salt": x2.salt}
+
+    # end to end through the public binding: pinned host in, pinned host out
+    host_in = {n: getattr(x, n).pin_memory() for n in ("q", "k", "v", "g", "beta", "h0")}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_host = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * h_host.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        kda.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["h0"],
+                None, x.scale, o=o, hT=hT, workspace=ws)
+        o_host.copy_(o, non_blocking=True)
+        h_host.copy_(hT, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * x.tokens / (float(e_ms.item()) * 1e-3)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    hbm, bf16_tf, peak_src = _peaks()
+    dom = int(np.argmax(per_kernel))
+    dom_name = KERNEL_NAMES[dom] if dom < len(KERNEL_NAMES) else f"kernel{dom}"
+    alg = _algorithmic_bytes(dom_name, x.tokens, H, D, D, nseq)
+    achieved = alg / (per_kernel[dom] * 1e-3) / 1e9
+    path_gbs = _path_bytes(x.tokens, H, D, D, nseq) / (ms_step * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": x.tokens, "heads": H, "dk": D,
+                   "dv": D, "l2": "no flush: 336 MB of inputs and ~300 MB of factors per step exceed the 129 MB L2",
+                   "salt": salt},
+        "gpu_launches": nl * args.steps,
+        "kernels_ms": {KERNEL_NAMES[j] if j < len(KERNEL_NAMES) else f"kernel{j}": per_kernel[j]
+                       for j in range(nl)},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for(dom_name),
+                     "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
+        "path_roofline": {"bytes_per_step": _path_bytes(x.tokens, H, D, D, nseq),
+                          "achieved_gbs": path_gbs, "frac": path_gbs / hbm},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "parity": parity,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

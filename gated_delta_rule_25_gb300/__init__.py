@@ -1,0 +1,173 @@
+"""Kimi Delta Attention prefill forward for GB300 (sm_103a).
+
+A thin binding over the C ABI in ``include/kda.h`` (``_lib/libkda.so``).  This
+module only checks and marshals arguments; every step of the computation runs in
+the library's CUDA kernels.  PyTorch provides device memory and the current
+stream.  There is no CPU path: without the built library every call raises.
+
+    o, hT = fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None)
+
+q, k: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, same dtype); g: [B, T, H, dk]
+fp32 (log of the per-channel decay, <= 0); beta: [B, T, H] fp32 in [0, 1];
+h0: [N, H, dk, dv] fp32 or None; cu_seqlens: int32 [N + 1] (packed varlen, B == 1)
+or None.  Returns o [B, T, H, dv] in q's dtype and hT [N, H, dk, dv] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkda.so")
+
+KDA_OK, KDA_ERR_DEVICE = 0, 6
+KDA_BF16, KDA_FP32 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size or dtype",
+           3: "tensor pointer not 16-byte aligned", 4: "workspace missing, too small or misaligned",
+           5: "CUDA runtime error", 6: "device reported malformed input"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str = "kda_fwd"):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS.get(status, 'unknown')} (status {status})")
+
+
+def load_library():
+    """Load libkda.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.kda_fwd_workspace_size.argtypes = [i32] * 6
+        lib.kda_fwd_workspace_size.restype = sz
+        lib.kda_fwd_launch_count.argtypes = [i32] * 6
+        lib.kda_fwd_launch_count.restype = i32
+        lib.kda_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                f32, vp, vp, vp, sz, vp]
+        lib.kda_fwd.restype = i32
+        lib.kda_fwd_profiled.argtypes = lib.kda_fwd.argtypes + [ctypes.POINTER(vp)]
+        lib.kda_fwd_profiled.restype = i32
+        lib.kda_fwd_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.kda_fwd_check.restype = i32
+        lib.kda_status_string.argtypes = [i32]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def workspace_size(B: int, T: int, H: int, dk: int, dv: int, num_seqs: int) -> int:
+    return int(load_library().kda_fwd_workspace_size(B, T, H, dk, dv, num_seqs))
+
+
+def launch_count(B: int, T: int, H: int, dk: int, dv: int, num_seqs: int) -> int:
+    return int(load_library().kda_fwd_launch_count(B, T, H, dk, dv, num_seqs))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+        beta: torch.Tensor, h0: Optional[torch.Tensor] = None,
+        cu_seqlens: Optional[torch.Tensor] = None, scale: Optional[float] = None, *,
+        output_final_state: bool = True, o: Optional[torch.Tensor] = None,
+        hT: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+        check: bool = False, events=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """KDA prefill forward on the current CUDA stream.  See the module docstring.
+
+    ``o``, ``hT``, ``workspace``: optional preallocated buffers (needed for CUDA-graph
+    capture with stable addresses).  ``check``: synchronise and raise on a device-side
+    error.  ``events``: launch_count + 1 recorded torch.cuda.Event objects; each kernel
+    launch is bracketed by two of them (per-kernel timing)."""
+    lib = load_library()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, dk]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _check(k, "k", q.dtype, (B, T, H, dk), dev)
+    _check(v, "v", q.dtype, (B, T, H, dv), dev)
+    _check(q, "q", q.dtype, (B, T, H, dk), dev)
+    _check(g, "g", torch.float32, (B, T, H, dk), dev)
+    _check(beta, "beta", torch.float32, (B, T, H), dev)
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("varlen (cu_seqlens) needs B == 1")
+        _check(cu_seqlens, "cu_seqlens", torch.int32, (cu_seqlens.numel(),), dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (N, H, dk, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", q.dtype, (B, T, H, dv), dev)
+    if output_final_state:
+        if hT is None:
+            hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+        else:
+            _check(hT, "hT", torch.float32, (N, H, dk, dv), dev)
+    else:
+        hT = None
+    ws_bytes = int(lib.kda_fwd_workspace_size(B, T, H, dk, dv, N))
+    if ws_bytes == 0:
+        raise KdaError(2, "kda_fwd_workspace_size")
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    ws_ptr = (workspace.data_ptr() + 255) & ~255
+    avail = workspace.numel() - (ws_ptr - workspace.data_ptr())
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    dt = KDA_BF16 if q.dtype == torch.bfloat16 else KDA_FP32
+    args = (_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+            N, B, T, H, dk, dv, float(scale), _ptr(o), _ptr(hT), ctypes.c_void_p(ws_ptr), avail,
+            ctypes.c_void_p(stream))
+    if events is None:
+        st = lib.kda_fwd(*args)
+    else:
+        # one torch.cuda.Event per launch boundary (kda_fwd_launch_count + 1), already
+        # recorded once so that its CUDA event exists
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        st = lib.kda_fwd_profiled(*args, arr)
+    if st != KDA_OK:
+        raise KdaError(st)
+    if check:
+        err = ctypes.c_uint32(0)
+        st = lib.kda_fwd_check(ctypes.c_void_p(ws_ptr), ctypes.c_void_p(stream), ctypes.byref(err))
+        if st != KDA_OK:
+            raise KdaError(st, f"kda_fwd_check (device error bits {err.value:#x})")
+    return o, hT
+
+
+__all__ = ["fwd", "workspace_size", "launch_count", "load_library", "KdaError", "LIB_PATH"]

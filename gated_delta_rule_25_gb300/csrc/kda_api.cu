@@ -1,0 +1,141 @@
+// C ABI of the KDA prefill forward: argument checks, workspace carving, launches.
+// Declarations and the contract are in include/kda.h.
+#include <cmath>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+bool valid_head_dim(int x) { return x == 64 || x == 128; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks sizes; fills Dims.  Returns KDA_OK or the status to report.
+kda_status make_dims(int B, int T, int H, int dk, int dv, int num_seqs, bool varlen,
+                     kda::Dims& d) {
+    if (B < 0 || T < 0 || H <= 0 || num_seqs < 0) return KDA_ERR_INVALID_ARG;
+    if (!valid_head_dim(dk) || !valid_head_dim(dv)) return KDA_ERR_UNSUPPORTED;
+    if (varlen) {
+        if (B != 1) return KDA_ERR_INVALID_ARG;
+    } else if (num_seqs != B) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    // token-head rows and grid sizes stay well inside 32-bit launch limits
+    if ((long long)B * T * H > (1LL << 31) / 4) return KDA_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * H * 4 > (1LL << 31) - 1) return KDA_ERR_UNSUPPORTED;
+    d = kda::Dims{B, T, H, dk, dv, num_seqs, varlen};
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs) {
+    // B == 1 may be either layout; the varlen bound (T/64 + N chunks) covers both.
+    kda::Dims d;
+    if (make_dims(B, T, H, dk, dv, num_seqs, B == 1, d) != KDA_OK) return 0;
+    return kda::WsLayout(d).total;
+}
+
+int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
+    (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)num_seqs;
+    return 3;  // schedule, factors, state recurrence
+}
+
+}  // extern "C"
+
+namespace {
+
+kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                    const float* g, const float* beta, const float* h0,
+                    const int32_t* cu_seqlens, int num_seqs,
+                    int B, int T, int H, int dk, int dv, float scale,
+                    void* o, float* hT,
+                    void* workspace, size_t workspace_bytes, kda_stream_t stream,
+                    void* const* events) {
+    if (qkv_dtype != KDA_BF16 && qkv_dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    kda::Dims d;
+    kda_status st = make_dims(B, T, H, dk, dv, num_seqs, cu_seqlens != nullptr, d);
+    if (st != KDA_OK) return st;
+    const bool any_tokens = (long long)B * T > 0;
+    if (any_tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o) ||
+        !aligned16(beta) || !aligned16(h0) || !aligned16(hT) || !aligned16(cu_seqlens))
+        return KDA_ERR_ALIGNMENT;
+    kda::WsLayout W(d);
+    if (!workspace || workspace_bytes < W.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KDA_ERR_WORKSPACE;
+    if (num_seqs == 0) return KDA_OK;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const bool bf16 = qkv_dtype == KDA_BF16;
+    int ev = 0;
+    auto mark = [&]() -> bool {
+        if (!events) return true;
+        return cudaEventRecord(static_cast<cudaEvent_t>(events[ev++]), s) == cudaSuccess;
+    };
+    if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!mark() || kda::launch_prep(d, bf16, q, k, v, g, beta, ws, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (!mark() || kda::launch_chain_simt(d, bf16, h0, scale, o, hT, ws, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (!mark()) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                   const float* g, const float* beta, const float* h0,
+                   const int32_t* cu_seqlens, int num_seqs,
+                   int B, int T, int H, int dk, int dv, float scale,
+                   void* o, float* hT,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return fwd_impl(q, k, v, qkv_dtype, g, beta, h0, cu_seqlens, num_seqs, B, T, H, dk, dv,
+                    scale, o, hT, workspace, workspace_bytes, stream, nullptr);
+}
+
+kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                            const float* g, const float* beta, const float* h0,
+                            const int32_t* cu_seqlens, int num_seqs,
+                            int B, int T, int H, int dk, int dv, float scale,
+                            void* o, float* hT,
+                            void* workspace, size_t workspace_bytes, kda_stream_t stream,
+                            void* const* events) {
+    if (!events) return KDA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, qkv_dtype, g, beta, h0, cu_seqlens, num_seqs, B, T, H, dk, dv,
+                    scale, o, hT, workspace, workspace_bytes, stream, events);
+}
+
+kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* device_error) {
+    if (!workspace) return KDA_ERR_WORKSPACE;
+    kda::Header hdr{};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&hdr, workspace, sizeof(hdr), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (device_error) *device_error = hdr.error;
+    return hdr.error ? KDA_ERR_DEVICE : KDA_OK;
+}
+
+const char* kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported size or dtype";
+        case KDA_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+        case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case KDA_ERR_CUDA: return "CUDA runtime error";
+        case KDA_ERR_DEVICE: return "device reported malformed input";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// Internal definitions shared by the KDA kernels and the C-ABI layer.
+//
+// Workspace (caller-owned, 256-byte aligned), carved as:
+//   [0, 256)        header: u32 error word, i32 total chunk count
+//   seq_first       int32[N + 1]: index of the first chunk of each sequence
+//   chunks          int4[Cmax]:   {sequence, first token row, valid rows L, 0}
+//   factors         per (chunk, head): the factors of the chunkwise form
+//
+// Per (chunk, head) factor block, every part a multiple of 256 bytes:
+//   W   [64 x dk] bf16, operand layout  w = (I + A)^-1 Diag(beta) (kh * exp(Gamma))
+//   QG  [64 x dk] bf16, operand layout  qh * exp(Gamma)
+//   KT  [dk x 64] bf16, operand layout  (kh * exp(Gamma_last - Gamma))^T
+//   P   [64 x 64] bf16, operand layout  sum_c qh_ic kh_jc exp(Gamma_ic - Gamma_jc), j <= i
+//   U0  [64 x dv] bf16, row-major       u = (I + A)^-1 Diag(beta) v
+//   GL  [dk] fp32                       exp(Gamma_last)
+//
+// "Operand layout" is the K-major, unswizzled tensor-core shared-memory layout for
+// an R x K bf16 tile: 8 x 8 core matrices of 128 contiguous bytes, core matrix
+// (row block rb, k block kb) at byte ((kb * R/8) + rb) * 128.  A bulk copy of the
+// block lands in shared memory ready for tcgen05.mma, with descriptor leading
+// byte offset (between core matrices adjacent in K) = R/8 * 128 and stride byte
+// offset (between core matrices adjacent in rows) = 128.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace kda {
+
+constexpr int kChunk = 64;
+
+struct Dims {
+    int B, T, H, dk, dv, N;
+    bool varlen;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Upper bound on the number of chunks over all sequences.
+__host__ __device__ inline long long max_chunks(const Dims& d) {
+    if (d.varlen) return (long long)d.T / kChunk + d.N;
+    return (long long)d.B * ((d.T + kChunk - 1) / kChunk);
+}
+
+struct FactorLayout {
+    size_t w, qg, kt, p, u0, gl, bytes;
+    __host__ __device__ explicit FactorLayout(int dk, int dv) {
+        size_t off = 0;
+        w = off;  off += align256(size_t(kChunk) * dk * 2);
+        qg = off; off += align256(size_t(kChunk) * dk * 2);
+        kt = off; off += align256(size_t(dk) * kChunk * 2);
+        p = off;  off += align256(size_t(kChunk) * kChunk * 2);
+        u0 = off; off += align256(size_t(kChunk) * dv * 2);
+        gl = off; off += align256(size_t(dk) * 4);
+        bytes = off;
+    }
+};
+
+struct WsLayout {
+    size_t header, seq_first, chunks, factors, total;
+    long long cmax;
+    size_t factor_bytes;
+    __host__ __device__ explicit WsLayout(const Dims& d) {
+        cmax = max_chunks(d);
+        FactorLayout f(d.dk, d.dv);
+        factor_bytes = f.bytes;
+        size_t off = 0;
+        header = off;    off += 256;
+        seq_first = off; off += align256(size_t(d.N + 1) * 4);
+        chunks = off;    off += align256(size_t(cmax) * 16);
+        factors = off;   off += size_t(cmax) * d.H * f.bytes;
+        total = off;
+    }
+};
+
+// Element index of (r, k) in an R x K tile stored in the operand layout.
+__host__ __device__ inline int op_index(int r, int k, int R) {
+    return (((k >> 3) * (R >> 3) + (r >> 3)) << 6) + ((r & 7) << 3) + (k & 7);
+}
+
+struct Header {
+    uint32_t error;
+    int32_t total_chunks;
+};
+
+// Raises a kernel's dynamic shared-memory limit once per device (the attribute
+// call is kept out of later calls, which may run under stream capture).
+template <typename Kernel>
+cudaError_t ensure_smem(Kernel kern, size_t bytes) {
+    static std::mutex mu;
+    static uint64_t done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done |= bit;
+    return e;
+}
+
+// Launchers (each enqueues on `stream`; return cudaGetLastError()).
+cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
+                            cudaStream_t stream);
+cudaError_t launch_prep(const Dims& d, bool qkv_bf16, const void* q, const void* k,
+                        const void* v, const float* g, const float* beta, uint8_t* ws,
+                        cudaStream_t stream);
+cudaError_t launch_chain_simt(const Dims& d, bool qkv_bf16, const float* h0, float scale,
+                              void* o, float* hT, uint8_t* ws, cudaStream_t stream);
+
+}  // namespace kda

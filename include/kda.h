@@ -1,0 +1,125 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention prefill forward.
+ *
+ * The operation ("NVIDIA Kernel Design Agents optimize Kimi Delta Attention",
+ * sections 01 RESULTS and 03 REWARD HACKING; "Autoresearch on Kimi Delta
+ * Attention", section THE MECHANISM): for every sequence s and head h, a dk x dv
+ * fp32 state S starts at h0[s,h] (or zero) and, for each token t in order,
+ *     qh = q_t / sqrt(|q_t|^2 + KDA_L2_EPS),  kh = k_t / sqrt(|k_t|^2 + KDA_L2_EPS)
+ *     S  = (I - beta_t kh kh^T) Diag(exp(g_t)) S + beta_t kh v_t^T
+ *     o_t = scale * S^T qh
+ * and hT[s,h] receives the final S.  The library computes this chunkwise (64
+ * tokens per chunk): the state moves from chunk to chunk in order, in fp32; the
+ * work inside a chunk is matrix products on the tensor cores with bf16 operands
+ * and fp32 accumulators.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous:
+ *       q, k : [B, T, H, dk]  (dtype = qkv_dtype)     g : [B, T, H, dk] fp32
+ *       v, o : [B, T, H, dv]  (dtype = qkv_dtype)     beta : [B, T, H] fp32
+ *       h0, hT : [N, H, dk, dv] fp32
+ *   - Fixed length: cu_seqlens == NULL and N == num_seqs == B.
+ *     Varlen: B == 1, T = total tokens, cu_seqlens is a DEVICE int32 array of
+ *     num_seqs + 1 non-decreasing offsets with cu_seqlens[0] == 0 and
+ *     cu_seqlens[num_seqs] == T.  Zero-length sequences are legal (hT = h0).
+ *   - Legal inputs: g <= 0 and finite (any depth: deep decays underflow to zero,
+ *     never overflow); beta in [0, 1]; any sequence length.
+ *   - The caller owns every buffer.  The library allocates no device memory and
+ *     keeps no state between calls other than cached device attributes.  All work
+ *     is enqueued on `stream`; the call returns without synchronising.
+ *   - No exception crosses this boundary and no kernel traps.  Host-side checks
+ *     return a status before anything is launched; conditions only the device can
+ *     see (malformed cu_seqlens) set an error word in the workspace, read back by
+ *     kda_fwd_check().
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (a cudaStream_t); 0 is the legacy default stream. */
+typedef void* kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null required pointer, bad size, non-finite scale */
+    KDA_ERR_UNSUPPORTED = 2,  /* dk or dv not in {64, 128}, unknown dtype */
+    KDA_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned */
+    KDA_ERR_WORKSPACE = 4,    /* workspace null, too small or not 256-byte aligned */
+    KDA_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, attribute, copy) */
+    KDA_ERR_DEVICE = 6        /* the device reported malformed input (kda_fwd_check) */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
+
+/* L2-normalisation epsilon: x / sqrt(sum(x^2) + KDA_L2_EPS).  The pages name the
+ * normalisation of q and k but not its epsilon; 1e-6 is the reading taken. */
+#define KDA_L2_EPS 1e-6f
+
+/* Tokens per chunk of the chunkwise form (fixed). */
+#define KDA_CHUNK 64
+
+/* Device error word bits (kda_fwd_check). */
+#define KDA_DEVERR_CU_SEQLENS 0x1u   /* cu_seqlens not 0-based, decreasing, or != T */
+
+/*
+ * Bytes of device workspace kda_fwd needs for these sizes (0 on bad sizes).
+ * B, T, H: batch, tokens per batch row, heads; num_seqs: N (== B when fixed length).
+ * The workspace holds a schedule of chunks and the per-chunk factors of the
+ * chunkwise form; its contents are scratch and need no initialisation.
+ */
+size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs);
+
+/*
+ * The KDA prefill forward.  Writes o (dtype qkv_dtype) and, when hT is not NULL,
+ * the final states.  h0 may be NULL (zero initial state).  scale multiplies the
+ * output (the usual choice is dk^-1/2).  workspace must be 256-byte aligned and at
+ * least kda_fwd_workspace_size(...) bytes.  q, k, v, g, o must be 16-byte aligned.
+ * Returns KDA_OK once the work is enqueued, or an error status with nothing
+ * enqueued.  Calls that share a workspace must be ordered on one stream.
+ */
+kda_status kda_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                   const float* g, const float* beta, const float* h0,
+                   const int32_t* cu_seqlens, int num_seqs,
+                   int B, int T, int H, int dk, int dv, float scale,
+                   void* o, float* hT,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads the device error word that the last kda_fwd
+ * on this workspace left.  Returns KDA_OK, KDA_ERR_DEVICE (and *device_error gets
+ * the KDA_DEVERR_* bits, if device_error is not NULL) or KDA_ERR_CUDA.
+ */
+kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* device_error);
+
+/* Static, human-readable name of a status. */
+const char* kda_status_string(kda_status status);
+
+/* Number of kernel launches kda_fwd enqueues for these sizes (for launch counts). */
+int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs);
+
+/*
+ * kda_fwd, and in addition cudaEventRecord(events[i], stream) just before its i-th
+ * kernel launch and events[n] after the last one, n = kda_fwd_launch_count(...),
+ * so that a profiler can time each kernel on the stream it runs on.  `events`
+ * holds n + 1 caller-created cudaEvent_t handles.  Same arguments and statuses as
+ * kda_fwd (KDA_ERR_CUDA if an event record fails).
+ */
+kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                            const float* g, const float* beta, const float* h0,
+                            const int32_t* cu_seqlens, int num_seqs,
+                            int B, int T, int H, int dk, int dv, float scale,
+                            void* o, float* hT,
+                            void* workspace, size_t workspace_bytes, kda_stream_t stream,
+                            void* const* events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

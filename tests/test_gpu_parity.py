@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Gates (relative RMSE over the whole tensor): outputs <= 1e-2, final states <= 5e-3.
+Inputs are salted per run (KDA_SALT pins a salt to reproduce a failure).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import gen
+from tests.metrics import HT_TOL, O_TOL, per_sequence_rel_rmse, rel_rmse
+
+pytestmark = pytest.mark.gpu
+
+SALT = gen.fresh_salt()
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_delta_rule_25_gb300 as m
+    return m
+
+
+def _gpu(kda, x, **kw):
+    xd = x.to("cuda")
+    o, hT = kda.fwd(**xd.tensors(), check=True, **kw)
+    torch.cuda.synchronize()
+    return o.cpu(), (hT.cpu() if hT is not None else None)
+
+
+def _assert_parity(x, o, hT, o_tol=O_TOL, h_tol=HT_TOL, heads=None):
+    t = x.tensors()
+    if heads is not None:
+        for key in ("q", "k", "v", "g", "beta"):
+            t[key] = t[key][:, :, heads].contiguous()
+        if t["h0"] is not None:
+            t["h0"] = t["h0"][:, heads].contiguous()
+        o = o[:, :, heads]
+        hT = hT[:, heads] if hT is not None else None
+    o_ref, h_ref = oracle.kda_recurrence_fp64(**t)
+    assert torch.isfinite(o.float()).all(), "non-finite output"
+    eo = rel_rmse(o, o_ref)
+    msg = f"{x.name} salt={x.salt}: o {eo:.3e}"
+    if hT is not None:
+        assert torch.isfinite(hT).all(), "non-finite state"
+        eh = rel_rmse(hT, h_ref)
+        msg += f" hT {eh:.3e}"
+        assert eh <= h_tol, msg
+    assert eo <= o_tol, msg
+    return o_ref, h_ref
+
+
+def test_cfg1_tiny_fp32(kda):
+    x = gen.make_cfg1(seed=1, salt=SALT)
+    o, hT = _gpu(kda, x)
+    assert o.dtype == torch.float32
+    _assert_parity(x, o, hT)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "cfg3", "cfg4"])
+def test_full_size_configs(kda, name):
+    x = {"cfg2": gen.make_cfg2, "cfg3": gen.make_cfg3, "cfg4": gen.make_cfg4}[name](
+        seed=2, salt=SALT)
+    o, hT = _gpu(kda, x)
+    o_ref, _ = _assert_parity(x, o, hT)
+    if x.cu_seqlens is not None:  # no sequence may hide behind the global average
+        per = per_sequence_rel_rmse(o, o_ref, x.seq_lens())
+        assert max(per) <= 5 * O_TOL, per
+
+
+@pytest.mark.parametrize("H,total,varlen", [(16, 32768, False), (64, 8192, True),
+                                            (32, 131072, True)])
+def test_cfg5_sampled_heads(kda, H, total, varlen):
+    x = gen.make_cfg5(H, total, varlen, seed=3, salt=SALT)
+    o, hT = _gpu(kda, x)
+    rng = np.random.default_rng(SALT)
+    heads = sorted(rng.choice(H, size=2, replace=False).tolist())
+    _assert_parity(x, o, hT, heads=heads)
+
+
+@pytest.mark.parametrize("d", [(64, 64), (64, 128), (128, 64), (128, 128)])
+def test_head_dims(kda, d):
+    dk, dv = d
+    x = gen.make_lengths([130, 64, 1, 200], seed=4, salt=SALT, H=3, dk=dk, dv=dv)
+    _assert_parity(x, *_gpu(kda, x))
+
+
+def test_boundary_lengths(kda):
+    x = gen.make_lengths([1, 63, 64, 65, 127, 128, 129, 0, 2], seed=5, salt=SALT, H=2, d=128)
+    _assert_parity(x, *_gpu(kda, x))
+
+
+@pytest.mark.parametrize("kind", gen.PROBES)
+def test_stress_probes(kda, kind):
+    T = 8192 if kind == "long_memory" else 300
+    x = gen.make_probe(kind, seed=6, salt=SALT, T=T, H=2, d=128)
+    _assert_parity(x, *_gpu(kda, x))
+
+
+def test_no_h0_no_hT(kda):
+    x = gen.make_lengths([100, 37], seed=7, salt=SALT, H=2, d=128, h0=False)
+    o, hT = _gpu(kda, x, output_final_state=False)
+    assert hT is None
+    _assert_parity(x, o, None)
+
+
+def test_varlen_equals_independent_sequences(kda):
+    x = gen.make_lengths([70, 1, 200, 64], seed=8, salt=SALT, H=2, d=128)
+    o, hT = _gpu(kda, x)
+    cu = x.cu_seqlens.tolist()
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        xs = gen.KdaInputs("one", x.q[:, a:b].contiguous(), x.k[:, a:b].contiguous(),
+                           x.v[:, a:b].contiguous(), x.g[:, a:b].contiguous(),
+                           x.beta[:, a:b].contiguous(), x.h0[s:s + 1].contiguous(), None,
+                           x.scale)
+        o1, h1 = _gpu(kda, xs)
+        assert torch.equal(o1, o[:, a:b]) and torch.equal(h1[0], hT[s])
+
+
+def test_fixed_batch_equals_varlen(kda):
+    x = gen.make_cfg2(seed=9, salt=SALT, T=200, H=2, B=3)
+    o, hT = _gpu(kda, x)
+    cu = torch.tensor([0, 200, 400, 600], dtype=torch.int32)
+    xv = gen.KdaInputs("v", x.q.reshape(1, 600, 2, 128), x.k.reshape(1, 600, 2, 128),
+                       x.v.reshape(1, 600, 2, 128), x.g.reshape(1, 600, 2, 128),
+                       x.beta.reshape(1, 600, 2), x.h0, cu, x.scale)
+    ov, hv = _gpu(kda, xv)
+    assert torch.equal(ov.reshape(3, 200, 2, 128), o) and torch.equal(hv, hT)
+
+
+@pytest.mark.parametrize("cut", [128, 100])
+def test_split_prefill_equals_whole(kda, cut):
+    x = gen.make_cfg2(seed=10, salt=SALT, T=320, H=2)
+    o, hT = _gpu(kda, x)
+    sl = lambda t, a, b: t[:, a:b].contiguous()  # noqa: E731
+    xa = gen.KdaInputs("a", sl(x.q, 0, cut), sl(x.k, 0, cut), sl(x.v, 0, cut),
+                       sl(x.g, 0, cut), sl(x.beta, 0, cut), x.h0, None, x.scale)
+    oa, ha = _gpu(kda, xa)
+    xb = gen.KdaInputs("b", sl(x.q, cut, 320), sl(x.k, cut, 320), sl(x.v, cut, 320),
+                       sl(x.g, cut, 320), sl(x.beta, cut, 320), ha, None, x.scale)
+    ob, hb = _gpu(kda, xb)
+    ocat = torch.cat([oa, ob], dim=1)
+    if cut % 64 == 0:  # same chunk partition: the same arithmetic
+        assert torch.equal(ocat, o) and torch.equal(hb, hT)
+    else:
+        assert rel_rmse(ocat, o.double()) < O_TOL and rel_rmse(hb, hT.double()) < HT_TOL
+
+
+def test_deterministic(kda):
+    x = gen.make_cfg4(seed=11, salt=SALT, H=4)
+    o1, h1 = _gpu(kda, x)
+    o2, h2 = _gpu(kda, x)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_graph_replay_with_fresh_inputs(kda):
+    """Capture, replay, then swap fresh inputs into the captured buffers and replay
+    again ("NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section 04,
+    CUDA Graph replay checks)."""
+    x1 = gen.make_cfg3(seed=12, salt=SALT, H=4)
+    x2 = gen.make_cfg3(seed=13, salt=SALT + 1, H=4)
+    x2.cu_seqlens = x1.cu_seqlens  # same layout, fresh values
+    x2.h0 = x2.h0[: x1.num_seqs]
+    d1 = x1.to("cuda")
+    ws = torch.empty(kda.workspace_size(1, x1.T, 4, 128, 128, x1.num_seqs) + 256,
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(d1.v)
+    hT = torch.empty_like(d1.h0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        kda.fwd(**d1.tensors(), o=o, hT=hT, workspace=ws)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        kda.fwd(**d1.tensors(), o=o, hT=hT, workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    _assert_parity(x1, o.cpu(), hT.cpu())
+    for name in ("q", "k", "v", "g", "beta", "h0"):
+        getattr(d1, name).copy_(getattr(x2, name).to("cuda"))
+    graph.replay()
+    torch.cuda.synchronize()
+    _assert_parity(x2, o.cpu(), hT.cpu())
+
+
+def test_malformed_cu_seqlens_reports_device_error(kda):
+    x = gen.make_lengths([10, 20, 34], seed=14, salt=SALT, H=2, d=64)
+    bad = torch.tensor([0, 20, 10, 64], dtype=torch.int32)
+    xd = x.to("cuda")
+    xd.cu_seqlens = bad.cuda()
+    with pytest.raises(kda.KdaError) as e:
+        kda.fwd(**xd.tensors(), check=True)
+    assert e.value.status == 6
+    # the context stays usable
+    _assert_parity(x, *_gpu(kda, x))
