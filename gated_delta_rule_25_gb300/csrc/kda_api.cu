@@ -1,9 +1,31 @@
 // C ABI of the KDA prefill forward: argument checks, workspace carving, launches.
 // Declarations and the contract are in include/kda.h.
 #include <cmath>
+#include <cstdlib>
+#include <map>
+#include <mutex>
 
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
+
+namespace kda {
+
+cudaError_t ensure_smem_raw(const void* kern, size_t bytes) {
+    static std::mutex mu;
+    static std::map<const void*, uint64_t> done;  // kernel -> mask of devices set up
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    uint64_t& mask = done[kern];
+    if (bit && (mask & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) mask |= bit;
+    return e;
+}
+
+}  // namespace kda
 
 namespace {
 
@@ -82,9 +104,14 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
     if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (!mark() || kda::launch_prep(d, bf16, q, k, v, g, beta, ws, s) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (!mark() || kda::launch_chain_simt(d, bf16, h0, scale, o, hT, ws, s) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    static const bool simt_chain = [] {
+        const char* e = std::getenv("KDA_DEBUG_SIMT_CHAIN");
+        return e && e[0] == '1';
+    }();
     if (!mark()) return KDA_ERR_CUDA;
+    cudaError_t ce = simt_chain ? kda::launch_chain_simt(d, bf16, h0, scale, o, hT, ws, s)
+                                : kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
+    if (ce != cudaSuccess || !mark()) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

@@ -17,7 +17,7 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int NV = 32;
+constexpr int NV = kNV;
 
 template <int DK>
 struct ChainSmem {
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) chain_simt_kernel(Dims d, const floa
         __syncthreads();
         // U = u - w S
         for (int i = r8; i < kChunk; i += kThreads / NV) {
-            float acc = __bfloat162float(gU[(size_t)i * DV + vt * NV + n]);
+            float acc = __bfloat162float(gU[u0_index(i, vt * NV + n)]);
             for (int cc = 0; cc < DK; ++cc) acc -= sm.Wm[i * DKP + cc] * sm.S[cc * NV + n];
             sm.U[i * NV + n] = acc;
         }

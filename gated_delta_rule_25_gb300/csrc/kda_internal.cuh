@@ -11,7 +11,8 @@
 //   QG  [64 x dk] bf16, operand layout  qh * exp(Gamma)
 //   KT  [dk x 64] bf16, operand layout  (kh * exp(Gamma_last - Gamma))^T
 //   P   [64 x 64] bf16, operand layout  sum_c qh_ic kh_jc exp(Gamma_ic - Gamma_jc), j <= i
-//   U0  [64 x dv] bf16, row-major       u = (I + A)^-1 Diag(beta) v
+//   U0  [dv/32][64][32] bf16            u = (I + A)^-1 Diag(beta) v, in 32-column
+//                                       slabs (one contiguous slab per value tile)
 //   GL  [dk] fp32                       exp(Gamma_last)
 //
 // "Operand layout" is the K-major, unswizzled tensor-core shared-memory layout for
@@ -31,6 +32,16 @@
 namespace kda {
 
 constexpr int kChunk = 64;
+constexpr int kNV = 32;  // value columns per state-recurrence chain
+
+// Device error word bits (mirrors of the KDA_DEVERR_* values of kda.h).
+constexpr unsigned kDevErrCuSeqlens = 0x1u;
+constexpr unsigned kDevErrTimeout = 0x2u;
+
+// Element index of (row r, value column n) in the slabbed U0 block.
+__host__ __device__ inline int u0_index(int r, int n) {
+    return ((n / kNV) * kChunk + r) * kNV + (n % kNV);
+}
 
 struct Dims {
     int B, T, H, dk, dv, N;
@@ -88,19 +99,12 @@ struct Header {
 
 // Raises a kernel's dynamic shared-memory limit once per device (the attribute
 // call is kept out of later calls, which may run under stream capture).
+// Bookkeeping is per kernel (keyed by its address) and per device.
+cudaError_t ensure_smem_raw(const void* kern, size_t bytes);
+
 template <typename Kernel>
 cudaError_t ensure_smem(Kernel kern, size_t bytes) {
-    static std::mutex mu;
-    static uint64_t done = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
-    if (bit && (done & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) done |= bit;
-    return e;
+    return ensure_smem_raw(reinterpret_cast<const void*>(kern), bytes);
 }
 
 // Launchers (each enqueues on `stream`; return cudaGetLastError()).
@@ -109,6 +113,8 @@ cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* w
 cudaError_t launch_prep(const Dims& d, bool qkv_bf16, const void* q, const void* k,
                         const void* v, const float* g, const float* beta, uint8_t* ws,
                         cudaStream_t stream);
+cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
+                         float* hT, uint8_t* ws, cudaStream_t stream);
 cudaError_t launch_chain_simt(const Dims& d, bool qkv_bf16, const float* h0, float scale,
                               void* o, float* hT, uint8_t* ws, cudaStream_t stream);
 

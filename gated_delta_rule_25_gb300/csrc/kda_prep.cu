@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(Dims d, const TIn* __res
         int i = e / DV, cc = e % DV;
         float acc = 0.f;
         for (int j = 0; j <= i; ++j) acc += sm.X[i * AP + j] * sm.vs[j * DVP + cc];
-        gU[(size_t)i * DV + cc] = __float2bfloat16(acc);
+        gU[u0_index(i, cc)] = __float2bfloat16(acc);
     }
 }
 

@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     if (bad) {
         for (int s = tid; s <= d.N; s += kThreads) seq_first[s] = 0;
         if (tid == 0) {
-            hdr->error = 0x1u;
+            hdr->error = kDevErrCuSeqlens;
             hdr->total_chunks = 0;
         }
         return;

@@ -66,6 +66,7 @@ typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
 
 /* Device error word bits (kda_fwd_check). */
 #define KDA_DEVERR_CU_SEQLENS 0x1u   /* cu_seqlens not 0-based, decreasing, or != T */
+#define KDA_DEVERR_TIMEOUT 0x2u      /* a kernel's bounded wait ran out (it left early) */
 
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (0 on bad sizes).
