@@ -44,7 +44,7 @@ struct __align__(128) ChainStage {
 template <int DK>
 struct __align__(128) ChainSmem {
     ChainStage<DK> st[2];
-    __nv_bfloat16 Sop[NV * DK];      // operand layout, NV x DK (B of GEMM1 / GEMM3a)
+    __nv_bfloat16 Sop[2][NV * DK];   // operand layout, NV x DK, two copies (B of GEMM1 / GEMM3a)
     __nv_bfloat16 Uop[NV * kChunk];  // operand layout, NV x 64 (B of GEMM2 / GEMM3b)
     uint64_t full[2], empty[2], d1, d2, d3[2], sready, uready, fin;
     uint32_t tmem_base;
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t sop = ptx::smem_u32(sm.Sop), uop = ptx::smem_u32(sm.Uop);
+            const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
             constexpr uint32_t id_w = ptx::idesc_bf16(64, NV);
             constexpr uint32_t id_k = ptx::idesc_bf16(DK, NV);
             bool ok = true;
@@ -163,27 +163,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t wa = ptx::smem_u32(sm.st[st].W), qa = ptx::smem_u32(sm.st[st].QG);
                 const uint32_t ka = ptx::smem_u32(sm.st[st].KT), pa = ptx::smem_u32(sm.st[st].P);
                 const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
+                const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk)  // D1 = W S
                     ptx::mma_bf16(tmem + kColD1, ptx::smem_desc(wa + kk * 2048, 1024, 128),
                                   ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
                                   id_w, kk > 0);
                 ptx::mma_commit(&sm.d1);
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk)  // D3 = QG S
-                    ptx::mma_bf16(d3, ptx::smem_desc(qa + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_w, kk > 0);
                 ok = ptx::mbar_wait_or_abort(&sm.uready, j & 1, abort);
                 if (!ok) break;
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)  // D2 = KT U
+                for (int kk = 0; kk < kChunk / 16; ++kk)  // D2 = KT U (the serial path)
                     ptx::mma_bf16(tmem + kColD2,
                                   ptx::smem_desc(ka + kk * 2 * (DK / 8) * 128, (DK / 8) * 128, 128),
                                   ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
                                   id_k, kk > 0);
                 ptx::mma_commit(&sm.d2);
+                // the output products are off the serial path: issued after D2.  They
+                // read S copy j & 1; the epilogue writes the next state into the other
+                // copy, and reuses this one only after d2 of chunk j + 1, whose commit
+                // covers these MMAs.
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk)  // D3 = QG S
+                    ptx::mma_bf16(d3, ptx::smem_desc(qa + kk * 2048, 1024, 128),
+                                  ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
+                                  id_w, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)  // D3 += P U
                     ptx::mma_bf16(d3, ptx::smem_desc(pa + kk * 2048, 1024, 128),
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < NV; ++n)
                 S[n] = h0 ? h0[(srow + ch) * DV + vt * NV + n] : 0.f;
 #pragma unroll
-            for (int n = 0; n < NV; ++n) sm.Sop[op_index(n, ch, NV)] = __float2bfloat16(S[n]);
+            for (int n = 0; n < NV; ++n) sm.Sop[0][op_index(n, ch, NV)] = __float2bfloat16(S[n]);
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(&sm.sready);
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int n = 0; n < NV; ++n) {
                     S[n] = fmaf(gl, S[n], acc[n]);
-                    sm.Sop[op_index(n, ch, NV)] = __float2bfloat16(S[n]);
+                    sm.Sop[(j + 1) & 1][op_index(n, ch, NV)] = __float2bfloat16(S[n]);
                 }
             }
             ptx::fence_proxy_async_smem();
