@@ -28,7 +28,9 @@ KDA_OK, KDA_ERR_DEVICE = 0, 6
 KDA_BF16, KDA_FP32 = 0, 1
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size or dtype",
            3: "tensor pointer not 16-byte aligned", 4: "workspace missing, too small or misaligned",
-           5: "CUDA runtime error", 6: "device reported malformed input"}
+           5: "CUDA runtime error", 6: "device reported malformed input",
+           7: "problem too large for the built-in no-allocation scratch"}
+KDA_ERR_TOO_LARGE = 7
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +63,9 @@ def load_library():
         lib.kda_fwd.restype = i32
         lib.kda_fwd_profiled.argtypes = lib.kda_fwd.argtypes + [ctypes.POINTER(vp)]
         lib.kda_fwd_profiled.restype = i32
+        lib.kda_fwd_noalloc.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
+                                        i32, i32, f32, vp, vp, vp]
+        lib.kda_fwd_noalloc.restype = i32
         lib.kda_fwd_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.kda_fwd_check.restype = i32
         lib.kda_status_string.argtypes = [i32]
@@ -170,4 +175,43 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     return o, hT
 
 
-__all__ = ["fwd", "workspace_size", "launch_count", "load_library", "KdaError", "LIB_PATH"]
+def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                beta: torch.Tensor, h0: Optional[torch.Tensor] = None,
+                cu_seqlens: Optional[torch.Tensor] = None, scale: Optional[float] = None, *,
+                o: Optional[torch.Tensor] = None,
+                hT: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The forward through ``kda_fwd_noalloc``: no workspace is passed, the library
+    uses the device scratch array built into it (KDA_NOALLOC_SCRATCH_BYTES, 32 MiB).
+
+    For callers that cannot allocate device memory where they run the forward
+    (a plugin inside an engine that owns all device memory, a path where an
+    allocation's latency or failure is not acceptable): pass preallocated ``o``
+    and ``hT``; the call then allocates nothing.  Problems too large for the
+    array raise KdaError with status KDA_ERR_TOO_LARGE.  Calls share the array,
+    so their work must not overlap on the GPU (order them on one stream)."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name}: must be a contiguous tensor on {dev}")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
+    if hT is None:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if scale is None:
+        scale = dk ** -0.5
+    dt = KDA_BF16 if q.dtype == torch.bfloat16 else KDA_FP32
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib.kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(h0),
+                             _ptr(cu_seqlens), N, B, T, H, dk, dv, float(scale), _ptr(o),
+                             _ptr(hT), ctypes.c_void_p(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_noalloc")
+    return o, hT
+
+
+__all__ = ["fwd", "fwd_noalloc", "workspace_size", "launch_count", "load_library", "KdaError",
+           "LIB_PATH"]

@@ -167,6 +167,7 @@ const char* kda_status_string(kda_status status) {
         case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case KDA_ERR_CUDA: return "CUDA runtime error";
         case KDA_ERR_DEVICE: return "device reported malformed input";
+        case KDA_ERR_TOO_LARGE: return "problem too large for the built-in no-allocation scratch";
     }
     return "unknown status";
 }

@@ -52,7 +52,8 @@ typedef enum {
     KDA_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned */
     KDA_ERR_WORKSPACE = 4,    /* workspace null, too small or not 256-byte aligned */
     KDA_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, attribute, copy) */
-    KDA_ERR_DEVICE = 6        /* the device reported malformed input (kda_fwd_check) */
+    KDA_ERR_DEVICE = 6,       /* the device reported malformed input (kda_fwd_check) */
+    KDA_ERR_TOO_LARGE = 7     /* kda_fwd_noalloc: needs more than KDA_NOALLOC_SCRATCH_BYTES */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
@@ -118,6 +119,44 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
                             void* o, float* hT,
                             void* workspace, size_t workspace_bytes, kda_stream_t stream,
                             void* const* events);
+
+/* Size of the device scratch array built into the library for kda_fwd_noalloc. */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * kda_fwd for callers that cannot allocate device memory.  The pages describe no
+ * such entry point; it exists for users of this library, not for the method.
+ *
+ * Some callers cannot obtain device memory where they run the forward: a plugin
+ * inside a host engine that owns every device allocation, code on a path where
+ * an allocation's latency or failure is not acceptable, or a runtime whose
+ * allocator this library cannot reach.  This entry point takes the same inputs
+ * and outputs as kda_fwd but no workspace: it uses a device array of
+ * KDA_NOALLOC_SCRATCH_BYTES (32 MiB) built into the library, which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Limits and behaviour:
+ *   - Problems whose workspace (kda_fwd_workspace_size) exceeds the array are
+ *     refused with KDA_ERR_TOO_LARGE before anything is launched; at d = 128 the
+ *     array holds about 450 (chunk, head) pairs, e.g. 1,024 tokens x 24 heads.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, and each call's kernels
+ *     overwrite it completely before reading it, so nothing needs clearing
+ *     between calls.  Calls whose work overlaps on the GPU (different streams
+ *     without ordering, or host threads racing) corrupt each other's results:
+ *     order them on one stream.
+ *   - The device error word lives in the built-in array and is not readable here;
+ *     callers that need kda_fwd_check use kda_fwd with their own workspace.
+ * Statuses are kda_fwd's, plus KDA_ERR_TOO_LARGE.
+ */
+kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                           const float* g, const float* beta, const float* h0,
+                           const int32_t* cu_seqlens, int num_seqs,
+                           int B, int T, int H, int dk, int dv, float scale,
+                           void* o, float* hT, kda_stream_t stream);
 
 #ifdef __cplusplus
 }
