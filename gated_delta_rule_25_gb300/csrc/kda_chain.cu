@@ -7,17 +7,19 @@
 // of tokens; "NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section
 // 01 RESULTS: the recurrent state must stay fp32, a bf16 state loses accuracy):
 //   U  = u - w S                                   GEMM1  M=64,  N=32, K=dk
-//   O  = scale ((qh * exp(Gamma)) S + P U)         GEMM3  M=64,  N=32, K=dk + 64
 //   S <- Diag(exp(Gamma_L)) S + KT U               GEMM2  M=dk,  N=32, K=64
-// S lives in fp32 registers of the epilogue warps (one key channel per thread);
-// a bf16 copy of S and of U in shared memory are the B operands of the MMAs,
-// which accumulate in fp32 in tensor memory.
+//   O  = scale ((qh * exp(Gamma)) S + P U)         GEMM3  M=64,  N=32, K=dk + 64
+// S lives in fp32 registers of the four epilogue warps (one key channel per
+// thread).  bf16 copies of S and U in shared memory (N-major) are the B operands
+// of the MMAs, which accumulate in fp32 in tensor memory.
 //
-// Warp roles (192 threads):
-//   warps 0-3  epilogue: TMEM -> registers, U and S updates, output stores
-//              (warp w reads TMEM lanes 32w..32w+31)
-//   warp 4     MMA issue (one thread)
-//   warp 5     bulk copies of the chunk factors (one thread), two stages deep
+// Only GEMM1 and GEMM2 are on the serial path.  Per chunk: thread 0 issues GEMM1;
+// while it runs, the epilogue stores the previous chunk's output; then U is formed
+// from D1, a named barrier, thread 0 issues GEMM2 and GEMM3, S is updated from D2,
+// a named barrier, and the next chunk starts.
+//
+// Warps 0-3: epilogue and MMA issue (warp w reads TMEM lanes 32w..32w+31).
+// Warp 4: bulk copies of the per-chunk factors, three stages deep.
 // Every wait is bounded; a time-out sets KDA_DEVERR_TIMEOUT in the workspace
 // error word and the CTA drains and leaves.
 #include "kda_internal.cuh"
@@ -28,8 +30,10 @@ namespace kda {
 namespace {
 
 constexpr int kEpiThreads = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 160;
+constexpr int kStages = 3;
 constexpr int NV = kNV;
+constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
 
 template <int DK>
 struct __align__(128) ChainStage {
@@ -43,10 +47,10 @@ struct __align__(128) ChainStage {
 
 template <int DK>
 struct __align__(128) ChainSmem {
-    ChainStage<DK> st[2];
-    __nv_bfloat16 Sop[2][NV * DK];   // operand layout, NV x DK, two copies (B of GEMM1 / GEMM3a)
-    __nv_bfloat16 Uop[NV * kChunk];  // operand layout, NV x 64 (B of GEMM2 / GEMM3b)
-    uint64_t full[2], empty[2], d1, d2, d3[2], sready, uready, fin;
+    ChainStage<DK> st[kStages];
+    __nv_bfloat16 Sop[2][NV * DK];   // N-major operand (B of GEMM1 / GEMM3a), two copies
+    __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM2 / GEMM3b)
+    uint64_t full[kStages], empty[kStages], d1, d2, d3[2], fin;
     uint32_t tmem_base;
     int abort;
 };
@@ -54,15 +58,15 @@ struct __align__(128) ChainSmem {
 // TMEM columns: D1 [0, 32), D2 [32, 64), D3 double buffer [64, 128).
 constexpr uint32_t kColD1 = 0, kColD2 = 32, kColD3 = 64, kTmemCols = 128;
 
-template <typename TOut>
-__device__ inline void store_out(TOut* p, float x);
-template <>
-__device__ inline void store_out<__nv_bfloat16>(__nv_bfloat16* p, float x) {
-    *p = __float2bfloat16(x);
+// Element index of (n, k) in an N-major, unswizzled operand with N = 32 rows:
+// 8 x 8 core matrices, 8 consecutive n contiguous, n-blocks fastest.
+__device__ inline int nmaj_index(int n, int k) {
+    return (((k >> 3) * (NV / 8) + (n >> 3)) << 6) + ((k & 7) << 3) + (n & 7);
 }
-template <>
-__device__ inline void store_out<float>(float* p, float x) {
-    *p = x;
+
+__device__ inline uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // Row of an M-row accumulator held by (warp w, lane l) of the epilogue, or -1.
@@ -74,9 +78,47 @@ __device__ inline int acc_row(int w, int l) {
     return l < 16 ? 16 * w + l : -1;
 }
 
+// Named barrier of the 128 epilogue threads that also ANDs a flag across them.
+__device__ inline bool epi_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 __device__ inline void raise_error(uint8_t* ws, volatile int* abort) {
     *abort = 1;
     atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
+}
+
+// Writes 32 output values of one row (bf16 or fp32) with 16-byte stores.
+__device__ inline void store_row(__nv_bfloat16* p, const float (&x)[NV], float scale) {
+#pragma unroll
+    for (int i = 0; i < NV; i += 8) {
+        uint4 u = make_uint4(pack_bf16(scale * x[i], scale * x[i + 1]),
+                             pack_bf16(scale * x[i + 2], scale * x[i + 3]),
+                             pack_bf16(scale * x[i + 4], scale * x[i + 5]),
+                             pack_bf16(scale * x[i + 6], scale * x[i + 7]));
+        *reinterpret_cast<uint4*>(p + i) = u;
+    }
+}
+__device__ inline void store_row(float* p, const float (&x)[NV], float scale) {
+#pragma unroll
+    for (int i = 0; i < NV; i += 4)
+        *reinterpret_cast<float4*>(p + i) =
+            make_float4(scale * x[i], scale * x[i + 1], scale * x[i + 2], scale * x[i + 3]);
+}
+
+__device__ inline void tmem_ld32(uint32_t taddr, float (&x)[NV]) {
+    ptx::tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&x[0]));
+    ptx::tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(&x[16]));
+    ptx::tmem_ld_wait();
 }
 
 template <int DK, int DV, typename TOut>
@@ -99,16 +141,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &sm.abort;
 
     if (tid == 0) {
-        ptx::mbar_init(&sm.full[0], 1);
-        ptx::mbar_init(&sm.full[1], 1);
-        ptx::mbar_init(&sm.empty[0], 1 + 4);
-        ptx::mbar_init(&sm.empty[1], 1 + 4);
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(&sm.full[i], 1);
+            ptx::mbar_init(&sm.empty[i], 2);  // MMA commit + epilogue release
+        }
         ptx::mbar_init(&sm.d1, 1);
         ptx::mbar_init(&sm.d2, 1);
         ptx::mbar_init(&sm.d3[0], 1);
         ptx::mbar_init(&sm.d3[1], 1);
-        ptx::mbar_init(&sm.sready, kEpiThreads);
-        ptx::mbar_init(&sm.uready, kEpiThreads);
         ptx::mbar_init(&sm.fin, 1);
         sm.abort = 0;
         ptx::fence_mbar_init();
@@ -122,15 +162,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 5) {
+    if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint32_t main_bytes = (uint32_t)(F.u0 - F.w);  // W, QG, KT, P back to back
             const uint32_t u_bytes = kChunk * NV * 2, gl_bytes = DK * 4;
             int issued = 0;
             for (int j = 0; j < nch; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !ptx::mbar_wait_or_abort(&sm.empty[st], ((j >> 1) - 1) & 1, abort)) {
+                const int st = j % kStages;
+                if (j >= kStages &&
+                    !ptx::mbar_wait_or_abort(&sm.empty[st], ((j / kStages) - 1) & 1, abort)) {
                     raise_error(ws, abort);
                     break;
                 }
@@ -143,47 +184,115 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (*abort) {  // let copies already in flight land before the CTA leaves
                 volatile int never = 0;
-                for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-                    ptx::mbar_wait_or_abort(&sm.full[j & 1], (j >> 1) & 1, &never);
+                const int first = issued - kStages < 0 ? 0 : issued - kStages;
+                for (int j = first; j < issued; ++j)
+                    ptx::mbar_wait_or_abort(&sm.full[j % kStages], (j / kStages) & 1, &never);
             }
         }
-    } else if (warp == 4) {
-        // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
-            constexpr uint32_t id_w = ptx::idesc_bf16(64, NV);
-            constexpr uint32_t id_k = ptx::idesc_bf16(DK, NV);
-            bool ok = true;
-            for (int j = 0; j < nch && ok; ++j) {
-                const int st = j & 1;
-                ok = ptx::mbar_wait_or_abort(&sm.full[st], (j >> 1) & 1, abort) &&
-                     ptx::mbar_wait_or_abort(&sm.sready, j & 1, abort);
-                if (!ok) break;
+    } else {
+        // ------------------------------------------------ epilogue + MMA issue
+        const int w = warp, l = lane;
+        const uint32_t lane_base = (uint32_t)(32 * w) << 16;
+        const int ch = acc_row<DK>(w, l);     // key channel of this thread's state row
+        const int ur = acc_row<64>(w, l);     // chunk row of this thread in D1 / D3
+        const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
+        constexpr uint32_t id_w = ptx::idesc_bf16(64, NV) | kBMajorMN;
+        constexpr uint32_t id_k = ptx::idesc_bf16(DK, NV) | kBMajorMN;
+        float S[NV];
+        const size_t srow = ((size_t)s * d.H + h) * DK;
+        if (ch >= 0) {
+#pragma unroll
+            for (int n = 0; n < NV; ++n) S[n] = h0 ? h0[(srow + ch) * DV + vt * NV + n] : 0.f;
+#pragma unroll
+            for (int nb = 0; nb < NV; nb += 8)
+                *reinterpret_cast<uint4*>(&sm.Sop[0][nmaj_index(nb, ch)]) =
+                    make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
+                               pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        // Exits are collective: a failed wait in any epilogue thread is folded into
+        // the next named-barrier reduction, so all 128 threads leave the loop at the
+        // same point and none is left waiting at a barrier.
+        bool ok = epi_sync_and(true);
+        int4 prev = make_int4(0, 0, 0, 0);
+        for (int j = 0; j <= nch && ok; ++j) {
+            const int st = j % kStages;
+            bool okl = true;
+            // -------- issue GEMM1 of chunk j: D1 = W S
+            if (j < nch && tid == 0) {
+                okl = ptx::mbar_wait_or_abort(&sm.full[st], (j / kStages) & 1, abort);
+                if (okl) {
+                    ptx::tc_fence_after();
+                    const uint32_t wa = ptx::smem_u32(sm.st[st].W);
+                    const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
+#pragma unroll
+                    for (int kk = 0; kk < DK / 16; ++kk)
+                        ptx::mma_bf16(tmem + kColD1, ptx::smem_desc(wa + kk * 2048, 1024, 128),
+                                      ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
+                                      id_w, kk > 0);
+                    ptx::mma_commit(&sm.d1);
+                }
+            }
+            // -------- output of chunk j - 1 (overlaps GEMM1 of chunk j)
+            if (j > 0) {
+                okl = okl && ptx::mbar_wait_or_abort(&sm.d3[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+                okl = __all_sync(0xffffffffu, okl);
+                if (okl) {
+                    ptx::tc_fence_after();
+                    float acc[NV];
+                    tmem_ld32(tmem + lane_base + kColD3 + (uint32_t)((j - 1) & 1) * NV, acc);
+                    if (ur >= 0 && ur < prev.z)
+                        store_row(o + ((size_t)(prev.y + ur) * d.H + h) * DV + vt * NV, acc, scale);
+                }
+            }
+            if (j == nch) {
+                ok = epi_sync_and(okl);
+                break;
+            }
+            const int4 chk = chunks[c0 + j];
+            // -------- U = u - D1  ->  Uop
+            okl = okl && ptx::mbar_wait_or_abort(&sm.d1, j & 1, abort) &&
+                  ptx::mbar_wait_or_abort(&sm.full[st], (j / kStages) & 1, abort);
+            okl = __all_sync(0xffffffffu, okl);
+            if (okl) {
                 ptx::tc_fence_after();
-                const uint32_t wa = ptx::smem_u32(sm.st[st].W), qa = ptx::smem_u32(sm.st[st].QG);
+                float acc[NV];
+                tmem_ld32(tmem + lane_base + kColD1, acc);
+                if (ur >= 0) {
+                    const uint4* u0 = reinterpret_cast<const uint4*>(sm.st[st].U0 + ur * NV);
+#pragma unroll
+                    for (int nb = 0; nb < NV; nb += 8) {
+                        const uint4 raw = u0[nb / 8];
+                        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                        float2 a = __bfloat1622float2(hb[0]), b = __bfloat1622float2(hb[1]);
+                        float2 c = __bfloat1622float2(hb[2]), e = __bfloat1622float2(hb[3]);
+                        *reinterpret_cast<uint4*>(&sm.Uop[nmaj_index(nb, ur)]) = make_uint4(
+                            pack_bf16(a.x - acc[nb], a.y - acc[nb + 1]),
+                            pack_bf16(b.x - acc[nb + 2], b.y - acc[nb + 3]),
+                            pack_bf16(c.x - acc[nb + 4], c.y - acc[nb + 5]),
+                            pack_bf16(e.x - acc[nb + 6], e.y - acc[nb + 7]));
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ok = epi_sync_and(okl);
+            if (!ok) break;
+            // -------- issue GEMM2 (serial path) then GEMM3 (output)
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t qa = ptx::smem_u32(sm.st[st].QG);
                 const uint32_t ka = ptx::smem_u32(sm.st[st].KT), pa = ptx::smem_u32(sm.st[st].P);
-                const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
                 const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
+                const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
 #pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk)  // D1 = W S
-                    ptx::mma_bf16(tmem + kColD1, ptx::smem_desc(wa + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_w, kk > 0);
-                ptx::mma_commit(&sm.d1);
-                ok = ptx::mbar_wait_or_abort(&sm.uready, j & 1, abort);
-                if (!ok) break;
-                ptx::tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)  // D2 = KT U (the serial path)
+                for (int kk = 0; kk < kChunk / 16; ++kk)  // D2 = KT U
                     ptx::mma_bf16(tmem + kColD2,
                                   ptx::smem_desc(ka + kk * 2 * (DK / 8) * 128, (DK / 8) * 128, 128),
                                   ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
                                   id_k, kk > 0);
                 ptx::mma_commit(&sm.d2);
-                // the output products are off the serial path: issued after D2.  They
-                // read S copy j & 1; the epilogue writes the next state into the other
-                // copy, and reuses this one only after d2 of chunk j + 1, whose commit
-                // covers these MMAs.
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk)  // D3 = QG S
                     ptx::mma_bf16(d3, ptx::smem_desc(qa + kk * 2048, 1024, 128),
@@ -197,90 +306,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_commit(&sm.d3[j & 1]);
                 ptx::mma_commit(&sm.empty[st]);
             }
-            if (!ok) raise_error(ws, abort);
-            // all issued MMAs complete before TMEM is released
-            ptx::mma_commit(&sm.fin);
-            volatile int never = 0;
-            ptx::mbar_wait_or_abort(&sm.fin, 0, &never);
-        }
-    } else {
-        // ------------------------------------------------------------ epilogue
-        const int w = warp, l = lane;
-        const uint32_t lane_base = (uint32_t)(32 * w) << 16;
-        const int ch = acc_row<DK>(w, l);     // key channel of this thread's state row
-        const int ur = acc_row<64>(w, l);     // chunk row of this thread in D1 / D3
-        float S[NV];
-        const size_t srow = ((size_t)s * d.H + h) * DK;
-        if (ch >= 0) {
+            // -------- S <- GL * S + D2  ->  Sop[(j + 1) & 1]
+            okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&sm.d2, j & 1, abort));
+            if (okl) {
+                ptx::tc_fence_after();
+                float acc[NV];
+                tmem_ld32(tmem + lane_base + kColD2, acc);
+                if (ch >= 0) {
+                    const float gl = sm.st[st].GL[ch];
+                    __nv_bfloat16* so = sm.Sop[(j + 1) & 1];
 #pragma unroll
-            for (int n = 0; n < NV; ++n)
-                S[n] = h0 ? h0[(srow + ch) * DV + vt * NV + n] : 0.f;
+                    for (int nb = 0; nb < NV; nb += 8) {
 #pragma unroll
-            for (int n = 0; n < NV; ++n) sm.Sop[0][op_index(n, ch, NV)] = __float2bfloat16(S[n]);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(&sm.sready);
-        bool ok = true;
-        for (int j = 0; j < nch; ++j) {
-            const int st = j & 1;
-            const int4 chk = chunks[c0 + j];
-            float acc[NV];
-            // (a) U = u - W S
-            ok = ptx::mbar_wait_or_abort(&sm.d1, j & 1, abort) &&
-                 ptx::mbar_wait_or_abort(&sm.full[st], (j >> 1) & 1, abort);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            ptx::tmem_ld16(tmem + lane_base + kColD1, *reinterpret_cast<float(*)[16]>(&acc[0]));
-            ptx::tmem_ld16(tmem + lane_base + kColD1 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
-            ptx::tmem_ld_wait();
-            if (ur >= 0) {
-                const __nv_bfloat16* u0 = sm.st[st].U0 + ur * NV;
-#pragma unroll
-                for (int n = 0; n < NV; ++n)
-                    sm.Uop[op_index(n, ur, NV)] = __float2bfloat16(__bfloat162float(u0[n]) - acc[n]);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&sm.uready);
-            // (b) S <- GL * S + KT U
-            ok = ptx::mbar_wait_or_abort(&sm.d2, j & 1, abort);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            ptx::tmem_ld16(tmem + lane_base + kColD2, *reinterpret_cast<float(*)[16]>(&acc[0]));
-            ptx::tmem_ld16(tmem + lane_base + kColD2 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
-            ptx::tmem_ld_wait();
-            if (ch >= 0) {
-                const float gl = sm.st[st].GL[ch];
-#pragma unroll
-                for (int n = 0; n < NV; ++n) {
-                    S[n] = fmaf(gl, S[n], acc[n]);
-                    sm.Sop[(j + 1) & 1][op_index(n, ch, NV)] = __float2bfloat16(S[n]);
+                        for (int e = 0; e < 8; ++e) S[nb + e] = fmaf(gl, S[nb + e], acc[nb + e]);
+                        *reinterpret_cast<uint4*>(&so[nmaj_index(nb, ch)]) =
+                            make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
+                                       pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
+                    }
                 }
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&sm.sready);
-            __syncwarp();
-            if (l == 0) ptx::mbar_arrive(&sm.empty[st]);
-            // (c) O = scale * D3
-            ok = ptx::mbar_wait_or_abort(&sm.d3[j & 1], (j >> 1) & 1, abort);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint32_t d3 = tmem + lane_base + kColD3 + (uint32_t)(j & 1) * NV;
-            ptx::tmem_ld16(d3, *reinterpret_cast<float(*)[16]>(&acc[0]));
-            ptx::tmem_ld16(d3 + 16, *reinterpret_cast<float(*)[16]>(&acc[16]));
-            ptx::tmem_ld_wait();
-            ptx::tc_fence_before();
-            if (ur >= 0 && ur < chk.z) {
-                TOut* orow = o + ((size_t)(chk.y + ur) * d.H + h) * DV + vt * NV;
-#pragma unroll
-                for (int n = 0; n < NV; ++n) store_out<TOut>(orow + n, scale * acc[n]);
-            }
+            ok = epi_sync_and(okl);
+            if (ok && tid == 0) ptx::mbar_arrive(&sm.empty[st]);  // U0, GL of this stage read
+            prev = chk;
         }
         if (!ok) raise_error(ws, abort);
         if (hT && ch >= 0) {
 #pragma unroll
-            for (int n = 0; n < NV; ++n) hT[(srow + ch) * DV + vt * NV + n] = S[n];
+            for (int n = 0; n < NV; n += 4)
+                *reinterpret_cast<float4*>(&hT[(srow + ch) * DV + vt * NV + n]) =
+                    make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
+        }
+        if (tid == 0) {  // every issued MMA completes before TMEM is released
+            volatile int never = 0;
+            ptx::mma_commit(&sm.fin);
+            ptx::mbar_wait_or_abort(&sm.fin, 0, &never);
         }
     }
     ptx::tc_fence_before();
