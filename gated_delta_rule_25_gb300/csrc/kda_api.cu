@@ -25,6 +25,21 @@ cudaError_t ensure_smem_raw(const void* kern, size_t bytes) {
     return e;
 }
 
+int num_sms() {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 1;
+    cache[dev] = n;
+    return n;
+}
+
 }  // namespace kda
 
 namespace {

@@ -15,11 +15,12 @@
 //
 // Only GEMM1 and GEMM2 are on the serial path.  Per chunk: thread 0 issues GEMM1;
 // while it runs, the epilogue stores the previous chunk's output; then U is formed
-// from D1, a named barrier, thread 0 issues GEMM2 and GEMM3, S is updated from D2,
-// a named barrier, and the next chunk starts.
+// from D1, a named barrier, thread 0 issues GEMM2 (and signals warp 5, which
+// issues GEMM3), S is updated from D2, a named barrier, and the next chunk starts.
 //
-// Warps 0-3: epilogue and MMA issue (warp w reads TMEM lanes 32w..32w+31).
+// Warps 0-3: epilogue, GEMM1/GEMM2 issue (warp w reads TMEM lanes 32w..32w+31).
 // Warp 4: bulk copies of the per-chunk factors, three stages deep.
+// Warp 5: GEMM3 issue (output products, off the serial path).
 // Every wait is bounded; a time-out sets KDA_DEVERR_TIMEOUT in the workspace
 // error word and the CTA drains and leaves.
 #include "kda_internal.cuh"
@@ -29,8 +30,7 @@ namespace kda {
 
 namespace {
 
-constexpr int kEpiThreads = 128;
-constexpr int kThreads = 160;
+constexpr int kThreads = 192;
 constexpr int kStages = 3;
 constexpr int NV = kNV;
 constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
@@ -50,7 +50,7 @@ struct __align__(128) ChainSmem {
     ChainStage<DK> st[kStages];
     __nv_bfloat16 Sop[2][NV * DK];   // N-major operand (B of GEMM1 / GEMM3a), two copies
     __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM2 / GEMM3b)
-    uint64_t full[kStages], empty[kStages], d1, d2, d3[2], fin;
+    uint64_t full[kStages], empty[kStages], d1, d2, d3[2], uready, fin, fin3;
     uint32_t tmem_base;
     int abort;
 };
@@ -143,13 +143,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&sm.full[i], 1);
-            ptx::mbar_init(&sm.empty[i], 2);  // MMA commit + epilogue release
+            ptx::mbar_init(&sm.empty[i], 3);  // two MMA commits + epilogue release
         }
         ptx::mbar_init(&sm.d1, 1);
         ptx::mbar_init(&sm.d2, 1);
         ptx::mbar_init(&sm.d3[0], 1);
         ptx::mbar_init(&sm.d3[1], 1);
+        ptx::mbar_init(&sm.uready, 1);
         ptx::mbar_init(&sm.fin, 1);
+        ptx::mbar_init(&sm.fin3, 1);
         sm.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -188,6 +190,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = first; j < issued; ++j)
                     ptx::mbar_wait_or_abort(&sm.full[j % kStages], (j / kStages) & 1, &never);
             }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ GEMM3 issue
+        if (lane == 0) {
+            const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
+            constexpr uint32_t id_w = ptx::idesc_bf16(64, NV) | kBMajorMN;
+            for (int j = 0; j < nch; ++j) {
+                const int st = j % kStages;
+                if (!ptx::mbar_wait_or_abort(&sm.uready, j & 1, abort)) break;
+                ptx::tc_fence_after();
+                const uint32_t qa = ptx::smem_u32(sm.st[st].QG), pa = ptx::smem_u32(sm.st[st].P);
+                const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
+                const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk)  // D3 = QG S
+                    ptx::mma_bf16(d3, ptx::smem_desc(qa + kk * 2048, 1024, 128),
+                                  ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
+                                  id_w, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk)  // D3 += P U
+                    ptx::mma_bf16(d3, ptx::smem_desc(pa + kk * 2048, 1024, 128),
+                                  ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
+                                  id_w, true);
+                ptx::mma_commit(&sm.d3[j & 1]);
+                ptx::mma_commit(&sm.empty[st]);
+            }
+            volatile int never = 0;  // its MMAs complete before TMEM is released
+            ptx::mma_commit(&sm.fin3);
+            ptx::mbar_wait_or_abort(&sm.fin3, 0, &never);
         }
     } else {
         // ------------------------------------------------ epilogue + MMA issue
@@ -279,13 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             ok = epi_sync_and(okl);
             if (!ok) break;
-            // -------- issue GEMM2 (serial path) then GEMM3 (output)
+            // -------- issue GEMM2 (serial path); warp 5 issues GEMM3 (output)
             if (tid == 0) {
                 ptx::tc_fence_after();
-                const uint32_t qa = ptx::smem_u32(sm.st[st].QG);
-                const uint32_t ka = ptx::smem_u32(sm.st[st].KT), pa = ptx::smem_u32(sm.st[st].P);
-                const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
-                const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
+                ptx::mbar_arrive(&sm.uready);
+                const uint32_t ka = ptx::smem_u32(sm.st[st].KT);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)  // D2 = KT U
                     ptx::mma_bf16(tmem + kColD2,
@@ -293,17 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
                                   id_k, kk > 0);
                 ptx::mma_commit(&sm.d2);
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk)  // D3 = QG S
-                    ptx::mma_bf16(d3, ptx::smem_desc(qa + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_w, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)  // D3 += P U
-                    ptx::mma_bf16(d3, ptx::smem_desc(pa + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_w, true);
-                ptx::mma_commit(&sm.d3[j & 1]);
                 ptx::mma_commit(&sm.empty[st]);
             }
             // -------- S <- GL * S + D2  ->  Sop[(j + 1) & 1]

@@ -102,6 +102,9 @@ struct Header {
 // Bookkeeping is per kernel (keyed by its address) and per device.
 cudaError_t ensure_smem_raw(const void* kern, size_t bytes);
 
+// Number of SMs of the current device (cached per device; 152 on GB300).
+int num_sms();
+
 template <typename Kernel>
 cudaError_t ensure_smem(Kernel kern, size_t bytes) {
     return ensure_smem_raw(reinterpret_cast<const void*>(kern), bytes);

@@ -1,5 +1,5 @@
 // Per-chunk factors of the chunkwise KDA forward on tensor cores: one CTA per
-// (chunk, head), 256 threads.
+// (chunk, head), 512 threads.
 //
 // For a chunk of L <= 64 tokens of one sequence and head ("Autoresearch on Kimi
 // Delta Attention", section THE MECHANISM: inside a block the work becomes matrix
@@ -32,7 +32,7 @@ namespace kda {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 
 template <int DK, int DV>
 struct __align__(128) PrepSmem {
@@ -57,7 +57,7 @@ struct __align__(128) PrepSmem {
             __nv_bfloat16 xop[kChunk * kChunk];        // X Diag(beta), operand layout
             __nv_bfloat16 bop[(DK + DV) * kChunk];     // [kh*gamma | v]^T, operand layout
         } t;
-        float scratch[3 * 16 * 16];
+        float scratch[32 * 32];
     } ops;
     float bs[kChunk];
     uint64_t bar;
@@ -109,6 +109,23 @@ __device__ inline uint32_t lds_pair(const __nv_bfloat16* t, int row, int k) {
     return *reinterpret_cast<const uint32_t*>(t + sw<DK>(row, k));
 }
 
+// Packed fp32x2 arithmetic (two lanes of work per instruction).
+__device__ inline float2 mul2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+    return *reinterpret_cast<float2*>(&r);
+}
+__device__ inline float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
+          "l"(*reinterpret_cast<unsigned long long*>(&c)));
+    return *reinterpret_cast<float2*>(&r);
+}
+
 __device__ inline void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
@@ -117,11 +134,53 @@ __device__ inline void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Joins pairs of inverted n x n diagonal blocks of X = (I + A)^-1 (row stride
+// kChunk + 1): X21 = -X22 (A21 X11).  Upper triangles of X are zero, so the
+// products run over full blocks.  Ends with the CTA synchronised.
+template <int N>
+__device__ __forceinline__ void inv_join(float* X, const float* A, float* T, int tid) {
+    constexpr int AP = kChunk + 1;
+    constexpr int OUT = (kChunk / (2 * N)) * N * N;
+    constexpr int PER = (OUT + kThreads - 1) / kThreads;
+#pragma unroll
+    for (int qq = 0; qq < PER; ++qq) {
+        const int e = tid + qq * kThreads;
+        if (e < OUT) {
+            const int pidx = e / (N * N), i = (e / N) % N, j = e % N;
+            const int r1 = 2 * pidx * N, r2 = r1 + N;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < N; m += 2) {
+                a0 = fmaf(A[(r2 + i) * AP + r1 + m], X[(r1 + m) * AP + r1 + j], a0);
+                a1 = fmaf(A[(r2 + i) * AP + r1 + m + 1], X[(r1 + m + 1) * AP + r1 + j], a1);
+            }
+            T[e] = a0 + a1;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int qq = 0; qq < PER; ++qq) {
+        const int e = tid + qq * kThreads;
+        if (e < OUT) {
+            const int pidx = e / (N * N), i = (e / N) % N, j = e % N;
+            const int r1 = 2 * pidx * N, r2 = r1 + N;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < N; m += 2) {
+                a0 = fmaf(X[(r2 + i) * AP + r2 + m], T[pidx * N * N + m * N + j], a0);
+                a1 = fmaf(X[(r2 + i) * AP + r2 + m + 1], T[pidx * N * N + (m + 1) * N + j], a1);
+            }
+            X[(r2 + i) * AP + r1 + j] = -(a0 + a1);
+        }
+    }
+    __syncthreads();
+}
+
 template <int DK, int DV, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(Dims d, const TIn* __restrict__ q, const TIn* __restrict__ k,
                    const TIn* __restrict__ v, const float* __restrict__ g,
-                   const float* __restrict__ beta, uint8_t* __restrict__ ws) {
+                   const float* __restrict__ beta, uint8_t* __restrict__ ws, int nsm) {
     using Sm = PrepSmem<DK, DV>;
     constexpr int AP = kChunk + 1;
     constexpr int NB = DK + DV;  // columns of the w/u product
@@ -159,28 +218,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- P1: load
     // 16-byte chunks: consecutive lanes take consecutive chunks of a row, so the
     // shared-memory stores are conflict free and a row's lanes reduce its norm.
+    // Every load of the thread is issued before any is used (one DRAM latency).
     {
         constexpr int CPR = DK / 8;            // chunks per row
         constexpr int RP = kThreads / CPR;     // rows per pass
+        constexpr int NP = kChunk / RP;        // passes
+        constexpr int VPR = DV / 8;
+        constexpr int VRP = kThreads / VPR;
+        constexpr int NVP = kChunk / VRP;
         const int ck = tid % CPR, rsub = tid / CPR;
-#pragma unroll 1
-        for (int r = rsub; r < kChunk; r += RP) {
-            const bool valid = r < L;
-            const size_t off = ((size_t)(row0 + r) * H + h) * DK + ck * 8;
-            float xq[8], xk[8], xg[8];
-            if (valid) {
-                load8<TIn>(q + off, xq);
-                load8<TIn>(k + off, xk);
-                load8<float>(g + off, xg);
+        const int vk = tid % VPR, vsub = tid / VPR;
+        float xq[NP][8], xk[NP][8], xg[NP][8], xv[NVP][8];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = rsub + p * RP;
+            if (r < L) {
+                const size_t off = ((size_t)(row0 + r) * H + h) * DK + ck * 8;
+                load8<TIn>(q + off, xq[p]);
+                load8<TIn>(k + off, xk[p]);
+                load8<float>(g + off, xg[p]);
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xq[e] = xk[e] = xg[e] = 0.f;
+                for (int e = 0; e < 8; ++e) xq[p][e] = xk[p][e] = xg[p][e] = 0.f;
             }
+        }
+#pragma unroll
+        for (int p = 0; p < NVP; ++p) {
+            const int r = vsub + p * VRP;
+            if (r < L) load8<TIn>(v + ((size_t)(row0 + r) * H + h) * DV + vk * 8, xv[p]);
+            else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[p][e] = 0.f;
+            }
+        }
+        const float bt = (tid < kChunk && tid < L) ? beta[(size_t)(row0 + tid) * H + h] : 0.f;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = rsub + p * RP;
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                sq = fmaf(xq[e], xq[e], sq);
-                sk = fmaf(xk[e], xk[e], sk);
+                sq = fmaf(xq[p][e], xq[p][e], sq);
+                sk = fmaf(xk[p][e], xk[p][e], sk);
             }
 #pragma unroll
             for (int o = 1; o < CPR; o <<= 1) {
@@ -191,122 +270,182 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* dq = &sm.qn[r * DK + ck * 8];
             float* dk_ = &sm.kn[r * DK + ck * 8];
             float* da = &sm.al[r * DK + ck * 8];
-            *reinterpret_cast<float4*>(dq) = make_float4(xq[0] * iq, xq[1] * iq, xq[2] * iq, xq[3] * iq);
-            *reinterpret_cast<float4*>(dq + 4) = make_float4(xq[4] * iq, xq[5] * iq, xq[6] * iq, xq[7] * iq);
-            *reinterpret_cast<float4*>(dk_) = make_float4(xk[0] * ik, xk[1] * ik, xk[2] * ik, xk[3] * ik);
-            *reinterpret_cast<float4*>(dk_ + 4) = make_float4(xk[4] * ik, xk[5] * ik, xk[6] * ik, xk[7] * ik);
-            *reinterpret_cast<float4*>(da) = make_float4(__expf(xg[0]), __expf(xg[1]), __expf(xg[2]), __expf(xg[3]));
-            *reinterpret_cast<float4*>(da + 4) = make_float4(__expf(xg[4]), __expf(xg[5]), __expf(xg[6]), __expf(xg[7]));
-        }
-        constexpr int VPR = DV / 8;
-        constexpr int VRP = kThreads / VPR;
-        const int vk = tid % VPR, vsub = tid / VPR;
-#pragma unroll 1
-        for (int r = vsub; r < kChunk; r += VRP) {
-            float xv[8];
-            if (r < L) load8<TIn>(v + ((size_t)(row0 + r) * H + h) * DV + vk * 8, xv);
-            else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+            for (int e = 0; e < 8; e += 4) {
+                *reinterpret_cast<float4*>(dq + e) = make_float4(xq[p][e] * iq, xq[p][e + 1] * iq,
+                                                                 xq[p][e + 2] * iq, xq[p][e + 3] * iq);
+                *reinterpret_cast<float4*>(dk_ + e) = make_float4(xk[p][e] * ik, xk[p][e + 1] * ik,
+                                                                  xk[p][e + 2] * ik, xk[p][e + 3] * ik);
+                *reinterpret_cast<float4*>(da + e) =
+                    make_float4(__expf(xg[p][e]), __expf(xg[p][e + 1]), __expf(xg[p][e + 2]),
+                                __expf(xg[p][e + 3]));
             }
-            *reinterpret_cast<uint4*>(&sm.vs[r * DV + vk * 8]) = pack8(xv);
         }
-        if (tid < kChunk) sm.bs[tid] = tid < L ? beta[(size_t)(row0 + tid) * H + h] : 0.f;
+#pragma unroll
+        for (int p = 0; p < NVP; ++p)
+            *reinterpret_cast<uint4*>(&sm.vs[(vsub + p * VRP) * DV + vk * 8]) = pack8(xv[p]);
+        if (tid < kChunk) sm.bs[tid] = bt;
     }
     __syncthreads();
 
-    // ------------------------------------------------ P2: decay products per channel
-    if (tid < DK) {
-        // forward: gamma prefix (QG, GL), row factors of the mma operands
-        const int ch = tid;
-        float gp = 1.f, p16 = 1.f, p8 = 1.f;
-        for (int r = 0; r < kChunk; ++r) {
-            const float a = sm.al[r * DK + ch];
-            gp *= a;
-            const int ri = r & 15;
-            p16 = ri == 0 ? 1.f : p16 * a;
-            p8 = ri == 8 ? 1.f : p8 * a;
-            const float kq = sm.kn[r * DK + ch], qq = sm.qn[r * DK + ch];
-            if (r >= 16) {
-                sm.ops.m.left[sw<DK>(r - 16, ch)] = __float2bfloat16(kq * p16);
-                sm.ops.m.leftq[sw<DK>(r - 16, ch)] = __float2bfloat16(qq * p16);
-            }
-            if (ri >= 8) {
-                const int rr = (r >> 4) * 8 + (ri - 8);
-                sm.ops.m.l8[sw<DK>(rr, ch)] = __float2bfloat16(kq * p8);
-                sm.ops.m.l8q[sw<DK>(rr, ch)] = __float2bfloat16(qq * p8);
-            }
-            gQG[op_index(r, ch, kChunk)] = __float2bfloat16(qq * gp);
-        }
-        gGL[ch] = gp;
-    } else if (tid < 2 * DK) {
-        // backward: suffix products (KT), column factors of the mma operands
-        const int ch = tid - DK;
-        float suf = 1.f;
-        for (int rb = kChunk - 8; rb >= 0; rb -= 8) {
-            float x[8];
-#pragma unroll
-            for (int e = 7; e >= 0; --e) {
-                const int r = rb + e;
-                x[e] = sm.kn[r * DK + ch] * suf;
-                suf *= sm.al[r * DK + ch];
-            }
-            *reinterpret_cast<uint4*>(&gKT[op_index(ch, rb, DK)]) = pack8(x);
-        }
-        // 16-level column factors: f_m(j) = D(m, j) for anchors m = 16, 32, 48
-        float f16[16], f32[16], f48[16];
-        {
-            float f = 1.f;
-#pragma unroll
-            for (int j = 15; j >= 0; --j) { f *= sm.al[(j + 1) * DK + ch]; f16[j] = f; }
-            f = 1.f;
-#pragma unroll
-            for (int j = 15; j >= 0; --j) { f *= sm.al[(j + 17) * DK + ch]; f32[j] = f; }
-            f = 1.f;
-#pragma unroll
-            for (int j = 15; j >= 0; --j) { f *= sm.al[(j + 33) * DK + ch]; f48[j] = f; }
-        }
-        const float d1632 = f32[0], d3248 = f48[0];  // D(32, 16), D(48, 32)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float k0 = sm.kn[j * DK + ch], k1 = sm.kn[(j + 16) * DK + ch];
-            const float k2 = sm.kn[(j + 32) * DK + ch];
-            sm.ops.m.right[sw<DK>(j, ch)] = __float2bfloat16(k0 * f16[j]);                   // R=1
-            sm.ops.m.right[sw<DK>(16 + j, ch)] = __float2bfloat16(k0 * f16[j] * d1632);       // R=2
-            sm.ops.m.right[sw<DK>(32 + j, ch)] = __float2bfloat16(k1 * f32[j]);
-            sm.ops.m.right[sw<DK>(48 + j, ch)] = __float2bfloat16(k0 * f16[j] * d1632 * d3248);  // R=3
-            sm.ops.m.right[sw<DK>(64 + j, ch)] = __float2bfloat16(k1 * f32[j] * d3248);
-            sm.ops.m.right[sw<DK>(80 + j, ch)] = __float2bfloat16(k2 * f48[j]);
-        }
-        // 8-level column factors: D(16R+8, j), j in [16R, 16R+8)
-#pragma unroll
-        for (int R = 0; R < 4; ++R) {
-            float f = 1.f;
-#pragma unroll
-            for (int e = 7; e >= 0; --e) {
-                const int j = 16 * R + e;
-                f *= sm.al[(j + 1) * DK + ch];
-                sm.ops.m.r8[sw<DK>(8 * R + e, ch)] = __float2bfloat16(sm.kn[j * DK + ch] * f);
+    // Warm L2 with the inputs of the CTA one wave ahead (it runs next on some SM),
+    // so that its loads do not all hit DRAM at the same moment as this wave's.
+    {
+        const long long lin = (long long)blockIdx.y * gridDim.x + blockIdx.x + nsm;
+        if (lin < (long long)gridDim.x * gridDim.y) {
+            const int cx = (int)(lin % gridDim.x), hy = (int)(lin / gridDim.x);
+            if (cx < hdr->total_chunks) {
+                const int4 nk = reinterpret_cast<const int4*>(ws + W.chunks)[cx];
+                constexpr int LQ = DK * (int)sizeof(TIn) / 128, LG = DK * 4 / 128;
+                constexpr int LV = DV * (int)sizeof(TIn) / 128, LR = 2 * LQ + LG + LV;
+                for (int e = tid; e < nk.z * LR; e += kThreads) {
+                    const int r = e / LR, li = e % LR;
+                    const size_t row = (size_t)(nk.y + r) * H + hy;
+                    const char* p;
+                    if (li < LQ) p = reinterpret_cast<const char*>(q + row * DK) + li * 128;
+                    else if (li < 2 * LQ) p = reinterpret_cast<const char*>(k + row * DK) + (li - LQ) * 128;
+                    else if (li < 2 * LQ + LG) p = reinterpret_cast<const char*>(g + row * DK) + (li - 2 * LQ) * 128;
+                    else p = reinterpret_cast<const char*>(v + row * DV) + (li - 2 * LQ - LG) * 128;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+                }
             }
         }
+    }
+
+    // ------------------------------------------------ P2: decay products
+    // Every decay factor used below is a product of alpha over a run of rows.  The
+    // rows split into eight 8-row blocks; per (block b, channel) the local forward
+    // products f_r = alpha(8b+1..r) and backward products g_r = alpha(r+1..8b+7)
+    // are formed in registers, and per channel a handful of block scalars join
+    // them: Gb_b = alpha(0..8b), Sb_b = alpha(8b+8..63), M(b, R) = alpha(8b+8..16R).
+    {
+        float* Bi = sm.X;                 // inner block products alpha(8b+1..8b+7) [8][DK]
+        float* Gb = sm.X + 8 * DK;        // [8][DK]
+        float* Sb = sm.X + 16 * DK;       // [8][DK]
+        float* Mt = sm.A;                 // M(b, R): 2 + 4 + 6 rows of [DK]
+        constexpr int TPB = kThreads / DK;   // tasks per block pass
+        // (a) inner products of every block
+        for (int e = tid; e < 8 * DK; e += kThreads) {
+            const int bb = e / DK, ch = e % DK;
+            float pr = 1.f;
+#pragma unroll
+            for (int u = 1; u < 8; ++u) pr *= sm.al[(8 * bb + u) * DK + ch];
+            Bi[bb * DK + ch] = pr;
+        }
+        __syncthreads();
+        // (b) per-channel block scalars
+        if (tid < DK) {
+            const int ch = tid;
+            float a[8], bi[8];
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb) {
+                a[bb] = sm.al[(8 * bb) * DK + ch];
+                bi[bb] = Bi[bb * DK + ch];
+            }
+            float gp = a[0];
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb) {
+                if (bb > 0) gp *= bi[bb - 1] * a[bb];
+                Gb[bb * DK + ch] = gp;
+            }
+            gGL[ch] = gp * bi[7];
+            float sp = 1.f;
+#pragma unroll
+            for (int bb = 7; bb >= 0; --bb) {
+                Sb[bb * DK + ch] = sp;
+                sp *= a[bb] * bi[bb];
+            }
+            int row = 0;
+#pragma unroll
+            for (int R = 1; R <= 3; ++R) {  // M(b, R) for b = 2R-1 .. 0
+                float m = a[2 * R];
+#pragma unroll
+                for (int bb = 2 * R - 1; bb >= 0; --bb) {
+                    Mt[(row + bb) * DK + ch] = m;
+                    m *= bi[bb] * a[bb];
+                }
+                row += 2 * R;
+            }
+        }
+        __syncthreads();
+        // (c) per (block, channel): local products, then every operand row
+        for (int e = tid; e < 8 * DK; e += kThreads) {
+            const int bb = e / DK, ch = e % DK;
+            const int r0 = 8 * bb;
+            float al[8], kq[8], qq[8], f[8], gq[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                al[u] = sm.al[(r0 + u) * DK + ch];
+                kq[u] = sm.kn[(r0 + u) * DK + ch];
+                qq[u] = sm.qn[(r0 + u) * DK + ch];
+            }
+            f[0] = 1.f;
+#pragma unroll
+            for (int u = 1; u < 8; ++u) f[u] = f[u - 1] * al[u];
+            gq[7] = 1.f;
+#pragma unroll
+            for (int u = 6; u >= 0; --u) gq[u] = gq[u + 1] * al[u + 1];
+            const float gb = Gb[bb * DK + ch], sb = Sb[bb * DK + ch];
+            // QG = qh * gamma (global, operand layout) and KT = (kh * gamma_L / gamma)^T
+            float kt[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                gQG[op_index(r0 + u, ch, kChunk)] = __float2bfloat16(qq[u] * gb * f[u]);
+                kt[u] = kq[u] * gq[u] * sb;
+            }
+            *reinterpret_cast<uint4*>(&gKT[op_index(ch, r0, DK)]) = pack8(kt);
+            const int R = bb >> 1;
+            if (bb >= 2) {  // 16-level row factors D(r, 16R)
+                const float pre = (bb & 1) ? Bi[(2 * R) * DK + ch] * sm.al[(16 * R + 8) * DK + ch] : 1.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int rr = r0 + u - 16;
+                    sm.ops.m.left[sw<DK>(rr, ch)] = __float2bfloat16(kq[u] * pre * f[u]);
+                    sm.ops.m.leftq[sw<DK>(rr, ch)] = __float2bfloat16(qq[u] * pre * f[u]);
+                }
+            }
+            if (bb & 1) {  // 8-level row factors D(r, 16R+8)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    sm.ops.m.l8[sw<DK>(8 * R + u, ch)] = __float2bfloat16(kq[u] * f[u]);
+                    sm.ops.m.l8q[sw<DK>(8 * R + u, ch)] = __float2bfloat16(qq[u] * f[u]);
+                }
+            } else {       // 8-level column factors D(16R+8, j) = g_j alpha(16R+8)
+                const float a8 = sm.al[(16 * R + 8) * DK + ch];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    sm.ops.m.r8[sw<DK>(8 * R + u, ch)] = __float2bfloat16(kq[u] * gq[u] * a8);
+            }
+            // 16-level column factors D(16R', j) for every R' with 16R' > j
+            int mrow = 0, rbase = 0;
+#pragma unroll
+            for (int Rp = 1; Rp <= 3; ++Rp) {
+                if (bb < 2 * Rp) {
+                    const float m = Mt[(mrow + bb) * DK + ch];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        sm.ops.m.right[sw<DK>(rbase + r0 + u, ch)] = __float2bfloat16(kq[u] * gq[u] * m);
+                }
+                mrow += 2 * Rp;
+                rbase += 16 * Rp;
+            }
+        }
+        (void)TPB;
     }
     __syncthreads();
 
     // ------------------------------------------ P3: factorised blocks on mma.sync
+    // Warps 0-11: one 8-column tile each of the 16-level blocks (R = 1: 2 tiles,
+    // R = 2: 4, R = 3: 6), A and P together.  Warps 12-15: the 8 x 8 quadrant of
+    // diagonal 16-block R = warp - 12.
     {
         const int gq = lane >> 2, tq = lane & 3;
-        if (warp < 4) {
-            // 16-level: block row R, n-tiles [n0, n1) of the 16R columns left of it
-            const int R = warp == 0 ? 1 : (warp == 1 ? 2 : 3);
-            const int n0 = warp == 3 ? 3 : 0;
-            const int n1 = warp == 0 ? 2 : (warp == 1 ? 4 : (warp == 2 ? 3 : 6));
+        if (warp < 12) {
+            const int R = warp < 2 ? 1 : (warp < 6 ? 2 : 3);
+            const int nt = warp < 2 ? warp : (warp < 6 ? warp - 2 : warp - 6);
             const int rbase = (R - 1) * 16;                    // rows in left/leftq
             const int cbase = R == 1 ? 0 : (R == 2 ? 16 : 48); // rows in right
-            float accA[4][4], accP[4][4];
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) accA[n][e] = accP[n][e] = 0.f;
+            float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
                 const int k0 = kk * 16 + 2 * tq;
@@ -319,35 +458,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 aq[1] = lds_pair<DK>(sm.ops.m.leftq, rbase + gq + 8, k0);
                 aq[2] = lds_pair<DK>(sm.ops.m.leftq, rbase + gq, k0 + 8);
                 aq[3] = lds_pair<DK>(sm.ops.m.leftq, rbase + gq + 8, k0 + 8);
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    if (n0 + n < n1) {
-                        const int brow = cbase + (n0 + n) * 8 + gq;
-                        const uint32_t b0 = lds_pair<DK>(sm.ops.m.right, brow, k0);
-                        const uint32_t b1 = lds_pair<DK>(sm.ops.m.right, brow, k0 + 8);
-                        mma16816(accA[n], a, b0, b1);
-                        mma16816(accP[n], aq, b0, b1);
-                    }
-                }
+                const int brow = cbase + nt * 8 + gq;
+                const uint32_t b0 = lds_pair<DK>(sm.ops.m.right, brow, k0);
+                const uint32_t b1 = lds_pair<DK>(sm.ops.m.right, brow, k0 + 8);
+                mma16816(accA, a, b0, b1);
+                mma16816(accP, aq, b0, b1);
             }
+            const int col = nt * 8 + 2 * tq;
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                if (n0 + n < n1) {
-                    const int col = (n0 + n) * 8 + 2 * tq;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int row = 16 * R + gq + 8 * hh;
-                        const float b = sm.bs[row];
-                        sm.A[row * AP + col] = b * accA[n][2 * hh];
-                        sm.A[row * AP + col + 1] = b * accA[n][2 * hh + 1];
-                        gP[op_index(row, col, kChunk)] = __float2bfloat16(accP[n][2 * hh]);
-                        gP[op_index(row, col + 1, kChunk)] = __float2bfloat16(accP[n][2 * hh + 1]);
-                    }
-                }
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = 16 * R + gq + 8 * hh;
+                const float b = sm.bs[row];
+                sm.A[row * AP + col] = b * accA[2 * hh];
+                sm.A[row * AP + col + 1] = b * accA[2 * hh + 1];
+                gP[op_index(row, col, kChunk)] = __float2bfloat16(accP[2 * hh]);
+                gP[op_index(row, col + 1, kChunk)] = __float2bfloat16(accP[2 * hh + 1]);
             }
         } else {
-            // 8-level quadrant of diagonal block R = warp - 4: rows 16R+8.., cols 16R..
-            const int R = warp - 4;
+            // 8-level quadrant of diagonal block R: rows 16R+8.., cols 16R..
+            const int R = warp - 12;
             float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
@@ -383,35 +512,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------- P4: 8 x 8 diagonal blocks (CUDA cores)
+    // Thread (block, row, channel group of DK/8): channel pairs with packed fp32x2
+    // arithmetic.  The pair order is rotated so that the 64-bit shared loads of a
+    // warp use every bank pair exactly twice (two wavefronts).
     {
-        constexpr int CQ = DK / 4;
-        const int blk = warp, rin = (lane >> 2) & 7, qt = lane & 3;
+        constexpr int CQ = DK / 8, CP = CQ / 2;
+        const int blk = warp >> 1, r4 = lane >> 3, q8 = lane & 7;
+        const int rin = 4 * (warp & 1) + r4;
         const int r = 8 * blk + rin;
-        float accA[8], accP[8];
+        float2 acc2A[8], acc2P[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) accA[e] = accP[e] = 0.f;
-        for (int i = 0; i < CQ; ++i) {
-            const int ch = qt * CQ + ((i + lane) & (CQ - 1));
-            const float kr = sm.kn[r * DK + ch], qr = sm.qn[r * DK + ch];
-            float f = 1.f;
+        for (int e = 0; e < 8; ++e) acc2A[e] = acc2P[e] = make_float2(0.f, 0.f);
+        for (int i = 0; i < CP; ++i) {
+            const int ch = q8 * CQ + 2 * ((i + (q8 >> 1) + 4 * (r4 & 1)) & (CP - 1));
+            const float2 kr = *reinterpret_cast<const float2*>(&sm.kn[r * DK + ch]);
+            const float2 qr = *reinterpret_cast<const float2*>(&sm.qn[r * DK + ch]);
+            float2 f = make_float2(1.f, 1.f);
 #pragma unroll
             for (int dd = 0; dd < 8; ++dd) {
                 if (dd <= rin) {
                     const int j = r - dd;
-                    if (dd > 0) f *= sm.al[(j + 1) * DK + ch];
-                    const float t = sm.kn[j * DK + ch] * f;
-                    accP[dd] = fmaf(qr, t, accP[dd]);
-                    accA[dd] = fmaf(kr, t, accA[dd]);
+                    if (dd > 0) f = mul2(f, *reinterpret_cast<const float2*>(&sm.al[(j + 1) * DK + ch]));
+                    const float2 t = mul2(*reinterpret_cast<const float2*>(&sm.kn[j * DK + ch]), f);
+                    acc2P[dd] = fma2(qr, t, acc2P[dd]);
+                    acc2A[dd] = fma2(kr, t, acc2A[dd]);
                 }
             }
         }
+        float accA[8], accP[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            accA[e] += __shfl_xor_sync(0xffffffffu, accA[e], 1);
-            accA[e] += __shfl_xor_sync(0xffffffffu, accA[e], 2);
-            accP[e] += __shfl_xor_sync(0xffffffffu, accP[e], 1);
-            accP[e] += __shfl_xor_sync(0xffffffffu, accP[e], 2);
+            accA[e] = acc2A[e].x + acc2A[e].y;
+            accP[e] = acc2P[e].x + acc2P[e].y;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                accA[e] += __shfl_xor_sync(0xffffffffu, accA[e], o);
+                accP[e] += __shfl_xor_sync(0xffffffffu, accP[e], o);
+            }
         }
+        const int qt = q8;
         if (qt == 0) {
             const float b = sm.bs[r];
 #pragma unroll
@@ -428,50 +567,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    // ------------------------------------------------- P5: X = (I + A)^-1, blocked
+    // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
+    // X starts at zero (its upper triangle stays zero).  8 x 8 diagonal blocks by
+    // forward substitution, then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two
+    // inverted n x n blocks into one 2n x 2n block (unrolled products, two
+    // accumulators per output).
     {
-        float* X = sm.X;
-        const float* A = sm.A;
-        // (a) diagonal 16-blocks by forward substitution, thread per (block, column)
+        for (int e = tid; e < kChunk * AP; e += kThreads) sm.X[e] = 0.f;
+        __syncthreads();
         if (tid < 64) {
-            const int b = tid >> 4, jc = tid & 15, base = 16 * b;
-            float x[16];
+            const int base = 8 * (tid >> 3), jc = tid & 7;
+            float x[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float s = (i == jc) ? 1.f : 0.f;
+            for (int i = 0; i < 8; ++i) {
+                float acc = (i == jc) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    if (m < i) s -= A[(base + i) * AP + base + m] * x[m];
-                x[i] = (i < jc) ? 0.f : s;
+                for (int m = 0; m < 8; ++m)
+                    if (m < i) acc -= sm.A[(base + i) * AP + base + m] * x[m];
+                x[i] = (i < jc) ? 0.f : acc;
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) X[(base + i) * AP + base + jc] = x[i];
+            for (int i = 0; i < 8; ++i) sm.X[(base + i) * AP + base + jc] = x[i];
         }
         __syncthreads();
-        // (b) blocks below the diagonal, by distance: X_RJ = -X_RR sum_K A_RK X_KJ
-        float* T = sm.ops.scratch;
-        for (int dist = 1; dist <= 3; ++dist) {
-            const int nblk = 4 - dist;
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int R = dist + e / 256, J = R - dist, i = (e % 256) >> 4, j = e & 15;
-                float s = 0.f;
-                for (int K = J; K < R; ++K)
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        s += A[(16 * R + i) * AP + 16 * K + m] * X[(16 * K + m) * AP + 16 * J + j];
-                T[e] = s;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kThreads) {
-                const int R = dist + e / 256, J = R - dist, i = (e % 256) >> 4, j = e & 15;
-                float s = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    s -= X[(16 * R + i) * AP + 16 * R + m] * T[(e / 256) * 256 + m * 16 + j];
-                X[(16 * R + i) * AP + 16 * J + j] = s;
-            }
-            __syncthreads();
-        }
+        inv_join<8>(sm.X, sm.A, sm.ops.scratch, tid);
+        inv_join<16>(sm.X, sm.A, sm.ops.scratch, tid);
+        inv_join<32>(sm.X, sm.A, sm.ops.scratch, tid);
     }
 
     // ------------------------------------- P6: tcgen05 operands X Diag(beta), [kh g | v]^T
@@ -482,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int j = jb + u;
-                x[u] = ((j >> 4) <= (i >> 4)) ? sm.X[i * AP + j] * sm.bs[j] : 0.f;
+                x[u] = (j <= i) ? sm.X[i * AP + j] * sm.bs[j] : 0.f;
             }
             *reinterpret_cast<uint4*>(&sm.ops.t.xop[op_index(i, jb, kChunk)]) = pack8(x);
         }
@@ -531,11 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && tid == 0) atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
     ptx::tc_fence_after();
     {
-        // warp w and w + 4 share TMEM lane quarter w; split the columns between them
+        // warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w; split the columns
         const int quarter = warp & 3, half = warp >> 2;
         const int row = 16 * quarter + lane;  // valid for lane < 16 (M = 64 layout)
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-        constexpr int HALF = NB / 2;
+        constexpr int HALF = NB / (kThreads / 128);
 #pragma unroll 1
         for (int cb = half * HALF; cb < (half + 1) * HALF; cb += 16) {
             float x[16];
@@ -575,7 +696,7 @@ cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v,
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)W.cmax, (unsigned)d.H);
     kern<<<grid, kThreads, smem, stream>>>(d, static_cast<const TIn*>(q), static_cast<const TIn*>(k),
-                                           static_cast<const TIn*>(v), g, beta, ws);
+                                           static_cast<const TIn*>(v), g, beta, ws, num_sms());
     return cudaGetLastError();
 }
 
