@@ -203,16 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qa = ptx::smem_u32(sm.st[st].QG), pa = ptx::smem_u32(sm.st[st].P);
                 const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
                 const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk)  // D3 = QG S
-                    ptx::mma_bf16(d3, ptx::smem_desc(qa + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_w, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)  // D3 += P U
-                    ptx::mma_bf16(d3, ptx::smem_desc(pa + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_w, true);
+                ptx::mma_chain<DK / 16>(d3, ptx::smem_desc(qa, 1024, 128), 2048,  // D3 = QG S
+                                        ptx::smem_desc(sop, (NV / 8) * 128, 128), 2 * (NV / 8) * 128,
+                                        id_w, false);
+                ptx::mma_chain<kChunk / 16>(d3, ptx::smem_desc(pa, 1024, 128), 2048,  // D3 += P U
+                                            ptx::smem_desc(uop, (NV / 8) * 128, 128),
+                                            2 * (NV / 8) * 128, id_w, true);
                 ptx::mma_commit(&sm.d3[j & 1]);
                 ptx::mma_commit(&sm.empty[st]);
             }
@@ -257,11 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t wa = ptx::smem_u32(sm.st[st].W);
                     const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
-#pragma unroll
-                    for (int kk = 0; kk < DK / 16; ++kk)
-                        ptx::mma_bf16(tmem + kColD1, ptx::smem_desc(wa + kk * 2048, 1024, 128),
-                                      ptx::smem_desc(sop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                      id_w, kk > 0);
+                    ptx::mma_chain<DK / 16>(tmem + kColD1, ptx::smem_desc(wa, 1024, 128), 2048,
+                                            ptx::smem_desc(sop, (NV / 8) * 128, 128),
+                                            2 * (NV / 8) * 128, id_w, false);
                     ptx::mma_commit(&sm.d1);
                 }
             }
@@ -315,12 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 ptx::mbar_arrive(&sm.uready);
                 const uint32_t ka = ptx::smem_u32(sm.st[st].KT);
-#pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)  // D2 = KT U
-                    ptx::mma_bf16(tmem + kColD2,
-                                  ptx::smem_desc(ka + kk * 2 * (DK / 8) * 128, (DK / 8) * 128, 128),
-                                  ptx::smem_desc(uop + kk * 2 * (NV / 8) * 128, (NV / 8) * 128, 128),
-                                  id_k, kk > 0);
+                ptx::mma_chain<kChunk / 16>(tmem + kColD2,  // D2 = KT U
+                                            ptx::smem_desc(ka, (DK / 8) * 128, 128), 2 * (DK / 8) * 128,
+                                            ptx::smem_desc(uop, (NV / 8) * 128, 128),
+                                            2 * (NV / 8) * 128, id_k, false);
                 ptx::mma_commit(&sm.d2);
                 ptx::mma_commit(&sm.empty[st]);
             }

@@ -60,6 +60,7 @@ struct __align__(128) PrepSmem {
         float scratch[32 * 32];
     } ops;
     float bs[kChunk];
+    float gb[8 * DK];  // alpha(0..8b) per block start b and channel (kept for the w operand)
     uint64_t bar;
     uint32_t tmem;
     int abort;
@@ -132,6 +133,71 @@ __device__ inline void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t 
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ inline uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ inline void mma1688_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// C (16 x 8 tile at rows cr, cols cc of an N x N block, row stride ldc) = P Q over
+// K = N, P and Q read from fp32 shared memory (row strides ldp, ldq), tf32 inputs,
+// fp32 accumulation; sign -1 negates.  One warp.
+template <int N>
+__device__ __forceinline__ void tile_mm_tf32(const float* P, int ldp, const float* Q, int ldq,
+                                             float* C, int ldc, int cr, int cc, float sign,
+                                             int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k0 = 0; k0 < N; k0 += 8) {
+        uint32_t a[4];
+        a[0] = to_tf32(P[(cr + gq) * ldp + k0 + tq]);
+        a[1] = to_tf32(P[(cr + gq + 8) * ldp + k0 + tq]);
+        a[2] = to_tf32(P[(cr + gq) * ldp + k0 + tq + 4]);
+        a[3] = to_tf32(P[(cr + gq + 8) * ldp + k0 + tq + 4]);
+        const uint32_t b0 = to_tf32(Q[(k0 + tq) * ldq + cc + gq]);
+        const uint32_t b1 = to_tf32(Q[(k0 + tq + 4) * ldq + cc + gq]);
+        mma1688_tf32(acc, a, b0, b1);
+    }
+    C[(cr + gq) * ldc + cc + 2 * tq] = sign * acc[0];
+    C[(cr + gq) * ldc + cc + 2 * tq + 1] = sign * acc[1];
+    C[(cr + gq + 8) * ldc + cc + 2 * tq] = sign * acc[2];
+    C[(cr + gq + 8) * ldc + cc + 2 * tq + 1] = sign * acc[3];
+}
+
+// Tensor-core join for n = 16, 32: one 16 x 8 tile of T = A21 X11, then of
+// X21 = -X22 T, per warp.  Ends with the CTA synchronised.
+template <int N>
+__device__ __forceinline__ void inv_join_tc(float* X, const float* A, float* T, int warp, int lane) {
+    constexpr int AP = kChunk + 1;
+    constexpr int PAIRS = kChunk / (2 * N);
+    constexpr int TILES = (N / 16) * (N / 8);        // tiles per pair
+    for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
+        const int pidx = t / TILES, tt = t % TILES;
+        const int r1 = 2 * pidx * N, r2 = r1 + N;
+        const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
+        tile_mm_tf32<N>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T + pidx * N * N, N, cr, cc,
+                        1.f, lane);
+    }
+    __syncthreads();
+    for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
+        const int pidx = t / TILES, tt = t % TILES;
+        const int r1 = 2 * pidx * N, r2 = r1 + N;
+        const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
+        tile_mm_tf32<N>(X + r2 * AP + r2, AP, T + pidx * N * N, N, X + r2 * AP + r1, AP, cr, cc,
+                        -1.f, lane);
+    }
+    __syncthreads();
 }
 
 // Joins pairs of inverted n x n diagonal blocks of X = (I + A)^-1 (row stride
@@ -320,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // them: Gb_b = alpha(0..8b), Sb_b = alpha(8b+8..63), M(b, R) = alpha(8b+8..16R).
     {
         float* Bi = sm.X;                 // inner block products alpha(8b+1..8b+7) [8][DK]
-        float* Gb = sm.X + 8 * DK;        // [8][DK]
+        float* Gb = sm.gb;                // [8][DK]
         float* Sb = sm.X + 16 * DK;       // [8][DK]
         float* Mt = sm.A;                 // M(b, R): 2 + 4 + 6 rows of [DK]
         constexpr int TPB = kThreads / DK;   // tasks per block pass
@@ -570,8 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
     // X starts at zero (its upper triangle stays zero).  8 x 8 diagonal blocks by
     // forward substitution, then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two
-    // inverted n x n blocks into one 2n x 2n block (unrolled products, two
-    // accumulators per output).
+    // inverted n x n blocks into one 2n x 2n block (n = 8 on CUDA cores, n = 16 and
+    // 32 with mma.sync on tf32 inputs and fp32 accumulation).
     {
         for (int e = tid; e < kChunk * AP; e += kThreads) sm.X[e] = 0.f;
         __syncthreads();
@@ -591,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         inv_join<8>(sm.X, sm.A, sm.ops.scratch, tid);
-        inv_join<16>(sm.X, sm.A, sm.ops.scratch, tid);
-        inv_join<32>(sm.X, sm.A, sm.ops.scratch, tid);
+        inv_join_tc<16>(sm.X, sm.A, sm.ops.scratch, warp, lane);
+        inv_join_tc<32>(sm.X, sm.A, sm.ops.scratch, warp, lane);
     }
 
     // ------------------------------------- P6: tcgen05 operands X Diag(beta), [kh g | v]^T
@@ -607,27 +673,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             *reinterpret_cast<uint4*>(&sm.ops.t.xop[op_index(i, jb, kChunk)]) = pack8(x);
         }
-        for (int col = tid; col < NB; col += kThreads) {
+        // [kh * gamma | v]^T, one task per (8-row block, column): gamma_r = Gb_b f_r
+        for (int e = tid; e < 8 * NB; e += kThreads) {
+            const int bb = e / NB, col = e % NB, r0 = 8 * bb;
             if (col < DK) {
-                float gp = 1.f;
-                for (int jb = 0; jb < kChunk; jb += 8) {
-                    float x[8];
+                float x[8];
+                float f = sm.gb[bb * DK + col];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        gp *= sm.al[(jb + u) * DK + col];
-                        x[u] = sm.kn[(jb + u) * DK + col] * gp;
-                    }
-                    *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(col, jb, NB)]) = pack8(x);
+                for (int u = 0; u < 8; ++u) {
+                    if (u > 0) f *= sm.al[(r0 + u) * DK + col];
+                    x[u] = sm.kn[(r0 + u) * DK + col] * f;
                 }
+                *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(col, r0, NB)]) = pack8(x);
             } else {
                 const int dcol = col - DK;
-                for (int jb = 0; jb < kChunk; jb += 8) {
-                    uint4 u4;
-                    __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(&u4);
+                uint4 u4;
+                __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(&u4);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) hb[u] = sm.vs[(jb + u) * DV + dcol];
-                    *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(col, jb, NB)]) = u4;
-                }
+                for (int u = 0; u < 8; ++u) hb[u] = sm.vs[(r0 + u) * DV + dcol];
+                *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(col, r0, NB)]) = u4;
             }
         }
         ptx::fence_proxy_async_smem();

@@ -157,6 +157,32 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// The two forms of the MMA with a constant accumulate flag.
+__device__ __forceinline__ void mma_bf16_first(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc) {
+    mma_bf16(d_tmem, a_desc, b_desc, idesc, false);
+}
+__device__ __forceinline__ void mma_bf16_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc) {
+    mma_bf16(d_tmem, a_desc, b_desc, idesc, true);
+}
+
+// Issues a K = 16 * KSTEPS product: the descriptors of step kk are the base
+// descriptors advanced by kk * a_step (b_step) bytes, in the 16-byte units of the
+// start-address field (valid while addresses stay below 256 KB, as shared memory
+// does).
+template <int KSTEPS>
+__device__ __forceinline__ void mma_chain(uint32_t d_tmem, uint64_t a_desc, uint32_t a_step,
+                                          uint64_t b_desc, uint32_t b_step, uint32_t idesc,
+                                          bool accumulate_first) {
+    if (accumulate_first) mma_bf16_acc(d_tmem, a_desc, b_desc, idesc);
+    else mma_bf16_first(d_tmem, a_desc, b_desc, idesc);
+#pragma unroll
+    for (int kk = 1; kk < KSTEPS; ++kk)
+        mma_bf16_acc(d_tmem, a_desc + (uint64_t)((kk * a_step) >> 4),
+                     b_desc + (uint64_t)((kk * b_step) >> 4), idesc);
+}
+
 // Arrive on `bar` once all previously issued MMAs of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
