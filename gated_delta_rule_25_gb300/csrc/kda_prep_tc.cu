@@ -434,63 +434,80 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        // (c) per (block, channel): local products, then every operand row
-        for (int e = tid; e < 8 * DK; e += kThreads) {
-            const int bb = e / DK, ch = e % DK;
+        // (c) per (block, channel pair): local products (packed fp32x2), then every
+        //     operand row, two adjacent channels per 32-bit store
+        for (int e = tid; e < 8 * (DK / 2); e += kThreads) {
+            const int bb = e / (DK / 2), ch = 2 * (e % (DK / 2));
             const int r0 = 8 * bb;
-            float al[8], kq[8], qq[8], f[8], gq[8];
+            float2 al[8], kq[8], qq[8], f[8], gq[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                al[u] = sm.al[(r0 + u) * DK + ch];
-                kq[u] = sm.kn[(r0 + u) * DK + ch];
-                qq[u] = sm.qn[(r0 + u) * DK + ch];
+                al[u] = *reinterpret_cast<const float2*>(&sm.al[(r0 + u) * DK + ch]);
+                kq[u] = *reinterpret_cast<const float2*>(&sm.kn[(r0 + u) * DK + ch]);
+                qq[u] = *reinterpret_cast<const float2*>(&sm.qn[(r0 + u) * DK + ch]);
             }
-            f[0] = 1.f;
+            f[0] = make_float2(1.f, 1.f);
 #pragma unroll
-            for (int u = 1; u < 8; ++u) f[u] = f[u - 1] * al[u];
-            gq[7] = 1.f;
+            for (int u = 1; u < 8; ++u) f[u] = mul2(f[u - 1], al[u]);
+            gq[7] = make_float2(1.f, 1.f);
 #pragma unroll
-            for (int u = 6; u >= 0; --u) gq[u] = gq[u + 1] * al[u + 1];
-            const float gb = Gb[bb * DK + ch], sb = Sb[bb * DK + ch];
+            for (int u = 6; u >= 0; --u) gq[u] = mul2(gq[u + 1], al[u + 1]);
+            const float2 gb = *reinterpret_cast<const float2*>(&Gb[bb * DK + ch]);
+            const float2 sb = *reinterpret_cast<const float2*>(&Sb[bb * DK + ch]);
             // QG = qh * gamma (global, operand layout) and KT = (kh * gamma_L / gamma)^T
-            float kt[8];
+            float kt0[8], kt1[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                gQG[op_index(r0 + u, ch, kChunk)] = __float2bfloat16(qq[u] * gb * f[u]);
-                kt[u] = kq[u] * gq[u] * sb;
+                const float2 qgv = mul2(qq[u], mul2(gb, f[u]));
+                *reinterpret_cast<uint32_t*>(&gQG[op_index(r0 + u, ch, kChunk)]) = pack_bf16(qgv.x, qgv.y);
+                const float2 ktv = mul2(kq[u], mul2(gq[u], sb));
+                kt0[u] = ktv.x;
+                kt1[u] = ktv.y;
             }
-            *reinterpret_cast<uint4*>(&gKT[op_index(ch, r0, DK)]) = pack8(kt);
+            *reinterpret_cast<uint4*>(&gKT[op_index(ch, r0, DK)]) = pack8(kt0);
+            *reinterpret_cast<uint4*>(&gKT[op_index(ch + 1, r0, DK)]) = pack8(kt1);
             const int R = bb >> 1;
             if (bb >= 2) {  // 16-level row factors D(r, 16R)
-                const float pre = (bb & 1) ? Bi[(2 * R) * DK + ch] * sm.al[(16 * R + 8) * DK + ch] : 1.f;
+                float2 pre = make_float2(1.f, 1.f);
+                if (bb & 1)
+                    pre = mul2(*reinterpret_cast<const float2*>(&Bi[(2 * R) * DK + ch]),
+                               *reinterpret_cast<const float2*>(&sm.al[(16 * R + 8) * DK + ch]));
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int rr = r0 + u - 16;
-                    sm.ops.m.left[sw<DK>(rr, ch)] = __float2bfloat16(kq[u] * pre * f[u]);
-                    sm.ops.m.leftq[sw<DK>(rr, ch)] = __float2bfloat16(qq[u] * pre * f[u]);
+                    const float2 pf = mul2(pre, f[u]);
+                    const float2 x = mul2(kq[u], pf), y = mul2(qq[u], pf);
+                    *reinterpret_cast<uint32_t*>(&sm.ops.m.left[sw<DK>(rr, ch)]) = pack_bf16(x.x, x.y);
+                    *reinterpret_cast<uint32_t*>(&sm.ops.m.leftq[sw<DK>(rr, ch)]) = pack_bf16(y.x, y.y);
                 }
             }
             if (bb & 1) {  // 8-level row factors D(r, 16R+8)
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    sm.ops.m.l8[sw<DK>(8 * R + u, ch)] = __float2bfloat16(kq[u] * f[u]);
-                    sm.ops.m.l8q[sw<DK>(8 * R + u, ch)] = __float2bfloat16(qq[u] * f[u]);
+                    const float2 x = mul2(kq[u], f[u]), y = mul2(qq[u], f[u]);
+                    *reinterpret_cast<uint32_t*>(&sm.ops.m.l8[sw<DK>(8 * R + u, ch)]) = pack_bf16(x.x, x.y);
+                    *reinterpret_cast<uint32_t*>(&sm.ops.m.l8q[sw<DK>(8 * R + u, ch)]) = pack_bf16(y.x, y.y);
                 }
             } else {       // 8-level column factors D(16R+8, j) = g_j alpha(16R+8)
-                const float a8 = sm.al[(16 * R + 8) * DK + ch];
+                const float2 a8 = *reinterpret_cast<const float2*>(&sm.al[(16 * R + 8) * DK + ch]);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    sm.ops.m.r8[sw<DK>(8 * R + u, ch)] = __float2bfloat16(kq[u] * gq[u] * a8);
+                for (int u = 0; u < 8; ++u) {
+                    const float2 x = mul2(kq[u], mul2(gq[u], a8));
+                    *reinterpret_cast<uint32_t*>(&sm.ops.m.r8[sw<DK>(8 * R + u, ch)]) = pack_bf16(x.x, x.y);
+                }
             }
             // 16-level column factors D(16R', j) for every R' with 16R' > j
             int mrow = 0, rbase = 0;
 #pragma unroll
             for (int Rp = 1; Rp <= 3; ++Rp) {
                 if (bb < 2 * Rp) {
-                    const float m = Mt[(mrow + bb) * DK + ch];
+                    const float2 m = *reinterpret_cast<const float2*>(&Mt[(mrow + bb) * DK + ch]);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        sm.ops.m.right[sw<DK>(rbase + r0 + u, ch)] = __float2bfloat16(kq[u] * gq[u] * m);
+                    for (int u = 0; u < 8; ++u) {
+                        const float2 x = mul2(kq[u], mul2(gq[u], m));
+                        *reinterpret_cast<uint32_t*>(&sm.ops.m.right[sw<DK>(rbase + r0 + u, ch)]) =
+                            pack_bf16(x.x, x.y);
+                    }
                 }
                 mrow += 2 * Rp;
                 rbase += 16 * Rp;
