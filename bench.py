@@ -36,9 +36,30 @@ import torch  # noqa: E402
 from tests import gen  # noqa: E402
 
 METRIC = "KDA fwd tokens/s at H=32,d=128,8192 tok; % tensor-pipe/HBM roofline"
-WORKLOAD = "fixed-length B=1 T=8192 H=32 dk=dv=128 bf16 q/k/v, fp32 g/beta/h0 (Student-t mixture, g=-softplus(N(-1,2)) clamped)"
-B, T, H, D = 1, 8192, 32, 128
+WORKLOADS = {
+    "cfg2": "fixed-length B=1 T=8192 H=32 dk=dv=128 bf16 q/k/v, fp32 g/beta/h0 (Student-t mixture, g=-softplus(N(-1,2)) clamped)",
+    "cfg3": "varlen 8192 tokens in 8 sequences (uniform split, one of length 1), H=32, dk=dv=128, bf16",
+    "cfg4": "varlen skewed 8192 tokens in 32 sequences (one ~5000), H=32, d=128, extreme-value probes",
+}
 KERNEL_NAMES = ["schedule", "factors", "state_recurrence"]
+
+
+def make_workload(name: str, seed: int, salt: int):
+    """cfg2 (default), cfg3, cfg4, or a throughput-sweep row cfg5-{fixed|varlen}-H{H}-{total}."""
+    if name == "cfg2":
+        return gen.make_cfg2(seed=seed, salt=salt), WORKLOADS[name]
+    if name == "cfg3":
+        return gen.make_cfg3(seed=seed, salt=salt), WORKLOADS[name]
+    if name == "cfg4":
+        return gen.make_cfg4(seed=seed, salt=salt), WORKLOADS[name]
+    if name.startswith("cfg5-"):
+        _, kind, hs, total = name.split("-")
+        H_, total_ = int(hs[1:]), int(total)
+        x = gen.make_cfg5(H_, total_, kind == "varlen", seed=seed, salt=salt)
+        desc = (f"throughput sweep: {kind} {total_} tokens, H={H_}, dk=dv=128, bf16 "
+                f"({'B=' + str(total_ // 8192) + ' x 8192' if kind == 'fixed' else str(x.num_seqs) + ' sequences'})")
+        return x, desc
+    raise ValueError(f"unknown workload {name}")
 
 
 def _peaks():
@@ -149,6 +170,7 @@ def cpu_baseline(x, budget_s: float = 12.0):
     """The fp64 oracle, as it stands, on this host's cores: whole heads of the same
     workload until ~budget_s of work; tokens/s scaled to all H heads."""
     import oracle
+    H = x.H
     cores = oracle.max_threads()
     heads = min(H, max(1, cores))
     dt = _oracle_sample(x, heads)
@@ -169,7 +191,8 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    x = gen.make_cfg2(seed=0, salt=gen.fresh_salt())
+    x, desc = make_workload(args.workload, 0, gen.fresh_salt())
+    H = x.H
     cores = oracle.max_threads()
     heads = min(H, max(1, cores))
     for _ in range(args.warmup):
@@ -181,7 +204,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per * 1e3 * H / heads, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens_per_step": x.tokens},
+            "config": {"workload": desc, "tokens_per_step": x.tokens},
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"each step: {heads} of {H} heads x {x.tokens} tokens "
                                        "(fp64 token recurrence); tokens/s scaled to all heads"},
@@ -197,6 +220,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="cfg2",
+                    help="cfg2 (the headline workload), cfg3, cfg4, cfg5-{fixed|varlen}-H{16|32|64}-{total}")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -218,9 +243,10 @@ def main():
     import gated_delta_rule_25_gb300 as kda
 
     salt = gen.fresh_salt() + rank
-    x = gen.make_cfg2(seed=0, salt=salt)
+    x, desc = make_workload(args.workload, 0, salt)
     xd = x.to(dev)
     nseq = x.num_seqs
+    B, T, H, D = x.B, x.T, x.H, x.dk
     o = torch.empty_like(xd.v)
     hT = torch.empty_like(xd.h0)
     ws = torch.empty(kda.workspace_size(B, T, H, D, D, nseq) + 256, dtype=torch.uint8, device=dev)
@@ -273,7 +299,10 @@ def main():
     value = world * x.tokens / (ms_step * 1e-3)
 
     # parity after timing, on fresh inputs through the same buffers (sampled heads)
-    x2 = gen.make_cfg2(seed=1, salt=salt + 7919)
+    x2, _ = make_workload(args.workload, 1, salt + 7919)
+    if x.cu_seqlens is not None:  # same layout, fresh values
+        x2.cu_seqlens = x.cu_seqlens
+        x2.h0 = x2.h0[: x.num_seqs]
     for name in ("q", "k", "v", "g", "beta", "h0"):
         getattr(xd, name).copy_(getattr(x2, name).to(dev))
     step()
@@ -282,7 +311,7 @@ def main():
     if rank == 0:
         import oracle
         from tests.metrics import rel_rmse
-        hs = [0, 17]
+        hs = [0, x2.H // 2 + 1]
         t = x2.tensors()
         for key in ("q", "k", "v", "g", "beta"):
             t[key] = t[key][:, :, hs].contiguous()
@@ -304,7 +333,7 @@ def main():
         for n, t in host_in.items():
             dev_in[n].copy_(t, non_blocking=True)
         kda.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["h0"],
-                None, x.scale, o=o, hT=hT, workspace=ws)
+                xd.cu_seqlens, x.scale, o=o, hT=hT, workspace=ws)
         o_host.copy_(o, non_blocking=True)
         h_host.copy_(hT, non_blocking=True)
 
@@ -330,6 +359,8 @@ def main():
         return
 
     hbm, bf16_tf, peak_src = _peaks()
+    in_mb = sum(t.numel() * t.element_size() for t in (x.q, x.k, x.v, x.g, x.beta)) / 1e6
+    ws_mb = ws.numel() / 1e6
     dom = int(np.argmax(per_kernel))
     dom_name = KERNEL_NAMES[dom] if dom < len(KERNEL_NAMES) else f"kernel{dom}"
     alg = _algorithmic_bytes(dom_name, x.tokens, H, D, D, nseq)
@@ -343,8 +374,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens_per_step": x.tokens, "heads": H, "dk": D,
-                   "dv": D, "l2": "no flush: 336 MB of inputs and ~300 MB of factors per step exceed the 129 MB L2",
+        "config": {"workload": desc, "name": args.workload, "tokens_per_step": x.tokens,
+                   "heads": H, "dk": D, "dv": D,
+                   "l2": f"no flush: {in_mb:.0f} MB of inputs and {ws_mb:.0f} MB of factors per step vs the 129 MB L2",
                    "salt": salt},
         "gpu_launches": nl * args.steps,
         "kernels_ms": {KERNEL_NAMES[j] if j < len(KERNEL_NAMES) else f"kernel{j}": per_kernel[j]

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NVT = DV / NV;
     const int vt = blockIdx.x % NVT;
     const int h = (blockIdx.x / NVT) % d.H;
-    const int s = blockIdx.x / (NVT * d.H);
+    const int s = reinterpret_cast<const int32_t*>(ws + WsLayout(d).order)[blockIdx.x / (NVT * d.H)];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const WsLayout W(d);
     const FactorLayout F(DK, DV);

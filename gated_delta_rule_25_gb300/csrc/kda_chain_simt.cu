@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kThreads) chain_simt_kernel(Dims d, const floa
     constexpr int NVT = DV / NV;
     const int vt = blockIdx.x % NVT;
     const int h = (blockIdx.x / NVT) % d.H;
-    const int s = blockIdx.x / (NVT * d.H);
+    const int s = reinterpret_cast<const int32_t*>(ws + WsLayout(d).order)[blockIdx.x / (NVT * d.H)];
     const int tid = threadIdx.x, n = tid % NV, r8 = tid / NV;
     WsLayout W(d);
     FactorLayout F(DK, DV);

@@ -3,6 +3,7 @@
 // Workspace (caller-owned, 256-byte aligned), carved as:
 //   [0, 256)        header: u32 error word, i32 total chunk count
 //   seq_first       int32[N + 1]: index of the first chunk of each sequence
+//   order           int32[N]:     sequences by decreasing chunk count (longest first)
 //   chunks          int4[Cmax]:   {sequence, first token row, valid rows L, 0}
 //   factors         per (chunk, head): the factors of the chunkwise form
 //
@@ -71,7 +72,7 @@ struct FactorLayout {
 };
 
 struct WsLayout {
-    size_t header, seq_first, chunks, factors, total;
+    size_t header, seq_first, order, chunks, factors, total;
     long long cmax;
     size_t factor_bytes;
     __host__ __device__ explicit WsLayout(const Dims& d) {
@@ -81,6 +82,7 @@ struct WsLayout {
         size_t off = 0;
         header = off;    off += 256;
         seq_first = off; off += align256(size_t(d.N + 1) * 4);
+        order = off;     off += align256(size_t(d.N) * 4);
         chunks = off;    off += align256(size_t(cmax) * 16);
         factors = off;   off += size_t(cmax) * d.H * f.bytes;
         total = off;

@@ -10,6 +10,7 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kRankMax = 2048;
 
 __device__ inline void seq_span(const Dims& d, const int32_t* cu, int s, long long& row0,
                                 int& len) {
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     __syncthreads();
     if (bad) {
         for (int s = tid; s <= d.N; s += kThreads) seq_first[s] = 0;
+        int32_t* order = reinterpret_cast<int32_t*>(ws + L.order);
+        for (int s = tid; s < d.N; s += kThreads) order[s] = s;
         if (tid == 0) {
             hdr->error = kDevErrCuSeqlens;
             hdr->total_chunks = 0;
@@ -99,6 +102,24 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         seq_first[d.N] = carry;
         hdr->error = 0;
         hdr->total_chunks = carry;
+    }
+    // Longest chains first: the state kernel maps its CTAs through this order so
+    // that a dominant sequence starts at once instead of after the short ones.
+    // Stable rank by chunk count for up to kRankMax sequences, identity beyond.
+    int32_t* order = reinterpret_cast<int32_t*>(ws + L.order);
+    __syncthreads();
+    if (d.N <= kRankMax) {
+        for (int s = tid; s < d.N; s += kThreads) {
+            const int ns = seq_first[s + 1] - seq_first[s];
+            int rank = 0;
+            for (int t = 0; t < d.N; ++t) {
+                const int nt = seq_first[t + 1] - seq_first[t];
+                rank += (nt > ns) || (nt == ns && t < s);
+            }
+            order[rank] = s;
+        }
+    } else {
+        for (int s = tid; s < d.N; s += kThreads) order[s] = s;
     }
 }
 
