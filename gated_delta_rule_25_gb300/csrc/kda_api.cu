@@ -1,7 +1,6 @@
 // C ABI of the KDA prefill forward: argument checks, workspace carving, launches.
 // Declarations and the contract are in include/kda.h.
 #include <cmath>
-#include <cstdlib>
 #include <map>
 #include <mutex>
 
@@ -117,21 +116,10 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         return cudaEventRecord(static_cast<cudaEvent_t>(events[ev++]), s) == cudaSuccess;
     };
     if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
-    static const bool simt_prep = [] {
-        const char* e = std::getenv("KDA_DEBUG_SIMT_PREP");
-        return e && e[0] == '1';
-    }();
-    if (!mark()) return KDA_ERR_CUDA;
-    if ((simt_prep ? kda::launch_prep(d, bf16, q, k, v, g, beta, ws, s)
-                   : kda::launch_prep_tc(d, bf16, q, k, v, g, beta, ws, s)) != cudaSuccess)
+    if (!mark() || kda::launch_prep_tc(d, bf16, q, k, v, g, beta, ws, s) != cudaSuccess)
         return KDA_ERR_CUDA;
-    static const bool simt_chain = [] {
-        const char* e = std::getenv("KDA_DEBUG_SIMT_CHAIN");
-        return e && e[0] == '1';
-    }();
     if (!mark()) return KDA_ERR_CUDA;
-    cudaError_t ce = simt_chain ? kda::launch_chain_simt(d, bf16, h0, scale, o, hT, ws, s)
-                                : kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
+    const cudaError_t ce = kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
     if (ce != cudaSuccess || !mark()) return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -18,8 +18,14 @@
 // from D1, a named barrier, thread 0 issues GEMM2 (and signals warp 5, which
 // issues GEMM3), S is updated from D2, a named barrier, and the next chunk starts.
 //
+// The kernel is persistent (one CTA per SM): the producer warp takes work items
+// (sequence, head, value tile), longest sequences first, from a counter in the
+// workspace, streams each item's chunks through the stage ring and stamps every
+// stage with its item; the other warps follow the stamps (a new item loads h0 at
+// its first chunk and stores h_T after its last), so chains run back to back.
+//
 // Warps 0-3: epilogue, GEMM1/GEMM2 issue (warp w reads TMEM lanes 32w..32w+31).
-// Warp 4: bulk copies of the per-chunk factors, three stages deep.
+// Warp 4: work items and bulk copies of the per-chunk factors, three stages deep.
 // Warp 5: GEMM3 issue (output products, off the serial path).
 // Every wait is bounded; a time-out sets KDA_DEVERR_TIMEOUT in the workspace
 // error word and the CTA drains and leaves.
@@ -43,6 +49,8 @@ struct __align__(128) ChainStage {
     __nv_bfloat16 P[kChunk * kChunk];
     __nv_bfloat16 U0[kChunk * NV];   // row-major 64 x 32 slab of u
     float GL[DK];
+    int4 item;                       // {sequence, head, value tile, chunk index j}
+    int4 info;                       // {chunks of the item, first token row, rows, end marker}
 };
 
 template <int DK>
@@ -128,16 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ChainSmem<DK>& sm = *reinterpret_cast<ChainSmem<DK>*>(smem_raw);
     constexpr int NVT = DV / NV;
-    const int vt = blockIdx.x % NVT;
-    const int h = (blockIdx.x / NVT) % d.H;
-    const int s = reinterpret_cast<const int32_t*>(ws + WsLayout(d).order)[blockIdx.x / (NVT * d.H)];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const WsLayout W(d);
     const FactorLayout F(DK, DV);
+    Header* hdr = reinterpret_cast<Header*>(ws + W.header);
     const int32_t* seq_first = reinterpret_cast<const int32_t*>(ws + W.seq_first);
+    const int32_t* order = reinterpret_cast<const int32_t*>(ws + W.order);
     const int4* chunks = reinterpret_cast<const int4*>(ws + W.chunks);
-    const int c0 = seq_first[s];
-    const int nch = seq_first[s + 1] - c0;
+    const int n_items = d.N * d.H * NVT;
     volatile int* abort = &sm.abort;
 
     if (tid == 0) {
@@ -165,30 +171,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 4) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint32_t main_bytes = (uint32_t)(F.u0 - F.w);  // W, QG, KT, P back to back
-            const uint32_t u_bytes = kChunk * NV * 2, gl_bytes = DK * 4;
-            int issued = 0;
-            for (int j = 0; j < nch; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages &&
-                    !ptx::mbar_wait_or_abort(&sm.empty[st], ((j / kStages) - 1) & 1, abort)) {
-                    raise_error(ws, abort);
-                    break;
+        // ------------------------------------------------ work items + producer
+        const uint32_t main_bytes = (uint32_t)(F.u0 - F.w);  // W, QG, KT, P back to back
+        const uint32_t u_bytes = kChunk * NV * 2, gl_bytes = DK * 4;
+        int gj = 0;
+        bool okp = true;
+        while (okp) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(&hdr->next_item, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            if (item >= n_items) break;
+            const int rank = item / (NVT * d.H), hh = (item / NVT) % d.H, vtt = item % NVT;
+            const int s = order[rank];
+            const int c0 = seq_first[s], nch = seq_first[s + 1] - c0;
+            if (nch == 0) {  // empty sequence: the state passes through unchanged
+                if (hT) {
+                    const size_t base = ((size_t)s * d.H + hh) * DK;
+                    for (int e = lane; e < DK * NV; e += 32) {
+                        const size_t off = (base + e / NV) * DV + vtt * NV + e % NV;
+                        hT[off] = h0 ? h0[off] : 0.f;
+                    }
                 }
-                const uint8_t* fb = ws + W.factors + ((size_t)(c0 + j) * d.H + h) * W.factor_bytes;
-                ptx::mbar_arrive_expect_tx(&sm.full[st], main_bytes + u_bytes + gl_bytes);
-                ptx::bulk_g2s(sm.st[st].W, fb + F.w, main_bytes, &sm.full[st]);
-                ptx::bulk_g2s(sm.st[st].U0, fb + F.u0 + (size_t)vt * u_bytes, u_bytes, &sm.full[st]);
-                ptx::bulk_g2s(sm.st[st].GL, fb + F.gl, gl_bytes, &sm.full[st]);
-                issued = j + 1;
+                continue;
             }
-            if (*abort) {  // let copies already in flight land before the CTA leaves
+            for (int j = 0; j < nch; ++j, ++gj) {
+                const int st = gj % kStages;
+                if (lane == 0) {
+                    if (gj >= kStages &&
+                        !ptx::mbar_wait_or_abort(&sm.empty[st], ((gj / kStages) - 1) & 1, abort)) {
+                        raise_error(ws, abort);
+                        okp = false;
+                    } else {
+                        const int4 chk = chunks[c0 + j];
+                        sm.st[st].item = make_int4(s, hh, vtt, j);
+                        sm.st[st].info = make_int4(nch, chk.y, chk.z, 0);
+                        const uint8_t* fb = ws + W.factors + ((size_t)(c0 + j) * d.H + hh) * W.factor_bytes;
+                        ptx::mbar_arrive_expect_tx(&sm.full[st], main_bytes + u_bytes + gl_bytes);
+                        ptx::bulk_g2s(sm.st[st].W, fb + F.w, main_bytes, &sm.full[st]);
+                        ptx::bulk_g2s(sm.st[st].U0, fb + F.u0 + (size_t)vtt * u_bytes, u_bytes,
+                                      &sm.full[st]);
+                        ptx::bulk_g2s(sm.st[st].GL, fb + F.gl, gl_bytes, &sm.full[st]);
+                    }
+                }
+                okp = __shfl_sync(0xffffffffu, okp, 0);
+                if (!okp) break;
+            }
+        }
+        if (lane == 0) {
+            if (okp) {  // end marker: a stage with no copies that tells the others to stop
+                const int st = gj % kStages;
+                if (gj >= kStages &&
+                    !ptx::mbar_wait_or_abort(&sm.empty[st], ((gj / kStages) - 1) & 1, abort)) {
+                    raise_error(ws, abort);
+                } else {
+                    sm.st[st].info = make_int4(0, 0, 0, 1);
+                    ptx::mbar_arrive(&sm.full[st]);
+                }
+            } else {  // let copies already in flight land before the CTA leaves
                 volatile int never = 0;
-                const int first = issued - kStages < 0 ? 0 : issued - kStages;
-                for (int j = first; j < issued; ++j)
-                    ptx::mbar_wait_or_abort(&sm.full[j % kStages], (j / kStages) & 1, &never);
+                const int first = gj - kStages < 0 ? 0 : gj - kStages;
+                for (int k2 = first; k2 < gj; ++k2)  // stages issued so far
+                    ptx::mbar_wait_or_abort(&sm.full[k2 % kStages], (k2 / kStages) & 1, &never);
             }
         }
     } else if (warp == 5) {
@@ -196,20 +239,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
             constexpr uint32_t id_w = ptx::idesc_bf16(64, NV) | kBMajorMN;
-            for (int j = 0; j < nch; ++j) {
-                const int st = j % kStages;
-                if (!ptx::mbar_wait_or_abort(&sm.uready, j & 1, abort)) break;
+            for (int gj = 0;; ++gj) {
+                const int st = gj % kStages;
+                if (!ptx::mbar_wait_or_abort(&sm.full[st], (gj / kStages) & 1, abort)) break;
+                if (sm.st[st].info.w) break;  // end marker
+                if (!ptx::mbar_wait_or_abort(&sm.uready, gj & 1, abort)) break;
                 ptx::tc_fence_after();
                 const uint32_t qa = ptx::smem_u32(sm.st[st].QG), pa = ptx::smem_u32(sm.st[st].P);
-                const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
-                const uint32_t d3 = tmem + kColD3 + (uint32_t)(j & 1) * NV;
+                const uint32_t sop = sop0 + (uint32_t)(gj & 1) * (NV * DK * 2);
+                const uint32_t d3 = tmem + kColD3 + (uint32_t)(gj & 1) * NV;
                 ptx::mma_chain<DK / 16>(d3, ptx::smem_desc(qa, 1024, 128), 2048,  // D3 = QG S
                                         ptx::smem_desc(sop, (NV / 8) * 128, 128), 2 * (NV / 8) * 128,
                                         id_w, false);
                 ptx::mma_chain<kChunk / 16>(d3, ptx::smem_desc(pa, 1024, 128), 2048,  // D3 += P U
                                             ptx::smem_desc(uop, (NV / 8) * 128, 128),
                                             2 * (NV / 8) * 128, id_w, true);
-                ptx::mma_commit(&sm.d3[j & 1]);
+                ptx::mma_commit(&sm.d3[gj & 1]);
                 ptx::mma_commit(&sm.empty[st]);
             }
             volatile int never = 0;  // its MMAs complete before TMEM is released
@@ -226,59 +271,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t id_w = ptx::idesc_bf16(64, NV) | kBMajorMN;
         constexpr uint32_t id_k = ptx::idesc_bf16(DK, NV) | kBMajorMN;
         float S[NV];
-        const size_t srow = ((size_t)s * d.H + h) * DK;
-        if (ch >= 0) {
 #pragma unroll
-            for (int n = 0; n < NV; ++n) S[n] = h0 ? h0[(srow + ch) * DV + vt * NV + n] : 0.f;
-#pragma unroll
-            for (int nb = 0; nb < NV; nb += 8)
-                *reinterpret_cast<uint4*>(&sm.Sop[0][nmaj_index(nb, ch)]) =
-                    make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
-                               pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
+        for (int n = 0; n < NV; ++n) S[n] = 0.f;
         // Exits are collective: a failed wait in any epilogue thread is folded into
         // the next named-barrier reduction, so all 128 threads leave the loop at the
         // same point and none is left waiting at a barrier.
-        bool ok = epi_sync_and(true);
-        int4 prev = make_int4(0, 0, 0, 0);
-        for (int j = 0; j <= nch && ok; ++j) {
-            const int st = j % kStages;
-            bool okl = true;
-            // -------- issue GEMM1 of chunk j: D1 = W S
-            if (j < nch && tid == 0) {
-                okl = ptx::mbar_wait_or_abort(&sm.full[st], (j / kStages) & 1, abort);
-                if (okl) {
-                    ptx::tc_fence_after();
-                    const uint32_t wa = ptx::smem_u32(sm.st[st].W);
-                    const uint32_t sop = sop0 + (uint32_t)(j & 1) * (NV * DK * 2);
-                    ptx::mma_chain<DK / 16>(tmem + kColD1, ptx::smem_desc(wa, 1024, 128), 2048,
-                                            ptx::smem_desc(sop, (NV / 8) * 128, 128),
-                                            2 * (NV / 8) * 128, id_w, false);
-                    ptx::mma_commit(&sm.d1);
+        bool ok = true;
+        bool have_prev = false;
+        int4 prev_row = make_int4(0, 0, 0, 0);   // {first token row, rows, head, value tile}
+        for (int gj = 0; ok; ++gj) {
+            const int st = gj % kStages;
+            bool okl = __all_sync(0xffffffffu,
+                                  ptx::mbar_wait_or_abort(&sm.full[st], (gj / kStages) & 1, abort));
+            ok = epi_sync_and(okl);
+            if (!ok) break;
+            const int4 it = sm.st[st].item, info = sm.st[st].info;
+            const bool end = info.w != 0;
+            // -------- a new item: its initial state into S and the bf16 copy
+            if (!end && it.w == 0) {
+                if (ch >= 0) {
+                    const size_t srow = ((size_t)it.x * d.H + it.y) * DK + ch;
+#pragma unroll
+                    for (int n = 0; n < NV; n += 4) {
+                        float4 v4 = h0 ? *reinterpret_cast<const float4*>(&h0[srow * DV + it.z * NV + n])
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                        S[n] = v4.x; S[n + 1] = v4.y; S[n + 2] = v4.z; S[n + 3] = v4.w;
+                    }
+#pragma unroll
+                    for (int nb = 0; nb < NV; nb += 8)
+                        *reinterpret_cast<uint4*>(&sm.Sop[gj & 1][nmaj_index(nb, ch)]) =
+                            make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
+                                       pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
                 }
+                ptx::fence_proxy_async_smem();
+                epi_sync_and(true);
             }
-            // -------- output of chunk j - 1 (overlaps GEMM1 of chunk j)
-            if (j > 0) {
-                okl = okl && ptx::mbar_wait_or_abort(&sm.d3[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
-                okl = __all_sync(0xffffffffu, okl);
+            // -------- issue GEMM1 of this step: D1 = W S
+            if (!end && tid == 0) {
+                ptx::tc_fence_after();
+                const uint32_t wa = ptx::smem_u32(sm.st[st].W);
+                const uint32_t sop = sop0 + (uint32_t)(gj & 1) * (NV * DK * 2);
+                ptx::mma_chain<DK / 16>(tmem + kColD1, ptx::smem_desc(wa, 1024, 128), 2048,
+                                        ptx::smem_desc(sop, (NV / 8) * 128, 128),
+                                        2 * (NV / 8) * 128, id_w, false);
+                ptx::mma_commit(&sm.d1);
+            }
+            // -------- output of the previous step (overlaps GEMM1)
+            if (have_prev) {
+                okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(
+                                                  &sm.d3[(gj - 1) & 1], ((gj - 1) >> 1) & 1, abort));
                 if (okl) {
                     ptx::tc_fence_after();
                     float acc[NV];
-                    tmem_ld32(tmem + lane_base + kColD3 + (uint32_t)((j - 1) & 1) * NV, acc);
-                    if (ur >= 0 && ur < prev.z)
-                        store_row(o + ((size_t)(prev.y + ur) * d.H + h) * DV + vt * NV, acc, scale);
+                    tmem_ld32(tmem + lane_base + kColD3 + (uint32_t)((gj - 1) & 1) * NV, acc);
+                    if (ur >= 0 && ur < prev_row.y)
+                        store_row(o + ((size_t)(prev_row.x + ur) * d.H + prev_row.z) * DV +
+                                      prev_row.w * NV,
+                                  acc, scale);
                 }
             }
-            if (j == nch) {
+            if (end) {
                 ok = epi_sync_and(okl);
                 break;
             }
-            const int4 chk = chunks[c0 + j];
             // -------- U = u - D1  ->  Uop
-            okl = okl && ptx::mbar_wait_or_abort(&sm.d1, j & 1, abort) &&
-                  ptx::mbar_wait_or_abort(&sm.full[st], (j / kStages) & 1, abort);
+            okl = okl && ptx::mbar_wait_or_abort(&sm.d1, gj & 1, abort);
             okl = __all_sync(0xffffffffu, okl);
             if (okl) {
                 ptx::tc_fence_after();
@@ -316,15 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_commit(&sm.d2);
                 ptx::mma_commit(&sm.empty[st]);
             }
-            // -------- S <- GL * S + D2  ->  Sop[(j + 1) & 1]
-            okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&sm.d2, j & 1, abort));
+            // -------- S <- GL * S + D2  ->  Sop[(gj + 1) & 1]
+            okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&sm.d2, gj & 1, abort));
             if (okl) {
                 ptx::tc_fence_after();
                 float acc[NV];
                 tmem_ld32(tmem + lane_base + kColD2, acc);
                 if (ch >= 0) {
                     const float gl = sm.st[st].GL[ch];
-                    __nv_bfloat16* so = sm.Sop[(j + 1) & 1];
+                    __nv_bfloat16* so = sm.Sop[(gj + 1) & 1];
 #pragma unroll
                     for (int nb = 0; nb < NV; nb += 8) {
 #pragma unroll
@@ -333,21 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
                                        pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
                     }
+                    if (hT && it.w == info.x - 1) {  // the item's last chunk: its final state
+                        const size_t srow = ((size_t)it.x * d.H + it.y) * DK + ch;
+#pragma unroll
+                        for (int n = 0; n < NV; n += 4)
+                            *reinterpret_cast<float4*>(&hT[srow * DV + it.z * NV + n]) =
+                                make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
+                    }
                 }
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ok = epi_sync_and(okl);
             if (ok && tid == 0) ptx::mbar_arrive(&sm.empty[st]);  // U0, GL of this stage read
-            prev = chk;
+            prev_row = make_int4(info.y, info.z, it.y, it.z);
+            have_prev = true;
         }
         if (!ok) raise_error(ws, abort);
-        if (hT && ch >= 0) {
-#pragma unroll
-            for (int n = 0; n < NV; n += 4)
-                *reinterpret_cast<float4*>(&hT[(srow + ch) * DV + vt * NV + n]) =
-                    make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
-        }
         if (tid == 0) {  // every issued MMA completes before TMEM is released
             volatile int never = 0;
             ptx::mma_commit(&sm.fin);
@@ -369,8 +428,9 @@ cudaError_t launch_t(const Dims& d, const float* h0, float scale, void* o, float
     const size_t smem = sizeof(ChainSmem<DK>);
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)d.N * d.H * (DV / NV);
-    if (grid == 0) return cudaSuccess;
+    const long long items = (long long)d.N * d.H * (DV / NV);
+    if (items == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)(items < num_sms() ? items : num_sms());  // persistent
     kern<<<grid, kThreads, smem, stream>>>(d, h0, scale, static_cast<TOut*>(o), hT, ws);
     return cudaGetLastError();
 }

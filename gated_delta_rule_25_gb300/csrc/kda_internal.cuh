@@ -1,7 +1,7 @@
 // Internal definitions shared by the KDA kernels and the C-ABI layer.
 //
 // Workspace (caller-owned, 256-byte aligned), carved as:
-//   [0, 256)        header: u32 error word, i32 total chunk count
+//   [0, 256)        header: u32 error word, i32 total chunk count, i32 work counter
 //   seq_first       int32[N + 1]: index of the first chunk of each sequence
 //   order           int32[N]:     sequences by decreasing chunk count (longest first)
 //   chunks          int4[Cmax]:   {sequence, first token row, valid rows L, 0}
@@ -97,6 +97,7 @@ __host__ __device__ inline int op_index(int r, int k, int R) {
 struct Header {
     uint32_t error;
     int32_t total_chunks;
+    int32_t next_item;  // work counter of the persistent state kernel (reset per call)
 };
 
 // Raises a kernel's dynamic shared-memory limit once per device (the attribute
@@ -115,15 +116,10 @@ cudaError_t ensure_smem(Kernel kern, size_t bytes) {
 // Launchers (each enqueues on `stream`; return cudaGetLastError()).
 cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
                             cudaStream_t stream);
-cudaError_t launch_prep(const Dims& d, bool qkv_bf16, const void* q, const void* k,
-                        const void* v, const float* g, const float* beta, uint8_t* ws,
-                        cudaStream_t stream);
 cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, const void* q, const void* k,
                            const void* v, const float* g, const float* beta, uint8_t* ws,
                            cudaStream_t stream);
 cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                          float* hT, uint8_t* ws, cudaStream_t stream);
-cudaError_t launch_chain_simt(const Dims& d, bool qkv_bf16, const float* h0, float scale,
-                              void* o, float* hT, uint8_t* ws, cudaStream_t stream);
 
 }  // namespace kda

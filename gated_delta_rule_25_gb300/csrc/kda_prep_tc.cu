@@ -66,12 +66,12 @@ struct __align__(128) PrepSmem {
     int abort;
 };
 
+// 8 elements from 16-byte words: one word of bf16, or two of fp32.
 template <typename TIn>
-__device__ inline void load8(const TIn* p, float (&x)[8]);
+__device__ inline void unpack8(const uint4* w, float (&x)[8]);
 template <>
-__device__ inline void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+__device__ inline void unpack8<__nv_bfloat16>(const uint4* w, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float2 f = __bfloat1622float2(h[i]);
@@ -80,11 +80,10 @@ __device__ inline void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8
     }
 }
 template <>
-__device__ inline void load8<float>(const float* p, float (&x)[8]) {
-    float4 a = *reinterpret_cast<const float4*>(p);
-    float4 b = *reinterpret_cast<const float4*>(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+__device__ inline void unpack8<float>(const uint4* w, float (&x)[8]) {
+    const float* f = reinterpret_cast<const float*>(w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = f[i];
 }
 
 __device__ inline uint32_t pack_bf16(float a, float b) {
@@ -255,21 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const WsLayout W(d);
     const Header* hdr = reinterpret_cast<const Header*>(ws + W.header);
-    const int c = blockIdx.x, h = blockIdx.y;
-    if (c >= hdr->total_chunks) return;
-    const int4 chk = reinterpret_cast<const int4*>(ws + W.chunks)[c];
-    const long long row0 = chk.y;
-    const int L = chk.z;
+    const int4* chunk_tab = reinterpret_cast<const int4*>(ws + W.chunks);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = d.H;
     const FactorLayout F(DK, DV);
-    uint8_t* fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
-    __nv_bfloat16* gW = reinterpret_cast<__nv_bfloat16*>(fb + F.w);
-    __nv_bfloat16* gQG = reinterpret_cast<__nv_bfloat16*>(fb + F.qg);
-    __nv_bfloat16* gKT = reinterpret_cast<__nv_bfloat16*>(fb + F.kt);
-    __nv_bfloat16* gP = reinterpret_cast<__nv_bfloat16*>(fb + F.p);
-    __nv_bfloat16* gU = reinterpret_cast<__nv_bfloat16*>(fb + F.u0);
-    float* gGL = reinterpret_cast<float*>(fb + F.gl);
 
     if (tid == 0) {
         ptx::mbar_init(&sm.bar, 1);
@@ -280,52 +268,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(&sm.tmem, 256);
         ptx::tmem_relinquish();
     }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem;
 
-    // ---------------------------------------------------------------- P1: load
-    // 16-byte chunks: consecutive lanes take consecutive chunks of a row, so the
+    // Persistent: items are (chunk, head) pairs, item = head * cmax + chunk, taken
+    // in steps of the grid size; chunk slots past the schedule's total are skipped.
+    const int total = hdr->total_chunks;
+    const long long cmax = W.cmax, n_items = cmax * H;
+    auto valid_from = [&](long long it) {
+        while (it < n_items && (it % cmax) >= total) it += gridDim.x;
+        return it;
+    };
+    // 16-byte load chunks: consecutive lanes take consecutive chunks of a row, so the
     // shared-memory stores are conflict free and a row's lanes reduce its norm.
-    // Every load of the thread is issued before any is used (one DRAM latency).
-    {
-        constexpr int CPR = DK / 8;            // chunks per row
-        constexpr int RP = kThreads / CPR;     // rows per pass
-        constexpr int NP = kChunk / RP;        // passes
-        constexpr int VPR = DV / 8;
-        constexpr int VRP = kThreads / VPR;
-        constexpr int NVP = kChunk / VRP;
-        const int ck = tid % CPR, rsub = tid / CPR;
-        const int vk = tid % VPR, vsub = tid / VPR;
-        float xq[NP][8], xk[NP][8], xg[NP][8], xv[NVP][8];
+    constexpr int CPR = DK / 8, RP = kThreads / CPR, NP = kChunk / RP;
+    constexpr int VPR = DV / 8, VRP = kThreads / VPR, NVP = kChunk / VRP;
+    const int ck = tid % CPR, rsub = tid / CPR;
+    const int vk = tid % VPR, vsub = tid / VPR;
+    // The next item's raw inputs (16-byte words, bf16 still packed), loaded into
+    // registers while this item finishes.
+    constexpr int QW = (int)sizeof(TIn) / 2;  // 16-byte words per 8 elements
+    uint4 rq[NP][QW], rk[NP][QW], rg[NP][2], rv[NVP][QW];
+    float rb = 0.f;
+    auto issue_loads = [&](long long it) {
+        const int cc = (int)(it % cmax), hh = (int)(it / cmax);
+        const int4 nk = chunk_tab[cc];
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = rsub + p * RP;
-            if (r < L) {
-                const size_t off = ((size_t)(row0 + r) * H + h) * DK + ck * 8;
-                load8<TIn>(q + off, xq[p]);
-                load8<TIn>(k + off, xk[p]);
-                load8<float>(g + off, xg[p]);
-            } else {
+            const bool ok_r = r < nk.z;
+            const size_t off = ((size_t)(nk.y + (ok_r ? r : 0)) * H + hh) * DK + ck * 8;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xq[p][e] = xk[p][e] = xg[p][e] = 0.f;
+            for (int w2 = 0; w2 < QW; ++w2) {
+                rq[p][w2] = ok_r ? reinterpret_cast<const uint4*>(q + off)[w2] : make_uint4(0, 0, 0, 0);
+                rk[p][w2] = ok_r ? reinterpret_cast<const uint4*>(k + off)[w2] : make_uint4(0, 0, 0, 0);
             }
+#pragma unroll
+            for (int w2 = 0; w2 < 2; ++w2)
+                rg[p][w2] = ok_r ? reinterpret_cast<const uint4*>(g + off)[w2] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int p = 0; p < NVP; ++p) {
             const int r = vsub + p * VRP;
-            if (r < L) load8<TIn>(v + ((size_t)(row0 + r) * H + h) * DV + vk * 8, xv[p]);
-            else {
+            const bool ok_r = r < nk.z;
+            const size_t off = ((size_t)(nk.y + (ok_r ? r : 0)) * H + hh) * DV + vk * 8;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xv[p][e] = 0.f;
-            }
+            for (int w2 = 0; w2 < QW; ++w2)
+                rv[p][w2] = ok_r ? reinterpret_cast<const uint4*>(v + off)[w2] : make_uint4(0, 0, 0, 0);
         }
-        const float bt = (tid < kChunk && tid < L) ? beta[(size_t)(row0 + tid) * H + h] : 0.f;
+        rb = (tid < kChunk && tid < nk.z) ? beta[(size_t)(nk.y + tid) * H + hh] : 0.f;
+    };
+
+    long long item = valid_from(blockIdx.x);
+    if (item < n_items) issue_loads(item);
+    uint32_t phase = 0;
+    while (item < n_items) {
+    const int c = (int)(item % cmax), h = (int)(item / cmax);
+    const long long next = valid_from(item + gridDim.x);
+    uint8_t* fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
+    __nv_bfloat16* gW = reinterpret_cast<__nv_bfloat16*>(fb + F.w);
+    __nv_bfloat16* gQG = reinterpret_cast<__nv_bfloat16*>(fb + F.qg);
+    __nv_bfloat16* gKT = reinterpret_cast<__nv_bfloat16*>(fb + F.kt);
+    __nv_bfloat16* gP = reinterpret_cast<__nv_bfloat16*>(fb + F.p);
+    __nv_bfloat16* gU = reinterpret_cast<__nv_bfloat16*>(fb + F.u0);
+    float* gGL = reinterpret_cast<float*>(fb + F.gl);
+
+    // ---------------------------------------------------------------- P1: load
+    // (the loads were issued earlier) normalise q and k, alpha = exp(g), stage v
+    {
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = rsub + p * RP;
+            float xq[8], xk[8], xg[8];
+            unpack8<TIn>(rq[p], xq);
+            unpack8<TIn>(rk[p], xk);
+            unpack8<float>(rg[p], xg);
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                sq = fmaf(xq[p][e], xq[p][e], sq);
-                sk = fmaf(xk[p][e], xk[p][e], sk);
+                sq = fmaf(xq[e], xq[e], sq);
+                sk = fmaf(xk[e], xk[e], sk);
             }
 #pragma unroll
             for (int o = 1; o < CPR; o <<= 1) {
@@ -338,42 +362,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* da = &sm.al[r * DK + ck * 8];
 #pragma unroll
             for (int e = 0; e < 8; e += 4) {
-                *reinterpret_cast<float4*>(dq + e) = make_float4(xq[p][e] * iq, xq[p][e + 1] * iq,
-                                                                 xq[p][e + 2] * iq, xq[p][e + 3] * iq);
-                *reinterpret_cast<float4*>(dk_ + e) = make_float4(xk[p][e] * ik, xk[p][e + 1] * ik,
-                                                                  xk[p][e + 2] * ik, xk[p][e + 3] * ik);
-                *reinterpret_cast<float4*>(da + e) =
-                    make_float4(__expf(xg[p][e]), __expf(xg[p][e + 1]), __expf(xg[p][e + 2]),
-                                __expf(xg[p][e + 3]));
+                *reinterpret_cast<float4*>(dq + e) = make_float4(xq[e] * iq, xq[e + 1] * iq,
+                                                                 xq[e + 2] * iq, xq[e + 3] * iq);
+                *reinterpret_cast<float4*>(dk_ + e) = make_float4(xk[e] * ik, xk[e + 1] * ik,
+                                                                  xk[e + 2] * ik, xk[e + 3] * ik);
+                *reinterpret_cast<float4*>(da + e) = make_float4(__expf(xg[e]), __expf(xg[e + 1]),
+                                                                 __expf(xg[e + 2]), __expf(xg[e + 3]));
             }
         }
 #pragma unroll
-        for (int p = 0; p < NVP; ++p)
-            *reinterpret_cast<uint4*>(&sm.vs[(vsub + p * VRP) * DV + vk * 8]) = pack8(xv[p]);
-        if (tid < kChunk) sm.bs[tid] = bt;
+        for (int p = 0; p < NVP; ++p) {
+            float xv[8];
+            unpack8<TIn>(rv[p], xv);
+            *reinterpret_cast<uint4*>(&sm.vs[(vsub + p * VRP) * DV + vk * 8]) = pack8(xv);
+        }
+        if (tid < kChunk) sm.bs[tid] = rb;
     }
     __syncthreads();
 
-    // Warm L2 with the inputs of the CTA one wave ahead (it runs next on some SM),
-    // so that its loads do not all hit DRAM at the same moment as this wave's.
+    // Warm L2 with the inputs of the item after next, so that its register loads
+    // (issued during the next item) find them there.
     {
-        const long long lin = (long long)blockIdx.y * gridDim.x + blockIdx.x + nsm;
-        if (lin < (long long)gridDim.x * gridDim.y) {
-            const int cx = (int)(lin % gridDim.x), hy = (int)(lin / gridDim.x);
-            if (cx < hdr->total_chunks) {
-                const int4 nk = reinterpret_cast<const int4*>(ws + W.chunks)[cx];
-                constexpr int LQ = DK * (int)sizeof(TIn) / 128, LG = DK * 4 / 128;
-                constexpr int LV = DV * (int)sizeof(TIn) / 128, LR = 2 * LQ + LG + LV;
-                for (int e = tid; e < nk.z * LR; e += kThreads) {
-                    const int r = e / LR, li = e % LR;
-                    const size_t row = (size_t)(nk.y + r) * H + hy;
-                    const char* p;
-                    if (li < LQ) p = reinterpret_cast<const char*>(q + row * DK) + li * 128;
-                    else if (li < 2 * LQ) p = reinterpret_cast<const char*>(k + row * DK) + (li - LQ) * 128;
-                    else if (li < 2 * LQ + LG) p = reinterpret_cast<const char*>(g + row * DK) + (li - 2 * LQ) * 128;
-                    else p = reinterpret_cast<const char*>(v + row * DV) + (li - 2 * LQ - LG) * 128;
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-                }
+        const long long nn = valid_from(next + gridDim.x);
+        if (nn < n_items) {
+            const int cx = (int)(nn % cmax), hy = (int)(nn / cmax);
+            const int4 nk = chunk_tab[cx];
+            constexpr int LQ = DK * (int)sizeof(TIn) / 128, LG = DK * 4 / 128;
+            constexpr int LV = DV * (int)sizeof(TIn) / 128, LR = 2 * LQ + LG + LV;
+            for (int e = tid; e < nk.z * LR; e += kThreads) {
+                const int r = e / LR, li = e % LR;
+                const size_t row = (size_t)(nk.y + r) * H + hy;
+                const char* p;
+                if (li < LQ) p = reinterpret_cast<const char*>(q + row * DK) + li * 128;
+                else if (li < 2 * LQ) p = reinterpret_cast<const char*>(k + row * DK) + (li - LQ) * 128;
+                else if (li < 2 * LQ + LG) p = reinterpret_cast<const char*>(g + row * DK) + (li - 2 * LQ) * 128;
+                else p = reinterpret_cast<const char*>(v + row * DV) + (li - 2 * LQ - LG) * 128;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
             }
         }
     }
@@ -716,7 +740,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = sm.tmem;
 
     // ------------------------------------------------- P7: [w | u] on tcgen05
     if (tid == 0) {
@@ -729,7 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kk > 0);
         ptx::mma_commit(&sm.bar);
     }
-    const bool ok = ptx::mbar_wait_or_abort(&sm.bar, 0, &sm.abort);
+    if (next < n_items) issue_loads(next);  // lands while the MMA and its epilogue run
+    const bool ok = ptx::mbar_wait_or_abort(&sm.bar, phase, &sm.abort);
     if (!ok && tid == 0) atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
     ptx::tc_fence_after();
     {
@@ -760,6 +784,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::tc_fence_after();
+    phase ^= 1u;
+    item = next;
+    }  // items
+    ptx::tc_fence_before();
+    __syncthreads();
     if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 256);
@@ -775,7 +805,8 @@ cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v,
     if (W.cmax == 0) return cudaSuccess;
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)W.cmax, (unsigned)d.H);
+    const long long items = W.cmax * d.H;
+    const unsigned grid = (unsigned)(items < num_sms() ? items : num_sms());  // persistent
     kern<<<grid, kThreads, smem, stream>>>(d, static_cast<const TIn*>(q), static_cast<const TIn*>(k),
                                            static_cast<const TIn*>(v), g, beta, ws, num_sms());
     return cudaGetLastError();

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         if (tid == 0) {
             hdr->error = kDevErrCuSeqlens;
             hdr->total_chunks = 0;
+            hdr->next_item = 0;
         }
         return;
     }
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         seq_first[d.N] = carry;
         hdr->error = 0;
         hdr->total_chunks = carry;
+        hdr->next_item = 0;
     }
     // Longest chains first: the state kernel maps its CTAs through this order so
     // that a dominant sequence starts at once instead of after the short ones.
