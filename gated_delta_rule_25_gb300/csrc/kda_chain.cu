@@ -6,17 +6,24 @@
 // Attention", section THE MECHANISM: the state moves sequentially between blocks
 // of tokens; "NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section
 // 01 RESULTS: the recurrent state must stay fp32, a bf16 state loses accuracy):
-//   U  = u - w S                                   GEMM1  M=64,  N=32, K=dk
+//   [w S ; QG S]  = [w ; QG] S                     GEMM1  M=128, N=32, K=dk
+//   U  = u - w S
 //   S <- Diag(exp(Gamma_L)) S + KT U               GEMM2  M=dk,  N=32, K=64
-//   O  = scale ((qh * exp(Gamma)) S + P U)         GEMM3  M=64,  N=32, K=dk + 64
-// S lives in fp32 registers of the four epilogue warps (one key channel per
-// thread).  bf16 copies of S and U in shared memory (N-major) are the B operands
-// of the MMAs, which accumulate in fp32 in tensor memory.
+//   O  = scale (QG S + P U)                        GEMM3  M=128, N=32, K=64
+// (QG = qh * exp(Gamma)).  w and QG arrive as one 128-row operand tile, so one
+// product gives both w S (accumulator rows 0-63) and QG S (rows 64-127).  GEMM3
+// accumulates P U onto rows 64-127 of the same accumulator: its A descriptor
+// starts one 8-row block-row group (1 KB) before the 64-row P tile, so that rows
+// 64-127 of the 128-row operand are exactly P (rows 0-63, already consumed, pick
+// up a dead sum).  S lives in fp32 registers of the four epilogue warps (one key
+// channel per thread).  bf16 copies of S and U in shared memory (N-major) are the
+// B operands of the MMAs, which accumulate in fp32 in tensor memory.
 //
 // Only GEMM1 and GEMM2 are on the serial path.  Per chunk: thread 0 issues GEMM1;
-// while it runs, the epilogue stores the previous chunk's output; then U is formed
-// from D1, a named barrier, thread 0 issues GEMM2 (and signals warp 5, which
-// issues GEMM3), S is updated from D2, a named barrier, and the next chunk starts.
+// warps 0-1 form U from its rows 0-63 while warps 2-3 store the previous chunk's
+// output (rows 64-127 of the other accumulator buffer); a named barrier; thread 0
+// issues GEMM2 (and signals warp 5, which issues GEMM3), S is updated from D2, a
+// named barrier, and the next chunk starts.
 //
 // The kernel is persistent (one CTA per SM): the producer warp takes work items
 // (sequence, head, value tile), longest sequences first, from a counter in the
@@ -43,8 +50,7 @@ constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-
 
 template <int DK>
 struct __align__(128) ChainStage {
-    __nv_bfloat16 W[kChunk * DK];    // operand layout, 64 x DK
-    __nv_bfloat16 QG[kChunk * DK];   // operand layout, 64 x DK
+    __nv_bfloat16 WQ[2 * kChunk * DK];  // operand layout, 128 x DK: rows w, then QG
     __nv_bfloat16 KT[DK * kChunk];   // operand layout, DK x 64
     __nv_bfloat16 P[kChunk * kChunk];
     __nv_bfloat16 U0[kChunk * NV];   // row-major 64 x 32 slab of u
@@ -56,15 +62,15 @@ struct __align__(128) ChainStage {
 template <int DK>
 struct __align__(128) ChainSmem {
     ChainStage<DK> st[kStages];
-    __nv_bfloat16 Sop[2][NV * DK];   // N-major operand (B of GEMM1 / GEMM3a), two copies
-    __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM2 / GEMM3b)
+    __nv_bfloat16 Sop[2][NV * DK];   // N-major operand (B of GEMM1), two copies
+    __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM2 / GEMM3)
     uint64_t full[kStages], empty[kStages], d1, d2, d3[2], uready, fin, fin3;
     uint32_t tmem_base;
     int abort;
 };
 
-// TMEM columns: D1 [0, 32), D2 [32, 64), D3 double buffer [64, 128).
-constexpr uint32_t kColD1 = 0, kColD2 = 32, kColD3 = 64, kTmemCols = 128;
+// TMEM columns: D1 (GEMM1, then GEMM3 on top) double buffer [0, 64), D2 [64, 96).
+constexpr uint32_t kColD1 = 0, kColD2 = 64, kTmemCols = 128;
 
 // Element index of (n, k) in an N-major, unswizzled operand with N = 32 rows:
 // 8 x 8 core matrices, 8 consecutive n contiguous, n-blocks fastest.
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 4) {
         // ------------------------------------------------ work items + producer
-        const uint32_t main_bytes = (uint32_t)(F.u0 - F.w);  // W, QG, KT, P back to back
+        const uint32_t main_bytes = (uint32_t)(F.u0 - F.wq);  // WQ, KT, P back to back
         const uint32_t u_bytes = kChunk * NV * 2, gl_bytes = DK * 4;
         int gj = 0;
         bool okp = true;
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sm.st[st].info = make_int4(nch, chk.y, chk.z, 0);
                         const uint8_t* fb = ws + W.factors + ((size_t)(c0 + j) * d.H + hh) * W.factor_bytes;
                         ptx::mbar_arrive_expect_tx(&sm.full[st], main_bytes + u_bytes + gl_bytes);
-                        ptx::bulk_g2s(sm.st[st].W, fb + F.w, main_bytes, &sm.full[st]);
+                        ptx::bulk_g2s(sm.st[st].WQ, fb + F.wq, main_bytes, &sm.full[st]);
                         ptx::bulk_g2s(sm.st[st].U0, fb + F.u0 + (size_t)vtt * u_bytes, u_bytes,
                                       &sm.full[st]);
                         ptx::bulk_g2s(sm.st[st].GL, fb + F.gl, gl_bytes, &sm.full[st]);
@@ -237,23 +243,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 5) {
         // ------------------------------------------------------------ GEMM3 issue
         if (lane == 0) {
-            const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
-            constexpr uint32_t id_w = ptx::idesc_bf16(64, NV) | kBMajorMN;
+            const uint32_t uop = ptx::smem_u32(sm.Uop);
+            constexpr uint32_t id_o = ptx::idesc_bf16(128, NV) | kBMajorMN;
             for (int gj = 0;; ++gj) {
                 const int st = gj % kStages;
                 if (!ptx::mbar_wait_or_abort(&sm.full[st], (gj / kStages) & 1, abort)) break;
                 if (sm.st[st].info.w) break;  // end marker
                 if (!ptx::mbar_wait_or_abort(&sm.uready, gj & 1, abort)) break;
                 ptx::tc_fence_after();
-                const uint32_t qa = ptx::smem_u32(sm.st[st].QG), pa = ptx::smem_u32(sm.st[st].P);
-                const uint32_t sop = sop0 + (uint32_t)(gj & 1) * (NV * DK * 2);
-                const uint32_t d3 = tmem + kColD3 + (uint32_t)(gj & 1) * NV;
-                ptx::mma_chain<DK / 16>(d3, ptx::smem_desc(qa, 1024, 128), 2048,  // D3 = QG S
-                                        ptx::smem_desc(sop, (NV / 8) * 128, 128), 2 * (NV / 8) * 128,
-                                        id_w, false);
-                ptx::mma_chain<kChunk / 16>(d3, ptx::smem_desc(pa, 1024, 128), 2048,  // D3 += P U
+                // rows 64-127 of this A operand are the P tile (k-block stride 1 KB)
+                const uint32_t pa = ptx::smem_u32(sm.st[st].P) - 1024;
+                const uint32_t d1 = tmem + kColD1 + (uint32_t)(gj & 1) * NV;
+                ptx::mma_chain<kChunk / 16>(d1, ptx::smem_desc(pa, 1024, 128), 2048,  // D1 += P U
                                             ptx::smem_desc(uop, (NV / 8) * 128, 128),
-                                            2 * (NV / 8) * 128, id_w, true);
+                                            2 * (NV / 8) * 128, id_o, true);
                 ptx::mma_commit(&sm.d3[gj & 1]);
                 ptx::mma_commit(&sm.empty[st]);
             }
@@ -266,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w = warp, l = lane;
         const uint32_t lane_base = (uint32_t)(32 * w) << 16;
         const int ch = acc_row<DK>(w, l);     // key channel of this thread's state row
-        const int ur = acc_row<64>(w, l);     // chunk row of this thread in D1 / D3
+        const int ur = 32 * w + l;            // D1 row (lane): w S rows 0-63, output rows 64-127
         const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
-        constexpr uint32_t id_w = ptx::idesc_bf16(64, NV) | kBMajorMN;
+        constexpr uint32_t id_w = ptx::idesc_bf16(128, NV) | kBMajorMN;
         constexpr uint32_t id_k = ptx::idesc_bf16(DK, NV) | kBMajorMN;
         float S[NV];
 #pragma unroll
@@ -306,42 +309,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_proxy_async_smem();
                 epi_sync_and(true);
             }
-            // -------- issue GEMM1 of this step: D1 = W S
+            // -------- issue GEMM1 of this step: D1[gj & 1] = [w ; QG] S
             if (!end && tid == 0) {
                 ptx::tc_fence_after();
-                const uint32_t wa = ptx::smem_u32(sm.st[st].W);
+                const uint32_t wa = ptx::smem_u32(sm.st[st].WQ);
                 const uint32_t sop = sop0 + (uint32_t)(gj & 1) * (NV * DK * 2);
-                ptx::mma_chain<DK / 16>(tmem + kColD1, ptx::smem_desc(wa, 1024, 128), 2048,
+                ptx::mma_chain<DK / 16>(tmem + kColD1 + (uint32_t)(gj & 1) * NV,
+                                        ptx::smem_desc(wa, 2048, 128), 4096,
                                         ptx::smem_desc(sop, (NV / 8) * 128, 128),
                                         2 * (NV / 8) * 128, id_w, false);
                 ptx::mma_commit(&sm.d1);
             }
-            // -------- output of the previous step (overlaps GEMM1)
-            if (have_prev) {
-                okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(
-                                                  &sm.d3[(gj - 1) & 1], ((gj - 1) >> 1) & 1, abort));
+            if (w >= 2) {
+                // -------- warps 2-3: output of the previous step (overlaps GEMM1)
+                if (have_prev) {
+                    okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(
+                                                      &sm.d3[(gj - 1) & 1], ((gj - 1) >> 1) & 1, abort));
+                    if (okl) {
+                        ptx::tc_fence_after();
+                        float acc[NV];
+                        tmem_ld32(tmem + lane_base + kColD1 + (uint32_t)((gj - 1) & 1) * NV, acc);
+                        const int orow = ur - kChunk;
+                        if (orow < prev_row.y)
+                            store_row(o + ((size_t)(prev_row.x + orow) * d.H + prev_row.z) * DV +
+                                          prev_row.w * NV,
+                                      acc, scale);
+                    }
+                }
+            } else if (!end) {
+                // -------- warps 0-1: U = u - (w S)  ->  Uop
+                // (Uop is overwritten only once the previous step's GEMM3 has read it)
+                bool okw = !have_prev || ptx::mbar_wait_or_abort(&sm.d3[(gj - 1) & 1],
+                                                                 ((gj - 1) >> 1) & 1, abort);
+                okw = okw && ptx::mbar_wait_or_abort(&sm.d1, gj & 1, abort);
+                okl = __all_sync(0xffffffffu, okw);
                 if (okl) {
                     ptx::tc_fence_after();
                     float acc[NV];
-                    tmem_ld32(tmem + lane_base + kColD3 + (uint32_t)((gj - 1) & 1) * NV, acc);
-                    if (ur >= 0 && ur < prev_row.y)
-                        store_row(o + ((size_t)(prev_row.x + ur) * d.H + prev_row.z) * DV +
-                                      prev_row.w * NV,
-                                  acc, scale);
-                }
-            }
-            if (end) {
-                ok = epi_sync_and(okl);
-                break;
-            }
-            // -------- U = u - D1  ->  Uop
-            okl = okl && ptx::mbar_wait_or_abort(&sm.d1, gj & 1, abort);
-            okl = __all_sync(0xffffffffu, okl);
-            if (okl) {
-                ptx::tc_fence_after();
-                float acc[NV];
-                tmem_ld32(tmem + lane_base + kColD1, acc);
-                if (ur >= 0) {
+                    tmem_ld32(tmem + lane_base + kColD1 + (uint32_t)(gj & 1) * NV, acc);
                     const uint4* u0 = reinterpret_cast<const uint4*>(sm.st[st].U0 + ur * NV);
 #pragma unroll
                     for (int nb = 0; nb < NV; nb += 8) {
@@ -356,6 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pack_bf16(e.x - acc[nb + 6], e.y - acc[nb + 7]));
                     }
                 }
+            }
+            if (end) {
+                ok = epi_sync_and(okl);
+                break;
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();

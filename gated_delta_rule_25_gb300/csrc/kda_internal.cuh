@@ -8,8 +8,8 @@
 //   factors         per (chunk, head): the factors of the chunkwise form
 //
 // Per (chunk, head) factor block, every part a multiple of 256 bytes:
-//   W   [64 x dk] bf16, operand layout  w = (I + A)^-1 Diag(beta) (kh * exp(Gamma))
-//   QG  [64 x dk] bf16, operand layout  qh * exp(Gamma)
+//   WQ  [128 x dk] bf16, operand layout: rows 0-63 w = (I + A)^-1 Diag(beta) (kh * exp(Gamma)),
+//                                        rows 64-127 qh * exp(Gamma) (one M = 128 operand)
 //   KT  [dk x 64] bf16, operand layout  (kh * exp(Gamma_last - Gamma))^T
 //   P   [64 x 64] bf16, operand layout  sum_c qh_ic kh_jc exp(Gamma_ic - Gamma_jc), j <= i
 //   U0  [dv/32][64][32] bf16            u = (I + A)^-1 Diag(beta) v, in 32-column
@@ -58,11 +58,10 @@ __host__ __device__ inline long long max_chunks(const Dims& d) {
 }
 
 struct FactorLayout {
-    size_t w, qg, kt, p, u0, gl, bytes;
+    size_t wq, kt, p, u0, gl, bytes;
     __host__ __device__ explicit FactorLayout(int dk, int dv) {
         size_t off = 0;
-        w = off;  off += align256(size_t(kChunk) * dk * 2);
-        qg = off; off += align256(size_t(kChunk) * dk * 2);
+        wq = off; off += align256(size_t(2 * kChunk) * dk * 2);
         kt = off; off += align256(size_t(dk) * kChunk * 2);
         p = off;  off += align256(size_t(kChunk) * kChunk * 2);
         u0 = off; off += align256(size_t(kChunk) * dv * 2);

@@ -14,6 +14,8 @@
 //   X        = (I + A)^-1                                        (fp32, blocked)
 //   [w | u]  = X Diag(beta) [kh * gamma | v]                     (tcgen05, M=64 N=dk+dv K=64)
 //   QG = qh * gamma,  KT = (kh * gamma_L / gamma)^T,  GL = gamma_L,  gamma = exp(Gamma)
+// w and QG are written as the two halves of one 128-row operand tile, so that the
+// state kernel forms w S and QG S with one M = 128 product.
 //
 // Every decay factor is a product of alphas over a run of consecutive tokens, so
 // it lies in [0, 1]: deep decays underflow to zero and nothing overflows (the
@@ -328,8 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = (int)(item % cmax), h = (int)(item / cmax);
     const long long next = valid_from(item + gridDim.x);
     uint8_t* fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
-    __nv_bfloat16* gW = reinterpret_cast<__nv_bfloat16*>(fb + F.w);
-    __nv_bfloat16* gQG = reinterpret_cast<__nv_bfloat16*>(fb + F.qg);
+    __nv_bfloat16* gWQ = reinterpret_cast<__nv_bfloat16*>(fb + F.wq);  // rows: w, then qh gamma
     __nv_bfloat16* gKT = reinterpret_cast<__nv_bfloat16*>(fb + F.kt);
     __nv_bfloat16* gP = reinterpret_cast<__nv_bfloat16*>(fb + F.p);
     __nv_bfloat16* gU = reinterpret_cast<__nv_bfloat16*>(fb + F.u0);
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float2 qgv = mul2(qq[u], mul2(gb, f[u]));
-                *reinterpret_cast<uint32_t*>(&gQG[op_index(r0 + u, ch, kChunk)]) = pack_bf16(qgv.x, qgv.y);
+                *reinterpret_cast<uint32_t*>(&gWQ[op_index(kChunk + r0 + u, ch, 2 * kChunk)]) = pack_bf16(qgv.x, qgv.y);
                 const float2 ktv = mul2(kq[u], mul2(gq[u], sb));
                 kt0[u] = ktv.x;
                 kt1[u] = ktv.y;
@@ -775,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 8; ++u) y[u] = x[8 * hh + u];
                     if (col < DK)
-                        *reinterpret_cast<uint4*>(&gW[op_index(row, col, kChunk)]) = pack8(y);
+                        *reinterpret_cast<uint4*>(&gWQ[op_index(row, col, 2 * kChunk)]) = pack8(y);
                     else
                         *reinterpret_cast<uint4*>(&gU[u0_index(row, col - DK)]) = pack8(y);
                 }
