@@ -27,6 +27,9 @@
 //   * the lower-left 8 x 8 quadrant of each diagonal 16-block: the same with the
 //     reference at its first row -> mma.sync;
 //   * the eight 8 x 8 diagonal blocks: running products per channel (CUDA cores).
+#include <cuda.h>          // CUtensorMap (the encoder itself is fetched at run time)
+#include <cudaTypedefs.h>  // the encoder's function-pointer type
+
 #include "kda_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -64,6 +67,7 @@ struct __align__(128) PrepSmem {
     float bs[kChunk];
     float gb[8 * DK];  // alpha(0..8b) per block start b and channel (kept for the w operand)
     uint64_t bar;
+    uint64_t ld_bar;  // bulk copies of an item's raw inputs
     uint32_t tmem;
     int abort;
 };
@@ -245,9 +249,9 @@ __device__ __forceinline__ void inv_join(float* X, const float* A, float* T, int
 
 template <int DK, int DV, typename TIn>
 __global__ void __launch_bounds__(kThreads, 1)
-    prep_tc_kernel(Dims d, const TIn* __restrict__ q, const TIn* __restrict__ k,
-                   const TIn* __restrict__ v, const float* __restrict__ g,
-                   const float* __restrict__ beta, uint8_t* __restrict__ ws, int nsm) {
+    prep_tc_kernel(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                   const float* __restrict__ beta, uint8_t* __restrict__ ws) {
     using Sm = PrepSmem<DK, DV>;
     constexpr int AP = kChunk + 1;
     constexpr int NB = DK + DV;  // columns of the w/u product
@@ -263,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         ptx::mbar_init(&sm.bar, 1);
+        ptx::mbar_init(&sm.ld_bar, 1);
         sm.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -289,46 +294,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int VPR = DV / 8, VRP = kThreads / VPR, NVP = kChunk / VRP;
     const int ck = tid % CPR, rsub = tid / CPR;
     const int vk = tid % VPR, vsub = tid / VPR;
-    // The next item's raw inputs (16-byte words, bf16 still packed), loaded into
-    // registers while this item finishes.
-    constexpr int QW = (int)sizeof(TIn) / 2;  // 16-byte words per 8 elements
-    uint4 rq[NP][QW], rk[NP][QW], rg[NP][2], rv[NVP][QW];
-    float rb = 0.f;
-    auto issue_loads = [&](long long it) {
-        const int cc = (int)(it % cmax), hh = (int)(it / cmax);
-        const int4 nk = chunk_tab[cc];
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            const int r = rsub + p * RP;
-            const bool ok_r = r < nk.z;
-            const size_t off = ((size_t)(nk.y + (ok_r ? r : 0)) * H + hh) * DK + ck * 8;
-#pragma unroll
-            for (int w2 = 0; w2 < QW; ++w2) {
-                rq[p][w2] = ok_r ? reinterpret_cast<const uint4*>(q + off)[w2] : make_uint4(0, 0, 0, 0);
-                rk[p][w2] = ok_r ? reinterpret_cast<const uint4*>(k + off)[w2] : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int w2 = 0; w2 < 2; ++w2)
-                rg[p][w2] = ok_r ? reinterpret_cast<const uint4*>(g + off)[w2] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int p = 0; p < NVP; ++p) {
-            const int r = vsub + p * VRP;
-            const bool ok_r = r < nk.z;
-            const size_t off = ((size_t)(nk.y + (ok_r ? r : 0)) * H + hh) * DV + vk * 8;
-#pragma unroll
-            for (int w2 = 0; w2 < QW; ++w2)
-                rv[p][w2] = ok_r ? reinterpret_cast<const uint4*>(v + off)[w2] : make_uint4(0, 0, 0, 0);
-        }
-        rb = (tid < kChunk && tid < nk.z) ? beta[(size_t)(nk.y + tid) * H + hh] : 0.f;
+    // Raw inputs of an item arrive by tensor copies (TMA: one box of 64 token rows
+    // of one head per tensor, rows past the end of the tensor read as zero) into
+    // shared regions that are dead while the previous item finishes: bf16 q and k in the
+    // upper halves of qn and kn (fp32 rows are written over them only after every
+    // thread has read its raw words), g into al, v into vs (bf16) or, as fp32, into
+    // the A and X arrays.
+    constexpr bool kBf16In = sizeof(TIn) == 2;
+    uint8_t* const st_q = reinterpret_cast<uint8_t*>(sm.qn) + (kBf16In ? kChunk * DK * 2 : 0);
+    uint8_t* const st_k = reinterpret_cast<uint8_t*>(sm.kn) + (kBf16In ? kChunk * DK * 2 : 0);
+    uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.al);
+    uint8_t* const st_v = kBf16In ? reinterpret_cast<uint8_t*>(sm.vs) : reinterpret_cast<uint8_t*>(sm.A);
+    static_assert(kBf16In || kChunk * DV * 4 <= 2 * kChunk * (kChunk + 1) * 4, "v staging");
+    constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * 4, VB = DV * sizeof(TIn);
+    float rb = 0.f;  // beta of this thread's row of the next item (threads < 64)
+    // {first token row, valid rows} of an item's chunk (zeros past the last item)
+    auto rows_of = [&](long long it) {
+        if (it >= n_items) return make_int2(0, 0);
+        const int4 t = chunk_tab[it % cmax];
+        return make_int2(t.y, t.z);
+    };
+    // One thread: the four tensor copies of an item, completing on ld_bar.  Rows
+    // of the box past the chunk's end (another sequence's tokens, or zeros past the
+    // tensor) are ignored below.
+    auto issue_copies = [&](long long it, int2 nk) {
+        const int hh = (int)(it / cmax);
+        ptx::mbar_arrive_expect_tx(&sm.ld_bar, (uint32_t)kChunk * (2 * QB + GB + VB));
+        ptx::tma_load_3d(st_q, &tm_q, 0, hh, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_k, &tm_k, 0, hh, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_g, &tm_g, 0, hh, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_v, &tm_v, 0, hh, nk.x, &sm.ld_bar);
+    };
+    auto load_beta = [&](long long it, int2 nk) {
+        const int hh = (int)(it / cmax);
+        rb = (tid < kChunk && tid < nk.y) ? beta[(size_t)(nk.x + tid) * H + hh] : 0.f;
     };
 
     long long item = valid_from(blockIdx.x);
-    if (item < n_items) issue_loads(item);
+    int2 rows_cur = rows_of(item);
+    if (item < n_items) {
+        if (tid == 32) issue_copies(item, rows_cur);
+        load_beta(item, rows_cur);
+    }
+    uint32_t ld_phase = 0;
     uint32_t phase = 0;
     while (item < n_items) {
     const int c = (int)(item % cmax), h = (int)(item / cmax);
     const long long next = valid_from(item + gridDim.x);
+    const long long after = valid_from(next + gridDim.x);
+    // chunk-table lookups of the next two items, issued now and consumed later
+    const int2 rows_next = rows_of(next), rows_after = rows_of(after);
     uint8_t* fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
     __nv_bfloat16* gWQ = reinterpret_cast<__nv_bfloat16*>(fb + F.wq);  // rows: w, then qh gamma
     __nv_bfloat16* gKT = reinterpret_cast<__nv_bfloat16*>(fb + F.kt);
@@ -337,8 +352,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* gGL = reinterpret_cast<float*>(fb + F.gl);
 
     // ---------------------------------------------------------------- P1: load
-    // (the loads were issued earlier) normalise q and k, alpha = exp(g), stage v
+    // (the bulk copies were issued earlier) normalise q and k, alpha = exp(g), stage v
     {
+        if (!ptx::mbar_wait_or_abort(&sm.ld_bar, ld_phase, &sm.abort) && tid == 0)
+            atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
+        ld_phase ^= 1u;
+        const int L = rows_cur.y;
+        constexpr int QW = (int)sizeof(TIn) / 2;  // 16-byte words per 8 elements
+        uint4 rq[NP][QW], rk[NP][QW], rg[NP][2];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = rsub + p * RP;
+            const bool ok_r = r < L;
+            const uint4* wq = reinterpret_cast<const uint4*>(st_q + r * QB + ck * 8 * sizeof(TIn));
+            const uint4* wk = reinterpret_cast<const uint4*>(st_k + r * QB + ck * 8 * sizeof(TIn));
+            const uint4* wg = reinterpret_cast<const uint4*>(st_g + r * GB + ck * 32);
+#pragma unroll
+            for (int w2 = 0; w2 < QW; ++w2) {
+                rq[p][w2] = ok_r ? wq[w2] : make_uint4(0, 0, 0, 0);
+                rk[p][w2] = ok_r ? wk[w2] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int w2 = 0; w2 < 2; ++w2) rg[p][w2] = ok_r ? wg[w2] : make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();  // every raw word is read before fp32 rows overwrite them
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = rsub + p * RP;
@@ -373,34 +410,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int p = 0; p < NVP; ++p) {
-            float xv[8];
-            unpack8<TIn>(rv[p], xv);
-            *reinterpret_cast<uint4*>(&sm.vs[(vsub + p * VRP) * DV + vk * 8]) = pack8(xv);
+            const int r = vsub + p * VRP;
+            uint4* dv = reinterpret_cast<uint4*>(&sm.vs[r * DV + vk * 8]);
+            if (r >= L) {
+                *dv = make_uint4(0, 0, 0, 0);
+            } else if (!kBf16In) {  // fp32 v staged in the A / X arrays
+                float xv[8];
+                unpack8<TIn>(reinterpret_cast<const uint4*>(st_v + r * VB + vk * 8 * sizeof(TIn)), xv);
+                *dv = pack8(xv);
+            }
         }
         if (tid < kChunk) sm.bs[tid] = rb;
     }
     __syncthreads();
 
-    // Warm L2 with the inputs of the item after next, so that its register loads
+    // Warm L2 with the inputs of the item after next, so that its tensor copies
     // (issued during the next item) find them there.
-    {
-        const long long nn = valid_from(next + gridDim.x);
-        if (nn < n_items) {
-            const int cx = (int)(nn % cmax), hy = (int)(nn / cmax);
-            const int4 nk = chunk_tab[cx];
-            constexpr int LQ = DK * (int)sizeof(TIn) / 128, LG = DK * 4 / 128;
-            constexpr int LV = DV * (int)sizeof(TIn) / 128, LR = 2 * LQ + LG + LV;
-            for (int e = tid; e < nk.z * LR; e += kThreads) {
-                const int r = e / LR, li = e % LR;
-                const size_t row = (size_t)(nk.y + r) * H + hy;
-                const char* p;
-                if (li < LQ) p = reinterpret_cast<const char*>(q + row * DK) + li * 128;
-                else if (li < 2 * LQ) p = reinterpret_cast<const char*>(k + row * DK) + (li - LQ) * 128;
-                else if (li < 2 * LQ + LG) p = reinterpret_cast<const char*>(g + row * DK) + (li - 2 * LQ) * 128;
-                else p = reinterpret_cast<const char*>(v + row * DV) + (li - 2 * LQ - LG) * 128;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-            }
-        }
+    if (tid == 64 && after < n_items) {
+        const int hy = (int)(after / cmax);
+        ptx::tma_prefetch_3d(&tm_q, 0, hy, rows_after.x);
+        ptx::tma_prefetch_3d(&tm_k, 0, hy, rows_after.x);
+        ptx::tma_prefetch_3d(&tm_g, 0, hy, rows_after.x);
+        ptx::tma_prefetch_3d(&tm_v, 0, hy, rows_after.x);
     }
 
     // ------------------------------------------------ P2: decay products
@@ -620,57 +651,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------- P4: 8 x 8 diagonal blocks (CUDA cores)
-    // Thread (block, row, channel group of DK/8): channel pairs with packed fp32x2
-    // arithmetic.  The pair order is rotated so that the 64-bit shared loads of a
-    // warp use every bank pair exactly twice (two wavefronts).
+    // Thread (block, row pair {a, 7 - a}, group of DK/16 channels): row a has a + 1
+    // entries on or below the diagonal and row 7 - a has 8 - a, so every lane runs
+    // the same 9 steps.  Channel pairs use packed fp32x2 arithmetic; their order is
+    // rotated so that a warp's 64-bit shared loads take two wavefronts.  The two
+    // warps of a block each cover half of the channels and meet in shared memory.
     {
-        constexpr int CQ = DK / 8, CP = CQ / 2;
-        const int blk = warp >> 1, r4 = lane >> 3, q8 = lane & 7;
-        const int rin = 4 * (warp & 1) + r4;
-        const int r = 8 * blk + rin;
-        float2 acc2A[8], acc2P[8];
+        constexpr int CG = DK / 16, CPp = CG / 2;
+        const int blk = warp >> 1, half = warp & 1;
+        const int rp = lane >> 3, cg = (lane & 7) + 8 * half;
+        const int ra = 8 * blk + rp, rz = 8 * blk + 7 - rp;
+        float2 acc2A[9], acc2P[9];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc2A[e] = acc2P[e] = make_float2(0.f, 0.f);
-        for (int i = 0; i < CP; ++i) {
-            const int ch = q8 * CQ + 2 * ((i + (q8 >> 1) + 4 * (r4 & 1)) & (CP - 1));
-            const float2 kr = *reinterpret_cast<const float2*>(&sm.kn[r * DK + ch]);
-            const float2 qr = *reinterpret_cast<const float2*>(&sm.qn[r * DK + ch]);
+        for (int t = 0; t < 9; ++t) acc2A[t] = acc2P[t] = make_float2(0.f, 0.f);
+#pragma unroll 1
+        for (int i = 0; i < CPp; ++i) {
+            const int ch = cg * CG + 2 * ((i + 2 * ((lane >> 2) & 1) + rp) & (CPp - 1));
+            const float2 ka = *reinterpret_cast<const float2*>(&sm.kn[ra * DK + ch]);
+            const float2 qa = *reinterpret_cast<const float2*>(&sm.qn[ra * DK + ch]);
+            const float2 kz = *reinterpret_cast<const float2*>(&sm.kn[rz * DK + ch]);
+            const float2 qz = *reinterpret_cast<const float2*>(&sm.qn[rz * DK + ch]);
             float2 f = make_float2(1.f, 1.f);
 #pragma unroll
-            for (int dd = 0; dd < 8; ++dd) {
-                if (dd <= rin) {
-                    const int j = r - dd;
-                    if (dd > 0) f = mul2(f, *reinterpret_cast<const float2*>(&sm.al[(j + 1) * DK + ch]));
-                    const float2 t = mul2(*reinterpret_cast<const float2*>(&sm.kn[j * DK + ch]), f);
-                    acc2P[dd] = fma2(qr, t, acc2P[dd]);
-                    acc2A[dd] = fma2(kr, t, acc2A[dd]);
+            for (int t = 0; t < 9; ++t) {
+                const bool first = t <= rp;
+                const int j = first ? ra - t : 8 * blk + 8 - t;
+                if (t == 0 || t == rp + 1) {
+                    f = make_float2(1.f, 1.f);
+                } else {
+                    f = mul2(f, *reinterpret_cast<const float2*>(&sm.al[(j + 1) * DK + ch]));
                 }
+                const float2 tk = mul2(*reinterpret_cast<const float2*>(&sm.kn[j * DK + ch]), f);
+                acc2P[t] = fma2(first ? qa : qz, tk, acc2P[t]);
+                acc2A[t] = fma2(first ? ka : kz, tk, acc2A[t]);
             }
         }
-        float accA[8], accP[8];
+        float accA[9], accP[9];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            accA[e] = acc2A[e].x + acc2A[e].y;
-            accP[e] = acc2P[e].x + acc2P[e].y;
+        for (int t = 0; t < 9; ++t) {
+            accA[t] = acc2A[t].x + acc2A[t].y;
+            accP[t] = acc2P[t].x + acc2P[t].y;
 #pragma unroll
             for (int o = 1; o < 8; o <<= 1) {
-                accA[e] += __shfl_xor_sync(0xffffffffu, accA[e], o);
-                accP[e] += __shfl_xor_sync(0xffffffffu, accP[e], o);
+                accA[t] += __shfl_xor_sync(0xffffffffu, accA[t], o);
+                accP[t] += __shfl_xor_sync(0xffffffffu, accP[t], o);
             }
         }
-        const int qt = q8;
-        if (qt == 0) {
-            const float b = sm.bs[r];
+        float* part = sm.X + (blk * 4 + rp) * 18;  // X is free until the inverse
+        if (half == 1 && (lane & 7) == 0) {
 #pragma unroll
-            for (int dd = 0; dd < 8; ++dd) {
-                if (dd <= rin) {
-                    const int j = r - dd;
-                    if (dd > 0) sm.A[r * AP + j] = b * accA[dd];
-                    gP[op_index(r, j, kChunk)] = __float2bfloat16(accP[dd]);
-                }
+            for (int t = 0; t < 9; ++t) {
+                part[t] = accA[t];
+                part[9 + t] = accP[t];
             }
+        }
+        __syncthreads();
+        if (half == 0 && (lane & 7) == 0) {
+            const float ba = sm.bs[ra], bz = sm.bs[rz];
             const __nv_bfloat16 z = __float2bfloat16(0.f);
-            for (int j = r + 1; j < 8 * blk + 8; ++j) gP[op_index(r, j, kChunk)] = z;
+#pragma unroll
+            for (int t = 0; t < 9; ++t) {
+                const bool first = t <= rp;
+                const int r = first ? ra : rz;
+                const int j = first ? ra - t : 8 * blk + 8 - t;
+                const float a = accA[t] + part[t], pv = accP[t] + part[9 + t];
+                if (j < r) sm.A[r * AP + j] = (first ? ba : bz) * a;
+                gP[op_index(r, j, kChunk)] = __float2bfloat16(pv);
+            }
+            for (int j = ra + 1; j < 8 * blk + 8; ++j) gP[op_index(ra, j, kChunk)] = z;
+            for (int j = rz + 1; j < 8 * blk + 8; ++j) gP[op_index(rz, j, kChunk)] = z;
         }
     }
     __syncthreads();
@@ -753,7 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kk > 0);
         ptx::mma_commit(&sm.bar);
     }
-    if (next < n_items) issue_loads(next);  // lands while the MMA and its epilogue run
+    if (next < n_items) {  // lands while the MMA and its epilogue run
+        if (tid == 32) issue_copies(next, rows_next);
+        load_beta(next, rows_next);
+    }
     const bool ok = ptx::mbar_wait_or_abort(&sm.bar, phase, &sm.abort);
     if (!ok && tid == 0) atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
     ptx::tc_fence_after();
@@ -788,6 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     phase ^= 1u;
     item = next;
+    rows_cur = rows_next;
     }  // items
     ptx::tc_fence_before();
     __syncthreads();
@@ -797,19 +850,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// The driver's tensor-map encoder, fetched once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// Tensor map of a [tokens, H, D] row-major tensor with a box of 64 tokens x 1 head
+// x D channels (so one copy brings one chunk of one head).
+bool encode_rows(CUtensorMap* m, const void* base, bool f32, int D, int H, long long tokens) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {D * es, (cuuint64_t)H * D * es};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kChunk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DK, int DV, typename TIn>
 cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, uint8_t* ws, cudaStream_t stream) {
     auto kern = prep_tc_kernel<DK, DV, TIn>;
     const size_t smem = sizeof(PrepSmem<DK, DV>);
     const WsLayout W(d);
-    if (W.cmax == 0) return cudaSuccess;
+    const long long tokens = (long long)d.B * d.T;
+    if (W.cmax == 0 || tokens == 0) return cudaSuccess;  // no chunk has a token
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
+    constexpr bool f32 = sizeof(TIn) == 4;
+    CUtensorMap tq, tk, tv, tg;
+    if (!encode_rows(&tq, q, f32, DK, d.H, tokens) || !encode_rows(&tk, k, f32, DK, d.H, tokens) ||
+        !encode_rows(&tv, v, f32, DV, d.H, tokens) || !encode_rows(&tg, g, true, DK, d.H, tokens))
+        return cudaErrorInvalidValue;
     const long long items = W.cmax * d.H;
     const unsigned grid = (unsigned)(items < num_sms() ? items : num_sms());  // persistent
-    kern<<<grid, kThreads, smem, stream>>>(d, static_cast<const TIn*>(q), static_cast<const TIn*>(k),
-                                           static_cast<const TIn*>(v), g, beta, ws, num_sms());
+    kern<<<grid, kThreads, smem, stream>>>(d, tq, tk, tv, tg, beta, ws);
     return cudaGetLastError();
 }
 

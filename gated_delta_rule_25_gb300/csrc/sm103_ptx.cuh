@@ -94,6 +94,26 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
         : "memory");
 }
 
+// Tiled tensor copy (TMA) of one 3-D box described by the tensor map at `tmap`
+// (a __grid_constant__ kernel parameter) at coordinates {c0, c1, c2}, innermost
+// first, into shared memory (128-byte aligned), completing on `bar`.  Elements
+// outside the tensor read as zero; the full box counts towards the transaction.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Hint: fetch the same box into L2 without waiting.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (tensor core, bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
