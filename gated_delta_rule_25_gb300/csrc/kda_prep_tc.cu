@@ -280,13 +280,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem;
 
-    // Persistent: items are (chunk, head) pairs, item = head * cmax + chunk, taken
-    // in steps of the grid size; chunk slots past the schedule's total are skipped.
+    // Persistent: items are (chunk, head) pairs over the schedule's chunks, item
+    // i = h * total + c, taken in steps of the grid size (32-bit, no division in the
+    // loop: the step is split once into whole heads and a chunk remainder).
     const int total = hdr->total_chunks;
-    const long long cmax = W.cmax, n_items = cmax * H;
-    auto valid_from = [&](long long it) {
-        while (it < n_items && (it % cmax) >= total) it += gridDim.x;
-        return it;
+    struct Item { int c, h; };
+    const int step_c = total > 0 ? (int)(gridDim.x % (unsigned)total) : 0;
+    const int step_h = total > 0 ? (int)(gridDim.x / (unsigned)total) : H;
+    auto advance = [&](Item a) {
+        a.c += step_c;
+        a.h += step_h;
+        if (a.c >= total) { a.c -= total; ++a.h; }
+        return a;
     };
     // 16-byte load chunks: consecutive lanes take consecutive chunks of a row, so the
     // shared-memory stores are conflict free and a row's lanes reduce its norm.
@@ -309,39 +314,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * 4, VB = DV * sizeof(TIn);
     float rb = 0.f;  // beta of this thread's row of the next item (threads < 64)
     // {first token row, valid rows} of an item's chunk (zeros past the last item)
-    auto rows_of = [&](long long it) {
-        if (it >= n_items) return make_int2(0, 0);
-        const int4 t = chunk_tab[it % cmax];
+    auto rows_of = [&](Item it) {
+        if (it.h >= H) return make_int2(0, 0);
+        const int4 t = chunk_tab[it.c];
         return make_int2(t.y, t.z);
     };
     // One thread: the four tensor copies of an item, completing on ld_bar.  Rows
     // of the box past the chunk's end (another sequence's tokens, or zeros past the
     // tensor) are ignored below.
-    auto issue_copies = [&](long long it, int2 nk) {
-        const int hh = (int)(it / cmax);
+    auto issue_copies = [&](Item it, int2 nk) {
+        const int hh = it.h;
         ptx::mbar_arrive_expect_tx(&sm.ld_bar, (uint32_t)kChunk * (2 * QB + GB + VB));
         ptx::tma_load_3d(st_q, &tm_q, 0, hh, nk.x, &sm.ld_bar);
         ptx::tma_load_3d(st_k, &tm_k, 0, hh, nk.x, &sm.ld_bar);
         ptx::tma_load_3d(st_g, &tm_g, 0, hh, nk.x, &sm.ld_bar);
         ptx::tma_load_3d(st_v, &tm_v, 0, hh, nk.x, &sm.ld_bar);
     };
-    auto load_beta = [&](long long it, int2 nk) {
-        const int hh = (int)(it / cmax);
+    auto load_beta = [&](Item it, int2 nk) {
+        const int hh = it.h;
         rb = (tid < kChunk && tid < nk.y) ? beta[(size_t)(nk.x + tid) * H + hh] : 0.f;
     };
 
-    long long item = valid_from(blockIdx.x);
+    Item item = total > 0 ? Item{(int)(blockIdx.x % (unsigned)total), (int)(blockIdx.x / (unsigned)total)}
+                          : Item{0, H};
     int2 rows_cur = rows_of(item);
-    if (item < n_items) {
+    if (item.h < H) {
         if (tid == 32) issue_copies(item, rows_cur);
         load_beta(item, rows_cur);
     }
     uint32_t ld_phase = 0;
     uint32_t phase = 0;
-    while (item < n_items) {
-    const int c = (int)(item % cmax), h = (int)(item / cmax);
-    const long long next = valid_from(item + gridDim.x);
-    const long long after = valid_from(next + gridDim.x);
+    while (item.h < H) {
+    const int c = item.c, h = item.h;
+    const Item next = advance(item), after = advance(next);
     // chunk-table lookups of the next two items, issued now and consumed later
     const int2 rows_next = rows_of(next), rows_after = rows_of(after);
     uint8_t* fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
@@ -426,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Warm L2 with the inputs of the item after next, so that its tensor copies
     // (issued during the next item) find them there.
-    if (tid == 64 && after < n_items) {
-        const int hy = (int)(after / cmax);
+    if (tid == 64 && after.h < H) {
+        const int hy = after.h;
         ptx::tma_prefetch_3d(&tm_q, 0, hy, rows_after.x);
         ptx::tma_prefetch_3d(&tm_k, 0, hy, rows_after.x);
         ptx::tma_prefetch_3d(&tm_g, 0, hy, rows_after.x);
@@ -802,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kk > 0);
         ptx::mma_commit(&sm.bar);
     }
-    if (next < n_items) {  // lands while the MMA and its epilogue run
+    if (next.h < H) {  // lands while the MMA and its epilogue run
         if (tid == 32) issue_copies(next, rows_next);
         load_beta(next, rows_next);
     }
@@ -814,24 +819,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3, half = warp >> 2;
         const int row = 16 * quarter + lane;  // valid for lane < 16 (M = 64 layout)
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-        constexpr int HALF = NB / (kThreads / 128);
-#pragma unroll 1
-        for (int cb = half * HALF; cb < (half + 1) * HALF; cb += 16) {
-            float x[16];
-            ptx::tmem_ld16(tmem + lane_base + cb, x);
-            ptx::tmem_ld_wait();
-            if (ok && lane < 16) {
+        constexpr int HALF = NB / (kThreads / 128), NLD = HALF / 16;
+        float x[NLD][16];  // all of this warp's columns, then one wait
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int col = cb + 8 * hh;
-                    float y[8];
+        for (int i = 0; i < NLD; ++i) ptx::tmem_ld16(tmem + lane_base + half * HALF + 16 * i, x[i]);
+        ptx::tmem_ld_wait();
+        if (ok && lane < 16) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) y[u] = x[8 * hh + u];
-                    if (col < DK)
-                        *reinterpret_cast<uint4*>(&gWQ[op_index(row, col, 2 * kChunk)]) = pack8(y);
-                    else
-                        *reinterpret_cast<uint4*>(&gU[u0_index(row, col - DK)]) = pack8(y);
-                }
+            for (int i = 0; i < 2 * NLD; ++i) {
+                const int col = half * HALF + 8 * i;
+                float y[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) y[u] = x[i >> 1][8 * (i & 1) + u];
+                if (col < DK)
+                    *reinterpret_cast<uint4*>(&gWQ[op_index(row, col, 2 * kChunk)]) = pack8(y);
+                else
+                    *reinterpret_cast<uint4*>(&gU[u0_index(row, col - DK)]) = pack8(y);
             }
         }
     }
