@@ -615,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float b = sm.bs[row];
                 sm.A[row * AP + col] = b * accA[2 * hh];
                 sm.A[row * AP + col + 1] = b * accA[2 * hh + 1];
-                gP[op_index(row, col, kChunk)] = __float2bfloat16(accP[2 * hh]);
-                gP[op_index(row, col + 1, kChunk)] = __float2bfloat16(accP[2 * hh + 1]);
+                *reinterpret_cast<uint32_t*>(&gP[op_index(row, col, kChunk)]) =
+                    pack_bf16(accP[2 * hh], accP[2 * hh + 1]);
             }
         } else {
             // 8-level quadrant of diagonal block R: rows 16R+8.., cols 16R..
@@ -640,18 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float b = sm.bs[row];
             sm.A[row * AP + col] = b * accA[0];
             sm.A[row * AP + col + 1] = b * accA[1];
-            gP[op_index(row, col, kChunk)] = __float2bfloat16(accP[0]);
-            gP[op_index(row, col + 1, kChunk)] = __float2bfloat16(accP[1]);
-            // zero blocks of P above the diagonal: upper-right quadrant of diagonal
-            // block R and the 16 x 16 blocks (R, J > R)
-            const __nv_bfloat16 z = __float2bfloat16(0.f);
-            for (int e = lane; e < 64; e += 32) {
-                const int rr = 16 * R + (e >> 3), cc = 16 * R + 8 + (e & 7);
-                gP[op_index(rr, cc, kChunk)] = z;
-            }
-            for (int J = R + 1; J < 4; ++J)
-                for (int e = lane; e < 256; e += 32)
-                    gP[op_index(16 * R + (e >> 4), 16 * J + (e & 15), kChunk)] = z;
+            *reinterpret_cast<uint32_t*>(&gP[op_index(row, col, kChunk)]) = pack_bf16(accP[0], accP[1]);
+            // zero blocks of P above the diagonal, whole 8 x 8 core matrices (128
+            // contiguous bytes each): the upper-right quadrant of diagonal block R
+            // and the 16 x 16 blocks (R, J > R)
+            uint4* gP4 = reinterpret_cast<uint4*>(gP);
+            const uint4 z4 = make_uint4(0, 0, 0, 0);
+            if (lane < 8) gP4[op_index(16 * R, 16 * R + 8, kChunk) / 8 + lane] = z4;
+            for (int J = R + 1; J < 4; ++J)  // core matrices (2R + i, 2J + c), 8 words each
+                gP4[op_index(16 * R + 8 * (lane >> 4), 16 * J + 8 * ((lane >> 3) & 1), kChunk) / 8 +
+                    (lane & 7)] = z4;
         }
     }
 
@@ -712,19 +710,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (half == 0 && (lane & 7) == 0) {
+            // A entries into shared memory; the two P rows of the block (8 columns,
+            // zeros above the diagonal) are one 16-byte run each in the operand layout
             const float ba = sm.bs[ra], bz = sm.bs[rz];
-            const __nv_bfloat16 z = __float2bfloat16(0.f);
+            float pa[8], pz[8], pv[9];
 #pragma unroll
             for (int t = 0; t < 9; ++t) {
                 const bool first = t <= rp;
                 const int r = first ? ra : rz;
                 const int j = first ? ra - t : 8 * blk + 8 - t;
-                const float a = accA[t] + part[t], pv = accP[t] + part[9 + t];
-                if (j < r) sm.A[r * AP + j] = (first ? ba : bz) * a;
-                gP[op_index(r, j, kChunk)] = __float2bfloat16(pv);
+                if (j < r) sm.A[r * AP + j] = (first ? ba : bz) * (accA[t] + part[t]);
+                pv[t] = accP[t] + part[9 + t];
             }
-            for (int j = ra + 1; j < 8 * blk + 8; ++j) gP[op_index(ra, j, kChunk)] = z;
-            for (int j = rz + 1; j < 8 * blk + 8; ++j) gP[op_index(rz, j, kChunk)] = z;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                pz[u] = (u <= 7 - rp) ? pv[8 - u] : 0.f;  // row rz, column 8 blk + u: t = 8 - u
+                const int t = rp - u;                       // row ra, column 8 blk + u
+                pa[u] = t == 0 ? pv[0] : t == 1 ? pv[1] : t == 2 ? pv[2] : t == 3 ? pv[3] : 0.f;
+            }
+            *reinterpret_cast<uint4*>(&gP[op_index(ra, 8 * blk, kChunk)]) = pack8(pa);
+            *reinterpret_cast<uint4*>(&gP[op_index(rz, 8 * blk, kChunk)]) = pack8(pz);
         }
     }
     __syncthreads();
