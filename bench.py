@@ -213,6 +213,128 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+DECODE_METRIC = "KDA decode tokens/s (one token per sequence per step); % HBM roofline"
+
+
+def _decode_bytes(N, H, dk, dv):
+    """Algorithmic HBM bytes of one decode step: the state read and written (fp32), the
+    token's bf16 q, k, v, fp32 g, beta, and the bf16 output."""
+    return N * H * (2 * dk * dv * 4 + 2 * dk * 2 + dk * 4 + 2 * dv * 2 + 4)
+
+
+def run_decode(args):
+    """Workload decode-N{N}-H{H}: one kda_decode step over N sequences x H heads,
+    dk = dv = 128, bf16 q/k/v, fp32 g/beta, cfg2-style values, states ~ N(0, 0.1)
+    updated in place (the state stays resident, as in serving)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_delta_rule_25_gb300 as kda
+    _, ns, hs = args.workload.split("-")
+    N, H, D = int(ns[1:]), int(hs[1:]), 128
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    salt = gen.fresh_salt()
+    x = gen.make_lengths([1] * N, seed=0, salt=salt, H=H, d=D, name="decode")
+    t = {n: getattr(x, n)[0].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    state = x.h0.to(dev)
+    o = torch.empty((N, H, D), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.decode(t["q"], t["k"], t["v"], t["g"], t["beta"], state, x.scale, out_state=state, o=o)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    value = N / (ms * 1e-3)
+    hbm, _, peak_src = _peaks()
+    alg = _decode_bytes(N, H, D, D)
+    achieved = alg / (ms * 1e-3) / 1e9
+
+    # parity after timing: one step from a fresh state against the fp64 oracle (2 heads)
+    import oracle
+    from tests.metrics import rel_rmse
+    x2 = gen.make_lengths([1] * N, seed=1, salt=salt + 7919, H=H, d=D, name="decode")
+    for n in ("q", "k", "v", "g", "beta"):
+        t[n].copy_(getattr(x2, n)[0].to(dev))
+    state.copy_(x2.h0.to(dev))
+    step()
+    torch.cuda.synchronize(dev)
+    hsel = [0, H // 2 + 1]
+    tt = x2.tensors()
+    for key in ("q", "k", "v", "g", "beta"):
+        tt[key] = tt[key][:, :, hsel].contiguous()
+    tt["h0"] = tt["h0"][:, hsel].contiguous()
+    o_ref, h_ref = oracle.kda_recurrence_fp64(**tt)
+    parity = {"heads": hsel, "o_rel_rmse": rel_rmse(o.cpu()[None][:, :, hsel], o_ref),
+              "state_rel_rmse": rel_rmse(state.cpu()[:, hsel], h_ref), "salt": x2.salt}
+
+    # end to end: the token's inputs from pinned host memory, the output back; states stay
+    host_in = {n: getattr(x, n)[0].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def e2e_step():
+        for n, v in host_in.items():
+            t[n].copy_(v, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_value = N / (e0.elapsed_time(e1) / args.steps * 1e-3)
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 5.0:
+            oracle.kda_recurrence_fp64(**x.tensors())
+            reps += 1
+        per = (time.perf_counter() - t0) / reps
+        cpu = {"value": N / per, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"the whole step ({N} sequences x {H} heads), {reps} runs, fp64 C recurrence"}
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"decode step: N={N} sequences x H={H} heads, dk=dv=128, bf16 q/k/v, "
+                               "fp32 states updated in place",
+                   "name": args.workload, "tokens_per_step": N,
+                   "l2": f"no flush: {N * H * D * D * 4 / 1e6:.0f} MB of state read and written per step vs the 129 MB L2",
+                   "salt": salt},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.steps},
+        "parity": parity,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -221,12 +343,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="cfg2",
-                    help="cfg2 (the headline workload), cfg3, cfg4, cfg5-{fixed|varlen}-H{16|32|64}-{total}")
+                    help="cfg2 (the headline workload), cfg3, cfg4, cfg5-{fixed|varlen}-H{16|32|64}-{total}, "
+                         "decode-N{sequences}-H{heads}")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload.startswith("decode-"):
+        run_decode(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

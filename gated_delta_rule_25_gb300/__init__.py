@@ -6,6 +6,7 @@ the library's CUDA kernels.  PyTorch provides device memory and the current
 stream.  There is no CPU path: without the built library every call raises.
 
     o, hT = fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None)
+    o, h  = decode(q, k, v, g, beta, state=None, scale=None)   # one token per sequence
 
 q, k: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, same dtype); g: [B, T, H, dk]
 fp32 (log of the per-channel decay, <= 0); beta: [B, T, H] fp32 in [0, 1];
@@ -68,6 +69,8 @@ def load_library():
         lib.kda_fwd_noalloc.restype = i32
         lib.kda_fwd_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.kda_fwd_check.restype = i32
+        lib.kda_decode.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
+        lib.kda_decode.restype = i32
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -215,3 +218,50 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
 
 __all__ = ["fwd", "fwd_noalloc", "workspace_size", "launch_count", "load_library", "KdaError",
            "LIB_PATH"]
+
+
+def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+           beta: torch.Tensor, state: Optional[torch.Tensor] = None,
+           scale: Optional[float] = None, *, out_state: Optional[torch.Tensor] = None,
+           o: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One recurrence step per sequence (single-token decode), via ``kda_decode``.
+
+    q, k: [N, H, dk]; v: [N, H, dv] (bf16 or fp32); g: [N, H, dk] fp32; beta: [N, H]
+    fp32; state: [N, H, dk, dv] fp32 or None (zeros).  Returns (o [N, H, dv] in q's
+    dtype, new state).  ``out_state`` may be ``state`` itself (update in place);
+    by default a new tensor is returned."""
+    lib = load_library()
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, dk]")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _check(q, "q", q.dtype, (N, H, dk), dev)
+    _check(k, "k", q.dtype, (N, H, dk), dev)
+    _check(v, "v", q.dtype, (N, H, dv), dev)
+    _check(g, "g", torch.float32, (N, H, dk), dev)
+    _check(beta, "beta", torch.float32, (N, H), dev)
+    if state is not None:
+        _check(state, "state", torch.float32, (N, H, dk, dv), dev)
+    if out_state is None:
+        out_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    else:
+        _check(out_state, "out_state", torch.float32, (N, H, dk, dv), dev)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    else:
+        _check(o, "o", q.dtype, (N, H, dv), dev)
+    if scale is None:
+        scale = dk ** -0.5
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    dt = KDA_BF16 if q.dtype == torch.bfloat16 else KDA_FP32
+    st = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(state),
+                        _ptr(out_state), N, H, dk, dv, float(scale), _ptr(o),
+                        ctypes.c_void_p(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode")
+    return o, out_state

@@ -139,7 +139,7 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
  * Limits and behaviour:
  *   - Problems whose workspace (kda_fwd_workspace_size) exceeds the array are
  *     refused with KDA_ERR_TOO_LARGE before anything is launched; at d = 128 the
- *     array holds about 450 (chunk, head) pairs, e.g. 1,024 tokens x 24 heads.
+ *     array holds about 310 (chunk, head) pairs, e.g. 1,024 tokens x 19 heads.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -157,6 +157,29 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, kda_dtyp
                            const int32_t* cu_seqlens, int num_seqs,
                            int B, int T, int H, int dk, int dv, float scale,
                            void* o, float* hT, kda_stream_t stream);
+
+/*
+ * One recurrence step per sequence: single-token decode ("Autoresearch on Kimi
+ * Delta Attention", section THE MECHANISM: the per-token state update that the
+ * chunked prefill batches).  For every sequence n and head h, with S = h_in[n,h]
+ * (zeros when h_in is NULL) and that sequence's one token:
+ *     qh = q / sqrt(|q|^2 + KDA_L2_EPS),  kh = k / sqrt(|k|^2 + KDA_L2_EPS)
+ *     S' = (I - beta kh kh^T) Diag(exp(g)) S + beta kh v^T,   o = scale * S'^T qh
+ * h_out[n,h] receives S'.  Every step is fp32 (no tensor cores: the work is one
+ * read and one write of the state, bound by HBM bandwidth).
+ *
+ * Layouts (DEVICE pointers, row-major, contiguous, 16-byte aligned):
+ *     q, k : [N, H, dk] (qkv_dtype)   g : [N, H, dk] fp32   beta : [N, H] fp32
+ *     v, o : [N, H, dv] (qkv_dtype)   h_in, h_out : [N, H, dk, dv] fp32
+ * h_out may be h_in itself (update in place); otherwise the two must not overlap
+ * (KDA_ERR_INVALID_ARG).  No workspace; nothing is allocated.  Same legal inputs
+ * as kda_fwd.  Statuses: KDA_ERR_INVALID_ARG (null pointer, N < 0, H <= 0,
+ * non-finite scale, overlapping states), KDA_ERR_UNSUPPORTED, KDA_ERR_ALIGNMENT,
+ * KDA_ERR_CUDA; KDA_OK with nothing enqueued when N == 0.
+ */
+kda_status kda_decode(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                      const float* g, const float* beta, const float* h_in, float* h_out,
+                      int N, int H, int dk, int dv, float scale, void* o, kda_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -89,3 +89,37 @@ def test_python_binding_fails_loudly_without_cuda():
     x = torch.zeros(1, 4, 1, 64)
     with pytest.raises(ValueError):
         kda.fwd(x, x, x, x.float(), torch.zeros(1, 4, 1))
+
+
+def _decode(lib, **kw):
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails host checks
+    args = dict(q=p, k=p, v=p, dt=0, g=p, beta=p, h_in=p, h_out=ctypes.c_void_p(1 << 30), N=2,
+                H=2, dk=64, dv=64, scale=0.125, o=p, stream=None)
+    args.update(kw)
+    return lib.kda_decode(args["q"], args["k"], args["v"], args["dt"], args["g"], args["beta"],
+                          args["h_in"], args["h_out"], args["N"], args["H"], args["dk"],
+                          args["dv"], args["scale"], args["o"], args["stream"])
+
+
+def test_decode_host_validation(lib):
+    assert _decode(lib, dk=96) == 2
+    assert _decode(lib, dv=256) == 2
+    assert _decode(lib, dt=3) == 2
+    assert _decode(lib, scale=float("inf")) == 1
+    assert _decode(lib, H=0) == 1
+    assert _decode(lib, N=-1) == 1
+    assert _decode(lib, q=None) == 1
+    assert _decode(lib, h_out=None) == 1
+    assert _decode(lib, o=ctypes.c_void_p((1 << 20) + 2)) == 3      # misaligned
+    # overlapping (but not identical) state buffers
+    assert _decode(lib, h_in=ctypes.c_void_p(1 << 30), h_out=ctypes.c_void_p((1 << 30) + 256)) == 1
+    assert _decode(lib, N=0) == 0                                   # nothing to do: no launch
+
+
+def test_python_decode_fails_loudly_without_cuda():
+    import torch
+
+    import gated_delta_rule_25_gb300 as kda
+    x = torch.zeros(2, 1, 64)
+    with pytest.raises(ValueError):
+        kda.decode(x, x, x, x.float(), torch.zeros(2, 1))
