@@ -8,7 +8,7 @@
 // 01 RESULTS: the recurrent state must stay fp32, a bf16 state loses accuracy):
 //   [w S ; QG S]  = [w ; QG] S                     GEMM1  M=128, N=32, K=dk
 //   U  = u - w S
-//   S <- Diag(exp(Gamma_L)) S + KT U               GEMM2  M=dk,  N=32, K=64
+//   S <- Diag(exp(Gamma_L)) S + KT U               GEMM2  M=dk,  N=32, K=64 (tf32)
 //   O  = scale (QG S + P U)                        GEMM3  M=128, N=32, K=64
 // (QG = qh * exp(Gamma)).  w and QG arrive as one 128-row operand tile, so one
 // product gives both w S (accumulator rows 0-63) and QG S (rows 64-127).  GEMM3
@@ -17,7 +17,9 @@
 // 64-127 of the 128-row operand are exactly P (rows 0-63, already consumed, pick
 // up a dead sum).  S lives in fp32 registers of the four epilogue warps (one key
 // channel per thread).  bf16 copies of S and U in shared memory (N-major) are the
-// B operands of the MMAs, which accumulate in fp32 in tensor memory.
+// B operands of GEMM1 and GEMM3; GEMM2, whose rounding would stay in the state,
+// takes KT, u and U in fp32 (tf32 products).  All accumulate in fp32 in tensor
+// memory.
 //
 // Only GEMM1 and GEMM2 are on the serial path.  Per chunk: thread 0 issues GEMM1;
 // warps 0-1 form U from its rows 0-63 while warps 2-3 store the previous chunk's
@@ -32,7 +34,7 @@
 // its first chunk and stores h_T after its last), so chains run back to back.
 //
 // Warps 0-3: epilogue, GEMM1/GEMM2 issue (warp w reads TMEM lanes 32w..32w+31).
-// Warp 4: work items and bulk copies of the per-chunk factors, three stages deep.
+// Warp 4: work items and bulk copies of the per-chunk factors, two stages deep.
 // Warp 5: GEMM3 issue (output products, off the serial path).
 // Every wait is bounded; a time-out sets KDA_DEVERR_TIMEOUT in the workspace
 // error word and the CTA drains and leaves.
@@ -44,16 +46,26 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int NV = kNV;
 constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
+
+// GEMM2's B operand: U^T (32 value columns x 64 chunk rows) in fp32, K-major core
+// matrices of 8 columns x 4 rows (16 bytes each).  K-adjacent core matrices sit
+// kU32Lbo = 144 bytes apart (not 128), so a warp's 32 consecutive chunk rows of one
+// column hit 32 different banks when the epilogue writes them.
+constexpr uint32_t kU32Lbo = 144, kU32Sbo = (kChunk / 4) * kU32Lbo;
+constexpr int kU32Words = (NV / 8) * kU32Sbo / 4;
+__device__ inline int u32_index(int n, int r) {
+    return (int)(((n >> 3) * kU32Sbo + (r >> 2) * kU32Lbo) / 4) + ((n & 7) << 2) + (r & 3);
+}
 
 template <int DK>
 struct __align__(128) ChainStage {
     __nv_bfloat16 WQ[2 * kChunk * DK];  // operand layout, 128 x DK: rows w, then QG
-    __nv_bfloat16 KT[DK * kChunk];   // operand layout, DK x 64
+    float KT[DK * kChunk];           // tf32 operand layout, DK x 64
     __nv_bfloat16 P[kChunk * kChunk];
-    __nv_bfloat16 U0[kChunk * NV];   // row-major 64 x 32 slab of u
+    float U0[kChunk * NV];           // row-major 64 x 32 slab of u
     float GL[DK];
     int4 item;                       // {sequence, head, value tile, chunk index j}
     int4 info;                       // {chunks of the item, first token row, rows, end marker}
@@ -63,7 +75,8 @@ template <int DK>
 struct __align__(128) ChainSmem {
     ChainStage<DK> st[kStages];
     __nv_bfloat16 Sop[2][NV * DK];   // N-major operand (B of GEMM1), two copies
-    __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM2 / GEMM3)
+    __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM3)
+    float Uop32[kU32Words];          // K-major tf32 operand (B of GEMM2), padded
     uint64_t full[kStages], empty[kStages], d1, d2, d3[2], uready, fin, fin3;
     uint32_t tmem_base;
     int abort;
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 4) {
         // ------------------------------------------------ work items + producer
         const uint32_t main_bytes = (uint32_t)(F.u0 - F.wq);  // WQ, KT, P back to back
-        const uint32_t u_bytes = kChunk * NV * 2, gl_bytes = DK * 4;
+        const uint32_t u_bytes = kChunk * NV * 4, gl_bytes = DK * 4;
         int gj = 0;
         bool okp = true;
         while (okp) {
@@ -270,9 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * w) << 16;
         const int ch = acc_row<DK>(w, l);     // key channel of this thread's state row
         const int ur = 32 * w + l;            // D1 row (lane): w S rows 0-63, output rows 64-127
-        const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop = ptx::smem_u32(sm.Uop);
+        const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop32 = ptx::smem_u32(sm.Uop32);
         constexpr uint32_t id_w = ptx::idesc_bf16(128, NV) | kBMajorMN;
-        constexpr uint32_t id_k = ptx::idesc_bf16(DK, NV) | kBMajorMN;
+        constexpr uint32_t id_k = ptx::idesc_tf32(DK, NV);   // both K-major
         float S[NV];
 #pragma unroll
         for (int n = 0; n < NV; ++n) S[n] = 0.f;
@@ -347,19 +360,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     float acc[NV];
                     tmem_ld32(tmem + lane_base + kColD1 + (uint32_t)(gj & 1) * NV, acc);
-                    const uint4* u0 = reinterpret_cast<const uint4*>(sm.st[st].U0 + ur * NV);
+                    const float4* u0 = reinterpret_cast<const float4*>(sm.st[st].U0 + ur * NV);
+                    float U[NV];
 #pragma unroll
-                    for (int nb = 0; nb < NV; nb += 8) {
-                        const uint4 raw = u0[nb / 8];
-                        const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&raw);
-                        float2 a = __bfloat1622float2(hb[0]), b = __bfloat1622float2(hb[1]);
-                        float2 c = __bfloat1622float2(hb[2]), e = __bfloat1622float2(hb[3]);
-                        *reinterpret_cast<uint4*>(&sm.Uop[nmaj_index(nb, ur)]) = make_uint4(
-                            pack_bf16(a.x - acc[nb], a.y - acc[nb + 1]),
-                            pack_bf16(b.x - acc[nb + 2], b.y - acc[nb + 3]),
-                            pack_bf16(c.x - acc[nb + 4], c.y - acc[nb + 5]),
-                            pack_bf16(e.x - acc[nb + 6], e.y - acc[nb + 7]));
+                    for (int n4 = 0; n4 < NV / 4; ++n4) {
+                        const float4 a = u0[n4];
+                        U[4 * n4] = a.x - acc[4 * n4];
+                        U[4 * n4 + 1] = a.y - acc[4 * n4 + 1];
+                        U[4 * n4 + 2] = a.z - acc[4 * n4 + 2];
+                        U[4 * n4 + 3] = a.w - acc[4 * n4 + 3];
                     }
+#pragma unroll
+                    for (int nb = 0; nb < NV; nb += 8)
+                        *reinterpret_cast<uint4*>(&sm.Uop[nmaj_index(nb, ur)]) = make_uint4(
+                            pack_bf16(U[nb], U[nb + 1]), pack_bf16(U[nb + 2], U[nb + 3]),
+                            pack_bf16(U[nb + 4], U[nb + 5]), pack_bf16(U[nb + 6], U[nb + 7]));
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) sm.Uop32[u32_index(n, ur)] = U[n];
                 }
             }
             if (end) {
@@ -375,10 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 ptx::mbar_arrive(&sm.uready);
                 const uint32_t ka = ptx::smem_u32(sm.st[st].KT);
-                ptx::mma_chain<kChunk / 16>(tmem + kColD2,  // D2 = KT U
-                                            ptx::smem_desc(ka, (DK / 8) * 128, 128), 2 * (DK / 8) * 128,
-                                            ptx::smem_desc(uop, (NV / 8) * 128, 128),
-                                            2 * (NV / 8) * 128, id_k, false);
+                const uint64_t a0 = ptx::smem_desc(ka, (DK / 8) * 128, 128);
+                const uint64_t b0 = ptx::smem_desc(uop32, kU32Lbo, kU32Sbo);
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 8; ++kk)  // D2 = KT U, tf32, K = 8 per step
+                    ptx::mma_tf32(tmem + kColD2, a0 + (uint64_t)((kk * 2 * (DK / 8) * 128) >> 4),
+                                  b0 + (uint64_t)((kk * 2 * kU32Lbo) >> 4), id_k, kk > 0);
                 ptx::mma_commit(&sm.d2);
                 ptx::mma_commit(&sm.empty[st]);
             }

@@ -10,18 +10,20 @@
 // Per (chunk, head) factor block, every part a multiple of 256 bytes:
 //   WQ  [128 x dk] bf16, operand layout: rows 0-63 w = (I + A)^-1 Diag(beta) (kh * exp(Gamma)),
 //                                        rows 64-127 qh * exp(Gamma) (one M = 128 operand)
-//   KT  [dk x 64] bf16, operand layout  (kh * exp(Gamma_last - Gamma))^T
+//   KT  [dk x 64] fp32, tf32 operand layout  (kh * exp(Gamma_last - Gamma))^T
 //   P   [64 x 64] bf16, operand layout  sum_c qh_ic kh_jc exp(Gamma_ic - Gamma_jc), j <= i
-//   U0  [dv/32][64][32] bf16            u = (I + A)^-1 Diag(beta) v, in 32-column
+//   U0  [dv/32][64][32] fp32            u = (I + A)^-1 Diag(beta) v, in 32-column
 //                                       slabs (one contiguous slab per value tile)
 //   GL  [dk] fp32                       exp(Gamma_last)
+// KT and u feed the state update, the one product whose rounding persists in the
+// state, so they are kept in fp32 and that product runs on tf32 inputs.
 //
 // "Operand layout" is the K-major, unswizzled tensor-core shared-memory layout for
-// an R x K bf16 tile: 8 x 8 core matrices of 128 contiguous bytes, core matrix
-// (row block rb, k block kb) at byte ((kb * R/8) + rb) * 128.  A bulk copy of the
-// block lands in shared memory ready for tcgen05.mma, with descriptor leading
-// byte offset (between core matrices adjacent in K) = R/8 * 128 and stride byte
-// offset (between core matrices adjacent in rows) = 128.
+// an R x K tile: core matrices of 8 rows x 16 contiguous bytes (8 bf16 or 4 fp32
+// elements of K), core matrix (row block rb, k block kb) at byte ((kb * R/8) + rb)
+// * 128.  A bulk copy of the block lands in shared memory ready for tcgen05.mma,
+// with descriptor leading byte offset (between core matrices adjacent in K) = R/8 *
+// 128 and stride byte offset (between core matrices adjacent in rows) = 128.
 #pragma once
 
 #include <cstddef>
@@ -39,7 +41,7 @@ constexpr int kNV = 32;  // value columns per state-recurrence chain
 constexpr unsigned kDevErrCuSeqlens = 0x1u;
 constexpr unsigned kDevErrTimeout = 0x2u;
 
-// Element index of (row r, value column n) in the slabbed U0 block.
+// Element index of (row r, value column n) in the slabbed U0 block (fp32).
 __host__ __device__ inline int u0_index(int r, int n) {
     return ((n / kNV) * kChunk + r) * kNV + (n % kNV);
 }
@@ -62,9 +64,9 @@ struct FactorLayout {
     __host__ __device__ explicit FactorLayout(int dk, int dv) {
         size_t off = 0;
         wq = off; off += align256(size_t(2 * kChunk) * dk * 2);
-        kt = off; off += align256(size_t(dk) * kChunk * 2);
+        kt = off; off += align256(size_t(dk) * kChunk * 4);
         p = off;  off += align256(size_t(kChunk) * kChunk * 2);
-        u0 = off; off += align256(size_t(kChunk) * dv * 2);
+        u0 = off; off += align256(size_t(kChunk) * dv * 4);
         gl = off; off += align256(size_t(dk) * 4);
         bytes = off;
     }
@@ -88,9 +90,14 @@ struct WsLayout {
     }
 };
 
-// Element index of (r, k) in an R x K tile stored in the operand layout.
+// Element index of (r, k) in an R x K bf16 tile stored in the operand layout.
 __host__ __device__ inline int op_index(int r, int k, int R) {
     return (((k >> 3) * (R >> 3) + (r >> 3)) << 6) + ((r & 7) << 3) + (k & 7);
+}
+
+// Element index of (r, k) in an R x K fp32 (tf32 operand) tile in the operand layout.
+__host__ __device__ inline int op_index32(int r, int k, int R) {
+    return (((k >> 2) * (R >> 3) + (r >> 3)) << 5) + ((r & 7) << 2) + (k & 3);
 }
 
 struct Header {

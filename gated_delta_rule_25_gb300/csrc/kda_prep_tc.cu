@@ -12,7 +12,8 @@
 //   P_ij     = sum_c qh_ic kh_jc D_c(i, j)                        j <= i
 //   with D_c(i, j) = exp(Gamma_ic - Gamma_jc) = alpha_c(j+1) ... alpha_c(i)
 //   X        = (I + A)^-1                                        (fp32, blocked)
-//   [w | u]  = X Diag(beta) [kh * gamma | v]                     (tcgen05, M=64 N=dk+dv K=64)
+//   [w | u]  = X Diag(beta) [kh * gamma | v]                     (tcgen05, M=64 N=dk+dv K=64,
+//                                                                 X Diag(beta) split hi + lo)
 //   QG = qh * gamma,  KT = (kh * gamma_L / gamma)^T,  GL = gamma_L,  gamma = exp(Gamma)
 // w and QG are written as the two halves of one 128-row operand tile, so that the
 // state kernel forms w S and QG S with one M = 128 product.
@@ -60,6 +61,7 @@ struct __align__(128) PrepSmem {
         } m;
         struct {
             __nv_bfloat16 xop[kChunk * kChunk];        // X Diag(beta), operand layout
+            __nv_bfloat16 xlo[kChunk * kChunk];        // its rounding remainder (hi + lo split)
             __nv_bfloat16 bop[(DK + DV) * kChunk];     // [kh*gamma | v]^T, operand layout
         } t;
         float scratch[32 * 32];
@@ -351,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int2 rows_next = rows_of(next), rows_after = rows_of(after);
     uint8_t* fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
     __nv_bfloat16* gWQ = reinterpret_cast<__nv_bfloat16*>(fb + F.wq);  // rows: w, then qh gamma
-    __nv_bfloat16* gKT = reinterpret_cast<__nv_bfloat16*>(fb + F.kt);
+    float* gKT = reinterpret_cast<float*>(fb + F.kt);
     __nv_bfloat16* gP = reinterpret_cast<__nv_bfloat16*>(fb + F.p);
-    __nv_bfloat16* gU = reinterpret_cast<__nv_bfloat16*>(fb + F.u0);
+    float* gU = reinterpret_cast<float*>(fb + F.u0);
     float* gGL = reinterpret_cast<float*>(fb + F.gl);
 
     // ---------------------------------------------------------------- P1: load
@@ -525,8 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kt0[u] = ktv.x;
                 kt1[u] = ktv.y;
             }
-            *reinterpret_cast<uint4*>(&gKT[op_index(ch, r0, DK)]) = pack8(kt0);
-            *reinterpret_cast<uint4*>(&gKT[op_index(ch + 1, r0, DK)]) = pack8(kt1);
+            // fp32 (tf32 operand layout): rows r0..r0+7 are two core matrices of 4
+            *reinterpret_cast<float4*>(&gKT[op_index32(ch, r0, DK)]) = make_float4(kt0[0], kt0[1], kt0[2], kt0[3]);
+            *reinterpret_cast<float4*>(&gKT[op_index32(ch, r0 + 4, DK)]) = make_float4(kt0[4], kt0[5], kt0[6], kt0[7]);
+            *reinterpret_cast<float4*>(&gKT[op_index32(ch + 1, r0, DK)]) = make_float4(kt1[0], kt1[1], kt1[2], kt1[3]);
+            *reinterpret_cast<float4*>(&gKT[op_index32(ch + 1, r0 + 4, DK)]) = make_float4(kt1[4], kt1[5], kt1[6], kt1[7]);
             const int R = bb >> 1;
             if (bb >= 2) {  // 16-level row factors D(r, 16R)
                 float2 pre = make_float2(1.f, 1.f);
@@ -766,13 +771,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         for (int e = tid; e < kChunk * 8; e += kThreads) {
             const int i = e >> 3, jb = (e & 7) * 8;
-            float x[8];
+            float x[8], lo[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int j = jb + u;
                 x[u] = (j <= i) ? sm.X[i * AP + j] * sm.bs[j] : 0.f;
             }
-            *reinterpret_cast<uint4*>(&sm.ops.t.xop[op_index(i, jb, kChunk)]) = pack8(x);
+            const uint4 hi = pack8(x);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hi);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                lo[2 * u] = x[2 * u] - f.x;
+                lo[2 * u + 1] = x[2 * u + 1] - f.y;
+            }
+            *reinterpret_cast<uint4*>(&sm.ops.t.xop[op_index(i, jb, kChunk)]) = hi;
+            *reinterpret_cast<uint4*>(&sm.ops.t.xlo[op_index(i, jb, kChunk)]) = pack8(lo);
         }
         // [kh * gamma | v]^T, one task per (8-row block, column): gamma_r = Gb_b f_r
         for (int e = tid; e < 8 * NB; e += kThreads) {
@@ -803,13 +817,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------- P7: [w | u] on tcgen05
     if (tid == 0) {
-        const uint32_t xa = ptx::smem_u32(sm.ops.t.xop), ba = ptx::smem_u32(sm.ops.t.bop);
+        // X Diag(beta) = hi + lo (both bf16): the split keeps the inverse's fp32
+        // accuracy through the product
+        const uint32_t ba = ptx::smem_u32(sm.ops.t.bop);
         constexpr uint32_t idesc = ptx::idesc_bf16(kChunk, NB);
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk)
-            ptx::mma_bf16(tmem, ptx::smem_desc(xa + kk * 2048, 1024, 128),
-                          ptx::smem_desc(ba + kk * 2 * (NB / 8) * 128, (NB / 8) * 128, 128), idesc,
-                          kk > 0);
+        for (int part = 0; part < 2; ++part) {
+            const uint32_t xa = ptx::smem_u32(part ? sm.ops.t.xlo : sm.ops.t.xop);
+#pragma unroll
+            for (int kk = 0; kk < kChunk / 16; ++kk)
+                ptx::mma_bf16(tmem, ptx::smem_desc(xa + kk * 2048, 1024, 128),
+                              ptx::smem_desc(ba + kk * 2 * (NB / 8) * 128, (NB / 8) * 128, 128),
+                              idesc, part > 0 || kk > 0);
+        }
         ptx::mma_commit(&sm.bar);
     }
     if (next.h < H) {  // lands while the MMA and its epilogue run
@@ -838,8 +858,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < 8; ++u) y[u] = x[i >> 1][8 * (i & 1) + u];
                 if (col < DK)
                     *reinterpret_cast<uint4*>(&gWQ[op_index(row, col, 2 * kChunk)]) = pack8(y);
-                else
-                    *reinterpret_cast<uint4*>(&gU[u0_index(row, col - DK)]) = pack8(y);
+                else {  // u stays fp32
+                    float4* du = reinterpret_cast<float4*>(&gU[u0_index(row, col - DK)]);
+                    du[0] = make_float4(y[0], y[1], y[2], y[3]);
+                    du[1] = make_float4(y[4], y[5], y[6], y[7]);
+                }
             }
         }
     }

@@ -102,6 +102,15 @@ def test_stress_probes(kda, kind):
     _assert_parity(x, *_gpu(kda, x))
 
 
+@pytest.mark.parametrize("salt", [4013173612, 1, 9])
+def test_repeated_keys_fixed_salts(kda, salt):
+    """The repeated-keys probe is the one closest to the state gate (every token writes
+    along the same direction, so operand roundings add up coherently); these salts
+    include one that a bf16 state-update product pushed past 5e-3."""
+    x = gen.make_probe("repeated_keys", seed=6, salt=salt, T=300, H=2, d=128)
+    _assert_parity(x, *_gpu(kda, x))
+
+
 def test_no_h0_no_hT(kda):
     x = gen.make_lengths([100, 37], seed=7, salt=SALT, H=2, d=128, h0=False)
     o, hT = _gpu(kda, x, output_final_state=False)
