@@ -65,7 +65,7 @@ struct __align__(128) ChainStage {
     __nv_bfloat16 WQ[2 * kChunk * DK];  // operand layout, 128 x DK: rows w, then QG
     float KT[DK * kChunk];           // tf32 operand layout, DK x 64
     __nv_bfloat16 P[kChunk * kChunk];
-    float U0[kChunk * NV];           // row-major 64 x 32 slab of u
+    float U0[kChunk * NV];           // 64 x 32 slab of u: [8 column groups][64 rows][4]
     float GL[DK];
     int4 item;                       // {sequence, head, value tile, chunk index j}
     int4 info;                       // {chunks of the item, first token row, rows, end marker}
@@ -360,11 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     float acc[NV];
                     tmem_ld32(tmem + lane_base + kColD1 + (uint32_t)(gj & 1) * NV, acc);
-                    const float4* u0 = reinterpret_cast<const float4*>(sm.st[st].U0 + ur * NV);
+                    const float4* u0 = reinterpret_cast<const float4*>(sm.st[st].U0);
                     float U[NV];
 #pragma unroll
                     for (int n4 = 0; n4 < NV / 4; ++n4) {
-                        const float4 a = u0[n4];
+                        const float4 a = u0[n4 * kChunk + ur];
                         U[4 * n4] = a.x - acc[4 * n4];
                         U[4 * n4 + 1] = a.y - acc[4 * n4 + 1];
                         U[4 * n4 + 2] = a.z - acc[4 * n4 + 2];

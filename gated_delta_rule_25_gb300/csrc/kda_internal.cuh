@@ -12,7 +12,7 @@
 //                                        rows 64-127 qh * exp(Gamma) (one M = 128 operand)
 //   KT  [dk x 64] fp32, tf32 operand layout  (kh * exp(Gamma_last - Gamma))^T
 //   P   [64 x 64] bf16, operand layout  sum_c qh_ic kh_jc exp(Gamma_ic - Gamma_jc), j <= i
-//   U0  [dv/32][64][32] fp32            u = (I + A)^-1 Diag(beta) v, in 32-column
+//   U0  [dv/32][8][64][4] fp32          u = (I + A)^-1 Diag(beta) v, in 32-column
 //                                       slabs (one contiguous slab per value tile)
 //   GL  [dk] fp32                       exp(Gamma_last)
 // KT and u feed the state update, the one product whose rounding persists in the
@@ -41,9 +41,12 @@ constexpr int kNV = 32;  // value columns per state-recurrence chain
 constexpr unsigned kDevErrCuSeqlens = 0x1u;
 constexpr unsigned kDevErrTimeout = 0x2u;
 
-// Element index of (row r, value column n) in the slabbed U0 block (fp32).
+// Element index of (row r, value column n) in the slabbed U0 block (fp32): one
+// slab of kChunk x kNV per value tile, inside it groups of 4 columns, each a
+// column-group-major [kChunk][4] array, so that consecutive rows of a 4-column
+// group are consecutive 16-byte words (conflict-free for a warp of rows).
 __host__ __device__ inline int u0_index(int r, int n) {
-    return ((n / kNV) * kChunk + r) * kNV + (n % kNV);
+    return (((n / kNV) * (kNV / 4) + (n % kNV) / 4) * kChunk + r) * 4 + (n & 3);
 }
 
 struct Dims {

@@ -314,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* const st_v = kBf16In ? reinterpret_cast<uint8_t*>(sm.vs) : reinterpret_cast<uint8_t*>(sm.A);
     static_assert(kBf16In || kChunk * DV * 4 <= 2 * kChunk * (kChunk + 1) * 4, "v staging");
     constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * 4, VB = DV * sizeof(TIn);
+    // Output staging for the bulk stores of w and u (in the operand region).
+    __nv_bfloat16* const st_w = reinterpret_cast<__nv_bfloat16*>(&sm.ops);
+    float* const st_u = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sm.ops) + kChunk * DK * 2);
+    static_assert(kChunk * DK * 2 + kChunk * DV * 4 <= sizeof(typename Sm::Ops), "output staging");
     float rb = 0.f;  // beta of this thread's row of the next item (threads < 64)
     // {first token row, valid rows} of an item's chunk (zeros past the last item)
     auto rows_of = [&](Item it) {
@@ -442,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------ P2: decay products
+    if (tid == 0) ptx::bulk_wait_read_all();  // the previous item's stores have left the
+                                              // operand region, written again below
     // Every decay factor used below is a product of alpha over a run of rows.  The
     // rows split into eight 8-row blocks; per (block b, channel) the local forward
     // products f_r = alpha(8b+1..r) and backward products g_r = alpha(r+1..8b+7)
@@ -840,7 +846,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && tid == 0) atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
     ptx::tc_fence_after();
     {
-        // warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w; split the columns
+        // warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w; split the columns.
+        // The results are staged in shared memory (the operand region, dead once the
+        // MMA has completed) in their global layouts and leave by bulk copies.
         const int quarter = warp & 3, half = warp >> 2;
         const int row = 16 * quarter + lane;  // valid for lane < 16 (M = 64 layout)
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
@@ -849,30 +857,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < NLD; ++i) ptx::tmem_ld16(tmem + lane_base + half * HALF + 16 * i, x[i]);
         ptx::tmem_ld_wait();
-        if (ok && lane < 16) {
+        if (lane < 16) {
 #pragma unroll
             for (int i = 0; i < 2 * NLD; ++i) {
                 const int col = half * HALF + 8 * i;
                 float y[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) y[u] = x[i >> 1][8 * (i & 1) + u];
-                if (col < DK)
-                    *reinterpret_cast<uint4*>(&gWQ[op_index(row, col, 2 * kChunk)]) = pack8(y);
-                else {  // u stays fp32
-                    float4* du = reinterpret_cast<float4*>(&gU[u0_index(row, col - DK)]);
-                    du[0] = make_float4(y[0], y[1], y[2], y[3]);
-                    du[1] = make_float4(y[4], y[5], y[6], y[7]);
+                if (col < DK) {  // w rows 0-63 of the 128-row tile: core matrices (col/8, row/8)
+                    *reinterpret_cast<uint4*>(&st_w[(((col >> 3) * 8 + (row >> 3)) << 6) + ((row & 7) << 3)]) =
+                        pack8(y);
+                } else {         // u stays fp32
+                    const int n = col - DK;
+                    *reinterpret_cast<float4*>(&st_u[u0_index(row, n)]) = make_float4(y[0], y[1], y[2], y[3]);
+                    *reinterpret_cast<float4*>(&st_u[u0_index(row, n + 4)]) = make_float4(y[4], y[5], y[6], y[7]);
                 }
             }
         }
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ok) {
+        // w: rows 0-63 of each 16-byte k block group of the WQ tile (1 KB of every 2 KB)
+#pragma unroll 1
+        for (int kb = 0; kb < DK / 8; ++kb)
+            ptx::bulk_s2g(reinterpret_cast<uint8_t*>(gWQ) + kb * 2048, st_w + kb * 512, 1024);
+        ptx::bulk_s2g(gU, st_u, kChunk * DV * 4);
+        ptx::bulk_commit();
+    }
     ptx::tc_fence_after();
     phase ^= 1u;
     item = next;
     rows_cur = rows_next;
     }  // items
+    if (tid == 0) ptx::bulk_wait_all();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {

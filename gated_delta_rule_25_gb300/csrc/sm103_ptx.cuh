@@ -114,6 +114,20 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1
                  : "memory");
 }
 
+// Shared -> global bulk copy (both addresses 16-byte aligned, bytes a multiple of
+// 16), tracked in this thread's bulk group; commit, then wait for the group's
+// shared-memory reads (.read) or for its completion.
+__device__ __forceinline__ void bulk_s2g(void* dst_gmem, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (tensor core, bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
