@@ -62,7 +62,7 @@ __device__ inline int u32_index(int n, int r) {
 
 template <int DK>
 struct __align__(128) ChainStage {
-    __nv_bfloat16 WQ[2 * kChunk * DK];  // operand layout, 128 x DK: rows w, then QG
+    __nv_bfloat16 WQ[2 * kChunk * DK];  // row-block-major operand layout, 128 x DK: w, then QG
     float KT[DK * kChunk];           // tf32 operand layout, DK x 64
     __nv_bfloat16 P[kChunk * kChunk];
     float U0[kChunk * NV];           // 64 x 32 slab of u: [8 column groups][64 rows][4]
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t wa = ptx::smem_u32(sm.st[st].WQ);
                 const uint32_t sop = sop0 + (uint32_t)(gj & 1) * (NV * DK * 2);
                 ptx::mma_chain<DK / 16>(tmem + kColD1 + (uint32_t)(gj & 1) * NV,
-                                        ptx::smem_desc(wa, 2048, 128), 4096,
+                                        ptx::smem_desc(wa, 128, (DK / 8) * 128), 256,
                                         ptx::smem_desc(sop, (NV / 8) * 128, 128),
                                         2 * (NV / 8) * 128, id_w, false);
                 ptx::mma_commit(&sm.d1);

@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float2 qgv = mul2(qq[u], mul2(gb, f[u]));
-                *reinterpret_cast<uint32_t*>(&gWQ[op_index(kChunk + r0 + u, ch, 2 * kChunk)]) = pack_bf16(qgv.x, qgv.y);
+                *reinterpret_cast<uint32_t*>(&gWQ[op_index_rm(kChunk + r0 + u, ch, DK)]) = pack_bf16(qgv.x, qgv.y);
                 const float2 ktv = mul2(kq[u], mul2(gq[u], sb));
                 kt0[u] = ktv.x;
                 kt1[u] = ktv.y;
@@ -864,9 +864,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float y[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) y[u] = x[i >> 1][8 * (i & 1) + u];
-                if (col < DK) {  // w rows 0-63 of the 128-row tile: core matrices (col/8, row/8)
-                    *reinterpret_cast<uint4*>(&st_w[(((col >> 3) * 8 + (row >> 3)) << 6) + ((row & 7) << 3)]) =
-                        pack8(y);
+                if (col < DK) {  // w: rows 0-63 of the 128-row tile, one contiguous block
+                    *reinterpret_cast<uint4*>(&st_w[op_index_rm(row, col, DK)]) = pack8(y);
                 } else {         // u stays fp32
                     const int n = col - DK;
                     *reinterpret_cast<float4*>(&st_u[u0_index(row, n)]) = make_float4(y[0], y[1], y[2], y[3]);
@@ -879,10 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
-        // w: rows 0-63 of each 16-byte k block group of the WQ tile (1 KB of every 2 KB)
-#pragma unroll 1
-        for (int kb = 0; kb < DK / 8; ++kb)
-            ptx::bulk_s2g(reinterpret_cast<uint8_t*>(gWQ) + kb * 2048, st_w + kb * 512, 1024);
+        ptx::bulk_s2g(gWQ, st_w, kChunk * DK * 2);  // w: the first half of the WQ tile
         ptx::bulk_s2g(gU, st_u, kChunk * DV * 4);
         ptx::bulk_commit();
     }
