@@ -48,6 +48,10 @@ def make_workload(name: str, seed: int, salt: int):
     """cfg2 (default), cfg3, cfg4, or a throughput-sweep row cfg5-{fixed|varlen}-H{H}-{total}."""
     if name == "cfg2":
         return gen.make_cfg2(seed=seed, salt=salt), WORKLOADS[name]
+    if name == "cfg2-gbf16":
+        x = gen.make_cfg2(seed=seed, salt=salt)
+        x.g = x.g.to(torch.bfloat16)
+        return x, WORKLOADS["cfg2"].replace("fp32 g/beta/h0", "bf16 g, fp32 beta/h0")
     if name == "cfg3":
         return gen.make_cfg3(seed=seed, salt=salt), WORKLOADS[name]
     if name == "cfg4":
@@ -71,18 +75,20 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def _algorithmic_bytes(kernel: str, tokens: int, heads: int, dk: int, dv: int, nseq: int):
-    """Algorithmic HBM bytes one launch of `kernel` must move (bf16 q/k/v/o, fp32 g/beta/states)."""
+def _algorithmic_bytes(kernel: str, tokens: int, heads: int, dk: int, dv: int, nseq: int,
+                       g_bytes: int = 4):
+    """Algorithmic HBM bytes one launch of `kernel` must move (bf16 q/k/v/o, fp32 or bf16 g,
+    fp32 beta/states)."""
     th = tokens * heads
     if kernel == "factors":       # reads q, k, v, g, beta
-        return th * (2 * dk * 2 + dv * 2 + dk * 4 + 4)
+        return th * (2 * dk * 2 + dv * 2 + dk * g_bytes + 4)
     if kernel == "state_recurrence":  # writes o; reads h0, writes hT
         return th * dv * 2 + 2 * nseq * heads * dk * dv * 4
     return 0
 
 
-def _path_bytes(tokens, heads, dk, dv, nseq):
-    return tokens * heads * (2 * dk * 2 + 2 * dv * 2 + dk * 4 + 4) + 2 * nseq * heads * dk * dv * 4
+def _path_bytes(tokens, heads, dk, dv, nseq, g_bytes=4):
+    return tokens * heads * (2 * dk * 2 + 2 * dv * 2 + dk * g_bytes + 4) + 2 * nseq * heads * dk * dv * 4
 
 
 class ClockSampler:
@@ -324,7 +330,7 @@ def run_decode(args):
                    "salt": salt},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for("decode"),
                      "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -343,7 +349,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="cfg2",
-                    help="cfg2 (the headline workload), cfg3, cfg4, cfg5-{fixed|varlen}-H{16|32|64}-{total}, "
+                    help="cfg2 (the headline workload), cfg2-gbf16 (bf16 gate), cfg3, cfg4, "
+                         "cfg5-{fixed|varlen}-H{16|32|64}-{total}, "
                          "decode-N{sequences}-H{heads}")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -489,9 +496,10 @@ def main():
     ws_mb = ws.numel() / 1e6
     dom = int(np.argmax(per_kernel))
     dom_name = KERNEL_NAMES[dom] if dom < len(KERNEL_NAMES) else f"kernel{dom}"
-    alg = _algorithmic_bytes(dom_name, x.tokens, H, D, D, nseq)
+    gb = x.g.element_size()
+    alg = _algorithmic_bytes(dom_name, x.tokens, H, D, D, nseq, gb)
     achieved = alg / (per_kernel[dom] * 1e-3) / 1e9
-    path_gbs = _path_bytes(x.tokens, H, D, D, nseq) / (ms_step * 1e-3) / 1e9
+    path_gbs = _path_bytes(x.tokens, H, D, D, nseq, gb) / (ms_step * 1e-3) / 1e9
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x)
@@ -510,7 +518,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for(dom_name),
                      "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
-        "path_roofline": {"bytes_per_step": _path_bytes(x.tokens, H, D, D, nseq),
+        "path_roofline": {"bytes_per_step": _path_bytes(x.tokens, H, D, D, nseq, gb),
                           "achieved_gbs": path_gbs, "frac": path_gbs / hbm},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

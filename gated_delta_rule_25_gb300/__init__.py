@@ -9,7 +9,7 @@ stream.  There is no CPU path: without the built library every call raises.
     o, h  = decode(q, k, v, g, beta, state=None, scale=None)   # one token per sequence
 
 q, k: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, same dtype); g: [B, T, H, dk]
-fp32 (log of the per-channel decay, <= 0); beta: [B, T, H] fp32 in [0, 1];
+fp32, or bf16 with bf16 q/k/v (log of the per-channel decay, <= 0); beta: [B, T, H] fp32 in [0, 1];
 h0: [N, H, dk, dv] fp32 or None; cu_seqlens: int32 [N + 1] (packed varlen, B == 1)
 or None.  Returns o [B, T, H, dv] in q's dtype and hT [N, H, dk, dv] fp32.
 """
@@ -62,7 +62,10 @@ def load_library():
         lib.kda_fwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                 f32, vp, vp, vp, sz, vp]
         lib.kda_fwd.restype = i32
-        lib.kda_fwd_profiled.argtypes = lib.kda_fwd.argtypes + [ctypes.POINTER(vp)]
+        lib.kda_fwd_ex.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                                   i32, f32, vp, vp, vp, sz, vp]
+        lib.kda_fwd_ex.restype = i32
+        lib.kda_fwd_profiled.argtypes = lib.kda_fwd_ex.argtypes + [ctypes.POINTER(vp)]
         lib.kda_fwd_profiled.restype = i32
         lib.kda_fwd_noalloc.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
                                         i32, i32, f32, vp, vp, vp]
@@ -125,7 +128,9 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     _check(k, "k", q.dtype, (B, T, H, dk), dev)
     _check(v, "v", q.dtype, (B, T, H, dv), dev)
     _check(q, "q", q.dtype, (B, T, H, dk), dev)
-    _check(g, "g", torch.float32, (B, T, H, dk), dev)
+    if g.dtype == torch.bfloat16 and q.dtype != torch.bfloat16:
+        raise TypeError("a bf16 gate needs bf16 q, k, v")
+    _check(g, "g", g.dtype if g.dtype == torch.bfloat16 else torch.float32, (B, T, H, dk), dev)
     _check(beta, "beta", torch.float32, (B, T, H), dev)
     if cu_seqlens is not None:
         if B != 1:
@@ -158,11 +163,12 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     avail = workspace.numel() - (ws_ptr - workspace.data_ptr())
     stream = torch.cuda.current_stream(dev).cuda_stream
     dt = KDA_BF16 if q.dtype == torch.bfloat16 else KDA_FP32
-    args = (_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+    gdt = KDA_BF16 if g.dtype == torch.bfloat16 else KDA_FP32
+    args = (_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), gdt, _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
             N, B, T, H, dk, dv, float(scale), _ptr(o), _ptr(hT), ctypes.c_void_p(ws_ptr), avail,
             ctypes.c_void_p(stream))
     if events is None:
-        st = lib.kda_fwd(*args)
+        st = lib.kda_fwd_ex(*args)
     else:
         # one torch.cuda.Event per launch boundary (kda_fwd_launch_count + 1), already
         # recorded once so that its CUDA event exists

@@ -85,13 +85,15 @@ int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
 namespace {
 
 kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
-                    const float* g, const float* beta, const float* h0,
+                    const void* g, kda_dtype g_dtype, const float* beta, const float* h0,
                     const int32_t* cu_seqlens, int num_seqs,
                     int B, int T, int H, int dk, int dv, float scale,
                     void* o, float* hT,
                     void* workspace, size_t workspace_bytes, kda_stream_t stream,
                     void* const* events) {
     if (qkv_dtype != KDA_BF16 && qkv_dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (g_dtype != KDA_FP32 && !(g_dtype == KDA_BF16 && qkv_dtype == KDA_BF16))
+        return KDA_ERR_UNSUPPORTED;
     if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
     kda::Dims d;
     kda_status st = make_dims(B, T, H, dk, dv, num_seqs, cu_seqlens != nullptr, d);
@@ -116,7 +118,8 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         return cudaEventRecord(static_cast<cudaEvent_t>(events[ev++]), s) == cudaSuccess;
     };
     if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
-    if (!mark() || kda::launch_prep_tc(d, bf16, q, k, v, g, beta, ws, s) != cudaSuccess)
+    if (!mark() || kda::launch_prep_tc(d, bf16, g_dtype == KDA_BF16, q, k, v, g, beta, ws, s) !=
+                       cudaSuccess)
         return KDA_ERR_CUDA;
     if (!mark()) return KDA_ERR_CUDA;
     const cudaError_t ce = kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
@@ -134,20 +137,30 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, kda_dtype qkv_dt
                    int B, int T, int H, int dk, int dv, float scale,
                    void* o, float* hT,
                    void* workspace, size_t workspace_bytes, kda_stream_t stream) {
-    return fwd_impl(q, k, v, qkv_dtype, g, beta, h0, cu_seqlens, num_seqs, B, T, H, dk, dv,
-                    scale, o, hT, workspace, workspace_bytes, stream, nullptr);
+    return fwd_impl(q, k, v, qkv_dtype, g, KDA_FP32, beta, h0, cu_seqlens, num_seqs, B, T, H, dk,
+                    dv, scale, o, hT, workspace, workspace_bytes, stream, nullptr);
+}
+
+kda_status kda_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                      const void* g, kda_dtype g_dtype, const float* beta, const float* h0,
+                      const int32_t* cu_seqlens, int num_seqs,
+                      int B, int T, int H, int dk, int dv, float scale,
+                      void* o, float* hT,
+                      void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return fwd_impl(q, k, v, qkv_dtype, g, g_dtype, beta, h0, cu_seqlens, num_seqs, B, T, H, dk,
+                    dv, scale, o, hT, workspace, workspace_bytes, stream, nullptr);
 }
 
 kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
-                            const float* g, const float* beta, const float* h0,
+                            const void* g, kda_dtype g_dtype, const float* beta, const float* h0,
                             const int32_t* cu_seqlens, int num_seqs,
                             int B, int T, int H, int dk, int dv, float scale,
                             void* o, float* hT,
                             void* workspace, size_t workspace_bytes, kda_stream_t stream,
                             void* const* events) {
     if (!events) return KDA_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, qkv_dtype, g, beta, h0, cu_seqlens, num_seqs, B, T, H, dk, dv,
-                    scale, o, hT, workspace, workspace_bytes, stream, events);
+    return fwd_impl(q, k, v, qkv_dtype, g, g_dtype, beta, h0, cu_seqlens, num_seqs, B, T, H, dk,
+                    dv, scale, o, hT, workspace, workspace_bytes, stream, events);
 }
 
 kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* device_error) {

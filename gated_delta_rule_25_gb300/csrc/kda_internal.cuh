@@ -134,8 +134,8 @@ cudaError_t ensure_smem(Kernel kern, size_t bytes) {
 // Launchers (each enqueues on `stream`; return cudaGetLastError()).
 cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
                             cudaStream_t stream);
-cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, const void* q, const void* k,
-                           const void* v, const float* g, const float* beta, uint8_t* ws,
+cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,
+                           const void* v, const void* g, const float* beta, uint8_t* ws,
                            cudaStream_t stream);
 cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                          float* hT, uint8_t* ws, cudaStream_t stream);

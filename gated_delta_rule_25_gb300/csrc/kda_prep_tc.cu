@@ -249,7 +249,7 @@ __device__ __forceinline__ void inv_join(float* X, const float* A, float* T, int
     __syncthreads();
 }
 
-template <int DK, int DV, typename TIn>
+template <int DK, int DV, typename TIn, typename TG>
 __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -305,15 +305,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of one head per tensor, rows past the end of the tensor read as zero) into
     // shared regions that are dead while the previous item finishes: bf16 q and k in the
     // upper halves of qn and kn (fp32 rows are written over them only after every
-    // thread has read its raw words), g into al, v into vs (bf16) or, as fp32, into
-    // the A and X arrays.
+    // thread has read its raw words), g into al (fp32 g) or the upper half of al
+    // (bf16 g), v into vs (bf16) or, as fp32, into the A and X arrays.
     constexpr bool kBf16In = sizeof(TIn) == 2;
+    constexpr bool kBf16G = sizeof(TG) == 2;
     uint8_t* const st_q = reinterpret_cast<uint8_t*>(sm.qn) + (kBf16In ? kChunk * DK * 2 : 0);
     uint8_t* const st_k = reinterpret_cast<uint8_t*>(sm.kn) + (kBf16In ? kChunk * DK * 2 : 0);
-    uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.al);
+    uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.al) + (kBf16G ? kChunk * DK * 2 : 0);
     uint8_t* const st_v = kBf16In ? reinterpret_cast<uint8_t*>(sm.vs) : reinterpret_cast<uint8_t*>(sm.A);
     static_assert(kBf16In || kChunk * DV * 4 <= 2 * kChunk * (kChunk + 1) * 4, "v staging");
-    constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * 4, VB = DV * sizeof(TIn);
+    constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * sizeof(TG), VB = DV * sizeof(TIn);
     // Output staging for the bulk stores of w and u (in the operand region).
     __nv_bfloat16* const st_w = reinterpret_cast<__nv_bfloat16*>(&sm.ops);
     float* const st_u = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sm.ops) + kChunk * DK * 2);
@@ -370,21 +371,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ld_phase ^= 1u;
         const int L = rows_cur.y;
         constexpr int QW = (int)sizeof(TIn) / 2;  // 16-byte words per 8 elements
-        uint4 rq[NP][QW], rk[NP][QW], rg[NP][2];
+        constexpr int GW = (int)sizeof(TG) / 2;
+        uint4 rq[NP][QW], rk[NP][QW], rg[NP][GW];
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = rsub + p * RP;
             const bool ok_r = r < L;
             const uint4* wq = reinterpret_cast<const uint4*>(st_q + r * QB + ck * 8 * sizeof(TIn));
             const uint4* wk = reinterpret_cast<const uint4*>(st_k + r * QB + ck * 8 * sizeof(TIn));
-            const uint4* wg = reinterpret_cast<const uint4*>(st_g + r * GB + ck * 32);
+            const uint4* wg = reinterpret_cast<const uint4*>(st_g + r * GB + ck * 8 * sizeof(TG));
 #pragma unroll
             for (int w2 = 0; w2 < QW; ++w2) {
                 rq[p][w2] = ok_r ? wq[w2] : make_uint4(0, 0, 0, 0);
                 rk[p][w2] = ok_r ? wk[w2] : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int w2 = 0; w2 < 2; ++w2) rg[p][w2] = ok_r ? wg[w2] : make_uint4(0, 0, 0, 0);
+            for (int w2 = 0; w2 < GW; ++w2) rg[p][w2] = ok_r ? wg[w2] : make_uint4(0, 0, 0, 0);
         }
         __syncthreads();  // every raw word is read before fp32 rows overwrite them
 #pragma unroll
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float xq[8], xk[8], xg[8];
             unpack8<TIn>(rq[p], xq);
             unpack8<TIn>(rk[p], xk);
-            unpack8<float>(rg[p], xg);
+            unpack8<TG>(rg[p], xg);
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -926,10 +928,10 @@ bool encode_rows(CUtensorMap* m, const void* base, bool f32, int D, int H, long 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DK, int DV, typename TIn>
-cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+template <int DK, int DV, typename TIn, typename TG>
+cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v, const void* g,
                      const float* beta, uint8_t* ws, cudaStream_t stream) {
-    auto kern = prep_tc_kernel<DK, DV, TIn>;
+    auto kern = prep_tc_kernel<DK, DV, TIn, TG>;
     const size_t smem = sizeof(PrepSmem<DK, DV>);
     const WsLayout W(d);
     const long long tokens = (long long)d.B * d.T;
@@ -939,7 +941,7 @@ cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v,
     constexpr bool f32 = sizeof(TIn) == 4;
     CUtensorMap tq, tk, tv, tg;
     if (!encode_rows(&tq, q, f32, DK, d.H, tokens) || !encode_rows(&tk, k, f32, DK, d.H, tokens) ||
-        !encode_rows(&tv, v, f32, DV, d.H, tokens) || !encode_rows(&tg, g, true, DK, d.H, tokens))
+        !encode_rows(&tv, v, f32, DV, d.H, tokens) || !encode_rows(&tg, g, sizeof(TG) == 4, DK, d.H, tokens))
         return cudaErrorInvalidValue;
     const long long items = W.cmax * d.H;
     const unsigned grid = (unsigned)(items < num_sms() ? items : num_sms());  // persistent
@@ -949,13 +951,17 @@ cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v,
 
 }  // namespace
 
-cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, const void* q, const void* k,
-                           const void* v, const float* g, const float* beta, uint8_t* ws,
+cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,
+                           const void* v, const void* g, const float* beta, uint8_t* ws,
                            cudaStream_t stream) {
-#define KDA_PREP_CASE(DK_, DV_)                                                                   \
-    if (d.dk == DK_ && d.dv == DV_)                                                               \
-        return qkv_bf16 ? launch_t<DK_, DV_, __nv_bfloat16>(d, q, k, v, g, beta, ws, stream)       \
-                        : launch_t<DK_, DV_, float>(d, q, k, v, g, beta, ws, stream);
+    using bf = __nv_bfloat16;
+#define KDA_PREP_CASE(DK_, DV_)                                                                  \
+    if (d.dk == DK_ && d.dv == DV_) {                                                            \
+        if (!qkv_bf16) return g_bf16 ? cudaErrorInvalidValue                                     \
+                                     : launch_t<DK_, DV_, float, float>(d, q, k, v, g, beta, ws, stream); \
+        return g_bf16 ? launch_t<DK_, DV_, bf, bf>(d, q, k, v, g, beta, ws, stream)               \
+                      : launch_t<DK_, DV_, bf, float>(d, q, k, v, g, beta, ws, stream);           \
+    }
     KDA_PREP_CASE(64, 64)
     KDA_PREP_CASE(64, 128)
     KDA_PREP_CASE(128, 64)

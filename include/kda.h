@@ -106,14 +106,30 @@ const char* kda_status_string(kda_status status);
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /*
- * kda_fwd, and in addition cudaEventRecord(events[i], stream) just before its i-th
- * kernel launch and events[n] after the last one, n = kda_fwd_launch_count(...),
+ * kda_fwd with the gate g stored as fp32 (g_dtype = KDA_FP32, exactly kda_fwd) or
+ * bf16 (g_dtype = KDA_BF16, which needs qkv_dtype = KDA_BF16): a bf16 gate halves
+ * the gate's bytes, the largest input at d = 128 ("NVIDIA Kernel Design Agents
+ * optimize Kimi Delta Attention", section 01 RESULTS, names the inputs and their
+ * dtypes; the gate's dtype is left open there).  The computation is the same, from
+ * the gate values as stored.  Other statuses as kda_fwd; an unsupported
+ * combination of dtypes is KDA_ERR_UNSUPPORTED.
+ */
+kda_status kda_fwd_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                      const void* g, kda_dtype g_dtype, const float* beta, const float* h0,
+                      const int32_t* cu_seqlens, int num_seqs,
+                      int B, int T, int H, int dk, int dv, float scale,
+                      void* o, float* hT,
+                      void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_fwd_ex, and in addition cudaEventRecord(events[i], stream) just before its
+ * i-th kernel launch and events[n] after the last one, n = kda_fwd_launch_count(...),
  * so that a profiler can time each kernel on the stream it runs on.  `events`
  * holds n + 1 caller-created cudaEvent_t handles.  Same arguments and statuses as
- * kda_fwd (KDA_ERR_CUDA if an event record fails).
+ * kda_fwd_ex (KDA_ERR_CUDA if an event record fails).
  */
 kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
-                            const float* g, const float* beta, const float* h0,
+                            const void* g, kda_dtype g_dtype, const float* beta, const float* h0,
                             const int32_t* cu_seqlens, int num_seqs,
                             int B, int T, int H, int dk, int dv, float scale,
                             void* o, float* hT,

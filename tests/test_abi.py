@@ -123,3 +123,17 @@ def test_python_decode_fails_loudly_without_cuda():
     x = torch.zeros(2, 1, 64)
     with pytest.raises(ValueError):
         kda.decode(x, x, x, x.float(), torch.zeros(2, 1))
+
+
+def test_fwd_ex_gate_dtypes(lib):
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails host checks
+
+    def call(dt, gdt, **kw):
+        a = dict(ws=ctypes.c_void_p(1 << 20), wsb=1 << 40)
+        a.update(kw)
+        return lib.kda_fwd_ex(p, p, p, dt, p, gdt, p, None, None, 1, 1, 64, 2, 64, 64, 0.125, p,
+                              None, a["ws"], a["wsb"], None)
+    assert call(1, 0) == 2      # bf16 gate with fp32 q/k/v
+    assert call(0, 5) == 2      # unknown gate dtype
+    assert call(0, 0, wsb=16) == 4   # valid dtypes reach the workspace check
+    assert call(0, 1, wsb=16) == 4

@@ -102,6 +102,19 @@ def test_stress_probes(kda, kind):
     _assert_parity(x, *_gpu(kda, x))
 
 
+def test_bf16_gate(kda):
+    """kda_fwd_ex with a bf16 gate: parity against the oracle on the stored bf16 gate
+    values, and bit-identical to the fp32-gate path fed the same values."""
+    x = gen.make_lengths([300, 64, 1, 129], seed=12, salt=SALT, H=3, d=128)
+    x.g = x.g.to(torch.bfloat16)
+    o16, h16 = _gpu(kda, x)
+    _assert_parity(x, o16, h16)
+    x32 = gen.make_lengths([300, 64, 1, 129], seed=12, salt=SALT, H=3, d=128)
+    x32.g = x.g.float()
+    o32, h32 = _gpu(kda, x32)
+    assert torch.equal(o16, o32) and torch.equal(h16, h32)
+
+
 @pytest.mark.parametrize("salt", [4013173612, 1, 9])
 def test_repeated_keys_fixed_salts(kda, salt):
     """The repeated-keys probe is the one closest to the state gate (every token writes
