@@ -59,7 +59,7 @@ struct __align__(128) PrepSmem {
             __nv_bfloat16 l8q[32 * DK];
             __nv_bfloat16 r8[32 * DK];      // kh_j D(16R+8, j), j in [16R, 16R+8)
         } m;
-        struct {
+        struct T {
             __nv_bfloat16 xop[kChunk * kChunk];        // X Diag(beta), operand layout
             __nv_bfloat16 xlo[kChunk * kChunk];        // its rounding remainder (hi + lo split)
             __nv_bfloat16 bop[(DK + DV) * kChunk];     // [kh*gamma | v]^T, operand layout
@@ -68,6 +68,7 @@ struct __align__(128) PrepSmem {
     } ops;
     float bs[kChunk];
     float gb[8 * DK];  // alpha(0..8b) per block start b and channel (kept for the w operand)
+    float sb[8 * DK];  // alpha(8b+8..63) per block b and channel (kept for KT)
     uint64_t bar;
     uint64_t ld_bar;  // bulk copies of an item's raw inputs
     uint32_t tmem;
@@ -315,6 +316,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* const st_v = kBf16In ? reinterpret_cast<uint8_t*>(sm.vs) : reinterpret_cast<uint8_t*>(sm.A);
     static_assert(kBf16In || kChunk * DV * 4 <= 2 * kChunk * (kChunk + 1) * 4, "v staging");
     constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * sizeof(TG), VB = DV * sizeof(TIn);
+    // KT staging for its bulk store (two halves of KTH floats).  bf16 inputs: the A
+    // array (dead after the inverse) and, at dk = 128, the operand region past the
+    // tcgen05 operands -- neither is touched by the next item's copies.  fp32 inputs
+    // (their v lands in A): the qn array, and the next item's copies are issued only
+    // once the store has read it.
+    constexpr int KTH = DK * kChunk / 2;
+    constexpr size_t kOpsT = sizeof(typename Sm::Ops::T);
+    float* const st_kt0 = kBf16In ? sm.A : sm.qn;
+    float* const st_kt1 = (kBf16In && DK == 128)
+                              ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sm.ops) + kOpsT)
+                              : st_kt0 + KTH;
+    static_assert(!kBf16In || (DK == 128 ? KTH : 2 * KTH) * 4 <= kChunk * (kChunk + 1) * 4, "KT in A");
+    static_assert(!kBf16In || DK != 128 || kOpsT + KTH * 4 <= sizeof(typename Sm::Ops), "KT in ops");
+    static_assert(kChunk * DK * 2 + kChunk * DV * 4 <= kOpsT || DK != 128, "w/u staging below KT");
     // Output staging for the bulk stores of w and u (in the operand region).
     __nv_bfloat16* const st_w = reinterpret_cast<__nv_bfloat16*>(&sm.ops);
     float* const st_u = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sm.ops) + kChunk * DK * 2);
@@ -346,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           : Item{0, H};
     int2 rows_cur = rows_of(item);
     if (item.h < H) {
-        if (tid == 32) issue_copies(item, rows_cur);
+        if (tid == 0) issue_copies(item, rows_cur);
         load_beta(item, rows_cur);
     }
     uint32_t ld_phase = 0;
@@ -458,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         float* Bi = sm.X;                 // inner block products alpha(8b+1..8b+7) [8][DK]
         float* Gb = sm.gb;                // [8][DK]
-        float* Sb = sm.X + 16 * DK;       // [8][DK]
+        float* Sb = sm.sb;                // [8][DK]
         float* Mt = sm.A;                 // M(b, R): 2 + 4 + 6 rows of [DK]
         constexpr int TPB = kThreads / DK;   // tasks per block pass
         // (a) inner products of every block
@@ -524,22 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 6; u >= 0; --u) gq[u] = mul2(gq[u + 1], al[u + 1]);
             const float2 gb = *reinterpret_cast<const float2*>(&Gb[bb * DK + ch]);
-            const float2 sb = *reinterpret_cast<const float2*>(&Sb[bb * DK + ch]);
-            // QG = qh * gamma (global, operand layout) and KT = (kh * gamma_L / gamma)^T
-            float kt0[8], kt1[8];
+            // QG = qh * gamma (global, operand layout); KT is formed in P6
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const float2 qgv = mul2(qq[u], mul2(gb, f[u]));
                 *reinterpret_cast<uint32_t*>(&gWQ[op_index_rm(kChunk + r0 + u, ch, DK)]) = pack_bf16(qgv.x, qgv.y);
-                const float2 ktv = mul2(kq[u], mul2(gq[u], sb));
-                kt0[u] = ktv.x;
-                kt1[u] = ktv.y;
             }
-            // fp32 (tf32 operand layout): rows r0..r0+7 are two core matrices of 4
-            *reinterpret_cast<float4*>(&gKT[op_index32(ch, r0, DK)]) = make_float4(kt0[0], kt0[1], kt0[2], kt0[3]);
-            *reinterpret_cast<float4*>(&gKT[op_index32(ch, r0 + 4, DK)]) = make_float4(kt0[4], kt0[5], kt0[6], kt0[7]);
-            *reinterpret_cast<float4*>(&gKT[op_index32(ch + 1, r0, DK)]) = make_float4(kt1[0], kt1[1], kt1[2], kt1[3]);
-            *reinterpret_cast<float4*>(&gKT[op_index32(ch + 1, r0 + 4, DK)]) = make_float4(kt1[4], kt1[5], kt1[6], kt1[7]);
             const int R = bb >> 1;
             if (bb >= 2) {  // 16-level row factors D(r, 16R)
                 float2 pre = make_float2(1.f, 1.f);
@@ -800,14 +805,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = tid; e < 8 * NB; e += kThreads) {
             const int bb = e / NB, col = e % NB, r0 = 8 * bb;
             if (col < DK) {
-                float x[8];
-                float f = sm.gb[bb * DK + col];
+                // gamma_r = Gb_b * alpha(r0+1..r) and gamma_L / gamma_r = alpha(r+1..r0+7) * Sb_b
+                float a[8], kv[8], x[8], kt[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    if (u > 0) f *= sm.al[(r0 + u) * DK + col];
-                    x[u] = sm.kn[(r0 + u) * DK + col] * f;
+                    a[u] = sm.al[(r0 + u) * DK + col];
+                    kv[u] = sm.kn[(r0 + u) * DK + col];
+                }
+                float f = sm.gb[bb * DK + col], bk = sm.sb[bb * DK + col];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (u > 0) f *= a[u];
+                    x[u] = kv[u] * f;
+                }
+#pragma unroll
+                for (int u = 7; u >= 0; --u) {
+                    kt[u] = kv[u] * bk;
+                    bk *= a[u];
                 }
                 *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(col, r0, NB)]) = pack8(x);
+                // KT (fp32, tf32 operand layout): rows r0..r0+7 are two 16-byte runs
+                float* kth = r0 < kChunk / 2 ? st_kt0 : st_kt1 - KTH;  // rows 0-31 | 32-63
+                *reinterpret_cast<float4*>(&kth[op_index32(col, r0, DK)]) = make_float4(kt[0], kt[1], kt[2], kt[3]);
+                *reinterpret_cast<float4*>(&kth[op_index32(col, r0 + 4, DK)]) = make_float4(kt[4], kt[5], kt[6], kt[7]);
             } else {
                 const int dcol = col - DK;
                 uint4 u4;
@@ -839,11 +859,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                               idesc, part > 0 || kk > 0);
         }
         ptx::mma_commit(&sm.bar);
+        // KT leaves by bulk copies (rows 0-31 and 32-63 of the chunk are the two
+        // contiguous halves of its operand layout)
+        ptx::bulk_s2g(gKT, st_kt0, KTH * 4);
+        ptx::bulk_s2g(gKT + KTH, st_kt1, KTH * 4);
+        ptx::bulk_commit();
+        if (!kBf16In) ptx::bulk_wait_read_all();  // fp32 inputs land where KT was staged
+        if (next.h < H) issue_copies(next, rows_next);  // lands while the epilogue runs
     }
-    if (next.h < H) {  // lands while the MMA and its epilogue run
-        if (tid == 32) issue_copies(next, rows_next);
-        load_beta(next, rows_next);
-    }
+    if (next.h < H) load_beta(next, rows_next);
     const bool ok = ptx::mbar_wait_or_abort(&sm.bar, phase, &sm.abort);
     if (!ok && tid == 0) atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
     ptx::tc_fence_after();
