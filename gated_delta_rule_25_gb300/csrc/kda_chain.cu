@@ -1,15 +1,17 @@
-// State recurrence across chunks on the tcgen05 tensor cores: one CTA per
-// (sequence, head, 32-column value tile).  The state's value columns evolve
-// independently, so each value tile is a chain of its own.
+// State recurrence across chunks on the tcgen05 tensor cores: one chain per
+// (sequence, head, NV-column value tile), NV = 32 or 64.  The state's value columns
+// evolve independently, so each value tile is a chain of its own; 64-column tiles
+// halve the number of chains (and the MMA issues per unit of work) when there are
+// more chains than SMs.
 //
 // For each chunk of the sequence, in order ("Autoresearch on Kimi Delta
 // Attention", section THE MECHANISM: the state moves sequentially between blocks
 // of tokens; "NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section
 // 01 RESULTS: the recurrent state must stay fp32, a bf16 state loses accuracy):
-//   [w S ; QG S]  = [w ; QG] S                     GEMM1  M=128, N=32, K=dk
+//   [w S ; QG S]  = [w ; QG] S                     GEMM1  M=128, N=NV, K=dk
 //   U  = u - w S
-//   S <- Diag(exp(Gamma_L)) S + KT U               GEMM2  M=dk,  N=32, K=64 (tf32)
-//   O  = scale (QG S + P U)                        GEMM3  M=128, N=32, K=64
+//   S <- Diag(exp(Gamma_L)) S + KT U               GEMM2  M=dk,  N=NV, K=64 (tf32)
+//   O  = scale (QG S + P U)                        GEMM3  M=128, N=NV, K=64
 // (QG = qh * exp(Gamma)).  w and QG arrive as one 128-row operand tile, so one
 // product gives both w S (accumulator rows 0-63) and QG S (rows 64-127).  GEMM3
 // accumulates P U onto rows 64-127 of the same accumulator: its A descriptor
@@ -47,46 +49,50 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kStages = 2;
-constexpr int NV = kNV;
 constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
 
-// GEMM2's B operand: U^T (32 value columns x 64 chunk rows) in fp32, K-major core
+// GEMM2's B operand: U^T (NV value columns x 64 chunk rows) in fp32, K-major core
 // matrices of 8 columns x 4 rows (16 bytes each).  K-adjacent core matrices sit
 // kU32Lbo = 144 bytes apart (not 128), so a warp's 32 consecutive chunk rows of one
 // column hit 32 different banks when the epilogue writes them.
 constexpr uint32_t kU32Lbo = 144, kU32Sbo = (kChunk / 4) * kU32Lbo;
-constexpr int kU32Words = (NV / 8) * kU32Sbo / 4;
+template <int NV>
+constexpr int u32_words() { return (NV / 8) * kU32Sbo / 4; }
 __device__ inline int u32_index(int n, int r) {
     return (int)(((n >> 3) * kU32Sbo + (r >> 2) * kU32Lbo) / 4) + ((n & 7) << 2) + (r & 3);
 }
 
-template <int DK>
+template <int DK, int NV>
 struct __align__(128) ChainStage {
     __nv_bfloat16 WQ[2 * kChunk * DK];  // row-block-major operand layout, 128 x DK: w, then QG
     float KT[DK * kChunk];           // tf32 operand layout, DK x 64
     __nv_bfloat16 P[kChunk * kChunk];
-    float U0[kChunk * NV];           // 64 x 32 slab of u: [8 column groups][64 rows][4]
+    float U0[kChunk * NV];           // NV/32 slabs of u, each [8 column groups][64 rows][4]
     float GL[DK];
     int4 item;                       // {sequence, head, value tile, chunk index j}
     int4 info;                       // {chunks of the item, first token row, rows, end marker}
 };
 
-template <int DK>
+template <int DK, int NV>
 struct __align__(128) ChainSmem {
-    ChainStage<DK> st[kStages];
-    __nv_bfloat16 Sop[2][NV * DK];   // N-major operand (B of GEMM1), two copies
+    ChainStage<DK, NV> st[kStages];
+    __nv_bfloat16 Sop[NV * DK];      // N-major operand (B of GEMM1)
     __nv_bfloat16 Uop[NV * kChunk];  // N-major operand (B of GEMM3)
-    float Uop32[kU32Words];          // K-major tf32 operand (B of GEMM2), padded
+    float Uop32[u32_words<NV>()];    // K-major tf32 operand (B of GEMM2), padded
     uint64_t full[kStages], empty[kStages], d1, d2, d3[2], uready, fin, fin3;
     uint32_t tmem_base;
     int abort;
 };
 
-// TMEM columns: D1 (GEMM1, then GEMM3 on top) double buffer [0, 64), D2 [64, 96).
-constexpr uint32_t kColD1 = 0, kColD2 = 64, kTmemCols = 128;
+// TMEM columns: D1 (GEMM1, then GEMM3 on top) double buffer [0, 2 NV), D2 [2 NV, 3 NV).
+template <int NV>
+struct Cols {
+    static constexpr uint32_t D1 = 0, D2 = 2 * NV, total = NV == 32 ? 128 : 256;
+};
 
-// Element index of (n, k) in an N-major, unswizzled operand with N = 32 rows:
+// Element index of (n, k) in an N-major, unswizzled operand with N = NV rows:
 // 8 x 8 core matrices, 8 consecutive n contiguous, n-blocks fastest.
+template <int NV>
 __device__ inline int nmaj_index(int n, int k) {
     return (((k >> 3) * (NV / 8) + (n >> 3)) << 6) + ((k & 7) << 3) + (n & 7);
 }
@@ -124,7 +130,8 @@ __device__ inline void raise_error(uint8_t* ws, volatile int* abort) {
     atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
 }
 
-// Writes 32 output values of one row (bf16 or fp32) with 16-byte stores.
+// Writes NV output values of one row (bf16 or fp32) with 16-byte stores.
+template <int NV>
 __device__ inline void store_row(__nv_bfloat16* p, const float (&x)[NV], float scale) {
 #pragma unroll
     for (int i = 0; i < NV; i += 8) {
@@ -135,6 +142,7 @@ __device__ inline void store_row(__nv_bfloat16* p, const float (&x)[NV], float s
         *reinterpret_cast<uint4*>(p + i) = u;
     }
 }
+template <int NV>
 __device__ inline void store_row(float* p, const float (&x)[NV], float scale) {
 #pragma unroll
     for (int i = 0; i < NV; i += 4)
@@ -142,18 +150,22 @@ __device__ inline void store_row(float* p, const float (&x)[NV], float scale) {
             make_float4(scale * x[i], scale * x[i + 1], scale * x[i + 2], scale * x[i + 3]);
 }
 
-__device__ inline void tmem_ld32(uint32_t taddr, float (&x)[NV]) {
-    ptx::tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&x[0]));
-    ptx::tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(&x[16]));
+// NV consecutive TMEM columns of this warp's 32 lanes, then one wait.
+template <int NV>
+__device__ inline void tmem_ldnv(uint32_t taddr, float (&x)[NV]) {
+#pragma unroll
+    for (int i = 0; i < NV / 16; ++i)
+        ptx::tmem_ld16(taddr + 16 * i, *reinterpret_cast<float(*)[16]>(&x[16 * i]));
     ptx::tmem_ld_wait();
 }
 
-template <int DK, int DV, typename TOut>
+template <int DK, int DV, int NV, typename TOut>
 __global__ void __launch_bounds__(kThreads, 1)
     chain_tc_kernel(Dims d, const float* __restrict__ h0, float scale, TOut* __restrict__ o,
                     float* __restrict__ hT, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    ChainSmem<DK>& sm = *reinterpret_cast<ChainSmem<DK>*>(smem_raw);
+    ChainSmem<DK, NV>& sm = *reinterpret_cast<ChainSmem<DK, NV>*>(smem_raw);
+    constexpr uint32_t kColD1 = Cols<NV>::D1, kColD2 = Cols<NV>::D2, kTmemCols = Cols<NV>::total;
     constexpr int NVT = DV / NV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const WsLayout W(d);
@@ -283,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * w) << 16;
         const int ch = acc_row<DK>(w, l);     // key channel of this thread's state row
         const int ur = 32 * w + l;            // D1 row (lane): w S rows 0-63, output rows 64-127
-        const uint32_t sop0 = ptx::smem_u32(sm.Sop[0]), uop32 = ptx::smem_u32(sm.Uop32);
+        const uint32_t sop = ptx::smem_u32(sm.Sop), uop32 = ptx::smem_u32(sm.Uop32);
         constexpr uint32_t id_w = ptx::idesc_bf16(128, NV) | kBMajorMN;
         constexpr uint32_t id_k = ptx::idesc_tf32(DK, NV);   // both K-major
         float S[NV];
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int nb = 0; nb < NV; nb += 8)
-                        *reinterpret_cast<uint4*>(&sm.Sop[gj & 1][nmaj_index(nb, ch)]) =
+                        *reinterpret_cast<uint4*>(&sm.Sop[nmaj_index<NV>(nb, ch)]) =
                             make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
                                        pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
                 }
@@ -326,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!end && tid == 0) {
                 ptx::tc_fence_after();
                 const uint32_t wa = ptx::smem_u32(sm.st[st].WQ);
-                const uint32_t sop = sop0 + (uint32_t)(gj & 1) * (NV * DK * 2);
                 ptx::mma_chain<DK / 16>(tmem + kColD1 + (uint32_t)(gj & 1) * NV,
                                         ptx::smem_desc(wa, 128, (DK / 8) * 128), 256,
                                         ptx::smem_desc(sop, (NV / 8) * 128, 128),
@@ -341,10 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (okl) {
                         ptx::tc_fence_after();
                         float acc[NV];
-                        tmem_ld32(tmem + lane_base + kColD1 + (uint32_t)((gj - 1) & 1) * NV, acc);
+                        tmem_ldnv<NV>(tmem + lane_base + kColD1 + (uint32_t)((gj - 1) & 1) * NV, acc);
                         const int orow = ur - kChunk;
                         if (orow < prev_row.y)
-                            store_row(o + ((size_t)(prev_row.x + orow) * d.H + prev_row.z) * DV +
+                            store_row<NV>(o + ((size_t)(prev_row.x + orow) * d.H + prev_row.z) * DV +
                                           prev_row.w * NV,
                                       acc, scale);
                     }
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (okl) {
                     ptx::tc_fence_after();
                     float acc[NV];
-                    tmem_ld32(tmem + lane_base + kColD1 + (uint32_t)(gj & 1) * NV, acc);
+                    tmem_ldnv<NV>(tmem + lane_base + kColD1 + (uint32_t)(gj & 1) * NV, acc);
                     const float4* u0 = reinterpret_cast<const float4*>(sm.st[st].U0);
                     float U[NV];
 #pragma unroll
@@ -372,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int nb = 0; nb < NV; nb += 8)
-                        *reinterpret_cast<uint4*>(&sm.Uop[nmaj_index(nb, ur)]) = make_uint4(
+                        *reinterpret_cast<uint4*>(&sm.Uop[nmaj_index<NV>(nb, ur)]) = make_uint4(
                             pack_bf16(U[nb], U[nb + 1]), pack_bf16(U[nb + 2], U[nb + 3]),
                             pack_bf16(U[nb + 4], U[nb + 5]), pack_bf16(U[nb + 6], U[nb + 7]));
 #pragma unroll
@@ -401,20 +412,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_commit(&sm.d2);
                 ptx::mma_commit(&sm.empty[st]);
             }
-            // -------- S <- GL * S + D2  ->  Sop[(gj + 1) & 1]
+            // -------- S <- GL * S + D2  ->  Sop (GEMM1 of this step, its one
+            //          reader, completed before the barrier above)
             okl = __all_sync(0xffffffffu, ptx::mbar_wait_or_abort(&sm.d2, gj & 1, abort));
             if (okl) {
                 ptx::tc_fence_after();
                 float acc[NV];
-                tmem_ld32(tmem + lane_base + kColD2, acc);
+                tmem_ldnv<NV>(tmem + lane_base + kColD2, acc);
                 if (ch >= 0) {
                     const float gl = sm.st[st].GL[ch];
-                    __nv_bfloat16* so = sm.Sop[(gj + 1) & 1];
+                    __nv_bfloat16* so = sm.Sop;
 #pragma unroll
                     for (int nb = 0; nb < NV; nb += 8) {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) S[nb + e] = fmaf(gl, S[nb + e], acc[nb + e]);
-                        *reinterpret_cast<uint4*>(&so[nmaj_index(nb, ch)]) =
+                        *reinterpret_cast<uint4*>(&so[nmaj_index<NV>(nb, ch)]) =
                             make_uint4(pack_bf16(S[nb], S[nb + 1]), pack_bf16(S[nb + 2], S[nb + 3]),
                                        pack_bf16(S[nb + 4], S[nb + 5]), pack_bf16(S[nb + 6], S[nb + 7]));
                     }
@@ -449,11 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int DK, int DV, typename TOut>
+template <int DK, int DV, int NV, typename TOut>
 cudaError_t launch_t(const Dims& d, const float* h0, float scale, void* o, float* hT, uint8_t* ws,
                      cudaStream_t stream) {
-    auto kern = chain_tc_kernel<DK, DV, TOut>;
-    const size_t smem = sizeof(ChainSmem<DK>);
+    auto kern = chain_tc_kernel<DK, DV, NV, TOut>;
+    const size_t smem = sizeof(ChainSmem<DK, NV>);
+    static_assert(sizeof(ChainSmem<DK, NV>) <= 227 * 1024, "state kernel shared memory");
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const long long items = (long long)d.N * d.H * (DV / NV);
@@ -463,14 +476,24 @@ cudaError_t launch_t(const Dims& d, const float* h0, float scale, void* o, float
     return cudaGetLastError();
 }
 
+// 64-column value tiles once 32-column chains outnumber the SMs: half the chains,
+// twice the work per MMA issue; otherwise 32-column tiles keep more SMs busy.
+template <int DK, int DV, typename TOut>
+cudaError_t launch_nv(const Dims& d, const float* h0, float scale, void* o, float* hT, uint8_t* ws,
+                      cudaStream_t stream) {
+    const long long chains32 = (long long)d.N * d.H * (DV / 32);
+    if (chains32 > num_sms()) return launch_t<DK, DV, 64, TOut>(d, h0, scale, o, hT, ws, stream);
+    return launch_t<DK, DV, 32, TOut>(d, h0, scale, o, hT, ws, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                          float* hT, uint8_t* ws, cudaStream_t stream) {
-#define KDA_CHAIN_CASE(DK_, DV_)                                                             \
-    if (d.dk == DK_ && d.dv == DV_)                                                          \
-        return qkv_bf16 ? launch_t<DK_, DV_, __nv_bfloat16>(d, h0, scale, o, hT, ws, stream) \
-                        : launch_t<DK_, DV_, float>(d, h0, scale, o, hT, ws, stream);
+#define KDA_CHAIN_CASE(DK_, DV_)                                                              \
+    if (d.dk == DK_ && d.dv == DV_)                                                           \
+        return qkv_bf16 ? launch_nv<DK_, DV_, __nv_bfloat16>(d, h0, scale, o, hT, ws, stream) \
+                        : launch_nv<DK_, DV_, float>(d, h0, scale, o, hT, ws, stream);
     KDA_CHAIN_CASE(64, 64)
     KDA_CHAIN_CASE(64, 128)
     KDA_CHAIN_CASE(128, 64)
