@@ -159,22 +159,25 @@ __device__ inline void mma1688_tf32(float (&d)[4], const uint32_t (&a)[4], uint3
 
 // C (16 x 8 tile at rows cr, cols cc of an N x N block, row stride ldc) = P Q over
 // K = N, P and Q read from fp32 shared memory (row strides ldp, ldq), tf32 inputs,
-// fp32 accumulation; sign -1 negates.  One warp.
-template <int N>
+// fp32 accumulation; sign -1 negates.  One warp.  LOWER_P / LOWER_Q: that operand
+// is lower triangular and its strict upper triangle, never written, reads as zero.
+template <int N, bool LOWER_P, bool LOWER_Q>
 __device__ __forceinline__ void tile_mm_tf32(const float* P, int ldp, const float* Q, int ldq,
                                              float* C, int ldc, int cr, int cc, float sign,
                                              int lane) {
     const int gq = lane >> 2, tq = lane & 3;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    auto pv = [&](int r, int k) { return (LOWER_P && k > r) ? 0.f : P[r * ldp + k]; };
+    auto qv = [&](int k, int n) { return (LOWER_Q && n > k) ? 0.f : Q[k * ldq + n]; };
 #pragma unroll
     for (int k0 = 0; k0 < N; k0 += 8) {
         uint32_t a[4];
-        a[0] = to_tf32(P[(cr + gq) * ldp + k0 + tq]);
-        a[1] = to_tf32(P[(cr + gq + 8) * ldp + k0 + tq]);
-        a[2] = to_tf32(P[(cr + gq) * ldp + k0 + tq + 4]);
-        a[3] = to_tf32(P[(cr + gq + 8) * ldp + k0 + tq + 4]);
-        const uint32_t b0 = to_tf32(Q[(k0 + tq) * ldq + cc + gq]);
-        const uint32_t b1 = to_tf32(Q[(k0 + tq + 4) * ldq + cc + gq]);
+        a[0] = to_tf32(pv(cr + gq, k0 + tq));
+        a[1] = to_tf32(pv(cr + gq + 8, k0 + tq));
+        a[2] = to_tf32(pv(cr + gq, k0 + tq + 4));
+        a[3] = to_tf32(pv(cr + gq + 8, k0 + tq + 4));
+        const uint32_t b0 = to_tf32(qv(k0 + tq, cc + gq));
+        const uint32_t b1 = to_tf32(qv(k0 + tq + 4, cc + gq));
         mma1688_tf32(acc, a, b0, b1);
     }
     C[(cr + gq) * ldc + cc + 2 * tq] = sign * acc[0];
@@ -194,16 +197,16 @@ __device__ __forceinline__ void inv_join_tc(float* X, const float* A, float* T, 
         const int pidx = t / TILES, tt = t % TILES;
         const int r1 = 2 * pidx * N, r2 = r1 + N;
         const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
-        tile_mm_tf32<N>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T + pidx * N * N, N, cr, cc,
-                        1.f, lane);
+        tile_mm_tf32<N, false, true>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T + pidx * N * N,
+                                     N, cr, cc, 1.f, lane);
     }
     __syncthreads();
     for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
         const int pidx = t / TILES, tt = t % TILES;
         const int r1 = 2 * pidx * N, r2 = r1 + N;
         const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
-        tile_mm_tf32<N>(X + r2 * AP + r2, AP, T + pidx * N * N, N, X + r2 * AP + r1, AP, cr, cc,
-                        -1.f, lane);
+        tile_mm_tf32<N, true, false>(X + r2 * AP + r2, AP, T + pidx * N * N, N, X + r2 * AP + r1, AP,
+                                     cr, cc, -1.f, lane);
     }
     __syncthreads();
 }
@@ -753,13 +756,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
-    // X starts at zero (its upper triangle stays zero).  8 x 8 diagonal blocks by
-    // forward substitution, then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two
-    // inverted n x n blocks into one 2n x 2n block (n = 8 on CUDA cores, n = 16 and
-    // 32 with mma.sync on tf32 inputs and fp32 accumulation).
+    // 8 x 8 diagonal blocks by forward substitution (written whole, zeros above the
+    // diagonal), then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two inverted n x n
+    // blocks into one 2n x 2n block (n = 8 on CUDA cores, n = 16 and 32 with mma.sync
+    // on tf32 inputs and fp32 accumulation).  Entries of X above the diagonal are never
+    // written; the joins read them as zero, and nothing else reads them.
     {
-        for (int e = tid; e < kChunk * AP; e += kThreads) sm.X[e] = 0.f;
-        __syncthreads();
         if (tid < 64) {
             const int base = 8 * (tid >> 3), jc = tid & 7;
             float x[8];
