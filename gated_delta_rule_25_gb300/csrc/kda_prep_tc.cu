@@ -730,27 +730,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        if (half == 0 && (lane & 7) == 0) {
-            // A entries into shared memory; the two P rows of the block (8 columns,
-            // zeros above the diagonal) are one 16-byte run each in the operand layout
+        if (half == 0) {
+            // The 8 lanes of a group hold the same totals; lane j stores entry t = j
+            // (lane 0 also t = 8) of A into shared memory and column 8 blk + j of the
+            // group's two P rows (one 16-byte run per row across the group).
+            const int j8 = lane & 7, g0 = lane & ~7;
             const float ba = sm.bs[ra], bz = sm.bs[rz];
-            float pa[8], pz[8], pv[9];
-#pragma unroll
-            for (int t = 0; t < 9; ++t) {
+            auto entry = [&](int t, float aA, float aP) {
                 const bool first = t <= rp;
                 const int r = first ? ra : rz;
-                const int j = first ? ra - t : 8 * blk + 8 - t;
-                if (j < r) sm.A[r * AP + j] = (first ? ba : bz) * (accA[t] + part[t]);
-                pv[t] = accP[t] + part[9 + t];
-            }
+                const int jc = first ? ra - t : 8 * blk + 8 - t;
+                if (jc < r) sm.A[r * AP + jc] = (first ? ba : bz) * (aA + part[t]);
+                return aP + part[9 + t];
+            };
+            float aA = accA[0], aP = accP[0];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                pz[u] = (u <= 7 - rp) ? pv[8 - u] : 0.f;  // row rz, column 8 blk + u: t = 8 - u
-                const int t = rp - u;                       // row ra, column 8 blk + u
-                pa[u] = t == 0 ? pv[0] : t == 1 ? pv[1] : t == 2 ? pv[2] : t == 3 ? pv[3] : 0.f;
-            }
-            *reinterpret_cast<uint4*>(&gP[op_index(ra, 8 * blk, kChunk)]) = pack8(pa);
-            *reinterpret_cast<uint4*>(&gP[op_index(rz, 8 * blk, kChunk)]) = pack8(pz);
+            for (int t = 1; t < 8; ++t)
+                if (j8 == t) { aA = accA[t]; aP = accP[t]; }
+            const float pv = entry(j8, aA, aP);
+            const float pv8 = j8 == 0 ? entry(8, accA[8], accP[8]) : 0.f;
+            // row rz, column 8 blk + u needs t = 8 - u (u <= 7 - rp); row ra needs t = rp - u
+            const float z8 = __shfl_sync(0xffffffffu, pv8, g0);
+            const float zt = __shfl_sync(0xffffffffu, pv, g0 | ((8 - j8) & 7));
+            const float at = __shfl_sync(0xffffffffu, pv, g0 | ((rp - j8) & 7));
+            const float pz = j8 <= 7 - rp ? (j8 == 0 ? z8 : zt) : 0.f;
+            const float pa = j8 <= rp ? at : 0.f;
+            gP[op_index(ra, 8 * blk + j8, kChunk)] = __float2bfloat16(pa);
+            gP[op_index(rz, 8 * blk + j8, kChunk)] = __float2bfloat16(pz);
         }
     }
     __syncthreads();
@@ -804,9 +810,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(&sm.ops.t.xlo[op_index(i, jb, kChunk)]) = pack8(lo);
         }
         // [kh * gamma | v]^T, one task per (8-row block, column): gamma_r = Gb_b f_r
-        for (int e = tid; e < 8 * NB; e += kThreads) {
-            const int bb = e / NB, col = e % NB, r0 = 8 * bb;
-            if (col < DK) {
+        // k columns and v columns in separate loops, so every thread gets its share of
+        // the heavier k tasks
+        for (int e = tid; e < 8 * DK; e += kThreads) {
+            const int bb = e / DK, col = e % DK, r0 = 8 * bb;
+            {
                 // gamma_r = Gb_b * alpha(r0+1..r) and gamma_L / gamma_r = alpha(r+1..r0+7) * Sb_b
                 float a[8], kv[8], x[8], kt[8];
 #pragma unroll
@@ -830,14 +838,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* kth = r0 < kChunk / 2 ? st_kt0 : st_kt1 - KTH;  // rows 0-31 | 32-63
                 *reinterpret_cast<float4*>(&kth[op_index32(col, r0, DK)]) = make_float4(kt[0], kt[1], kt[2], kt[3]);
                 *reinterpret_cast<float4*>(&kth[op_index32(col, r0 + 4, DK)]) = make_float4(kt[4], kt[5], kt[6], kt[7]);
-            } else {
-                const int dcol = col - DK;
-                uint4 u4;
-                __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(&u4);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) hb[u] = sm.vs[(r0 + u) * DV + dcol];
-                *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(col, r0, NB)]) = u4;
             }
+        }
+        for (int e = tid; e < 8 * DV; e += kThreads) {
+            const int bb = e / DV, dcol = e % DV, r0 = 8 * bb;
+            uint4 u4;
+            __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(&u4);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) hb[u] = sm.vs[(r0 + u) * DV + dcol];
+            *reinterpret_cast<uint4*>(&sm.ops.t.bop[op_index(DK + dcol, r0, NB)]) = u4;
         }
         ptx::fence_proxy_async_smem();
     }
