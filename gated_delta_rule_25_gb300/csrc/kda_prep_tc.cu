@@ -347,13 +347,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One thread: the four tensor copies of an item, completing on ld_bar.  Rows
     // of the box past the chunk's end (another sequence's tokens, or zeros past the
     // tensor) are ignored below.
-    auto issue_copies = [&](Item it, int2 nk) {
-        const int hh = it.h;
+    // With bf16 inputs the q copy goes out early (its array is dead after the diagonal
+    // blocks) and the expected bytes of all four are announced with it.
+    auto issue_q = [&](Item it, int2 nk) {
         ptx::mbar_arrive_expect_tx(&sm.ld_bar, (uint32_t)kChunk * (2 * QB + GB + VB));
-        ptx::tma_load_3d(st_q, &tm_q, 0, hh, nk.x, &sm.ld_bar);
-        ptx::tma_load_3d(st_k, &tm_k, 0, hh, nk.x, &sm.ld_bar);
-        ptx::tma_load_3d(st_g, &tm_g, 0, hh, nk.x, &sm.ld_bar);
-        ptx::tma_load_3d(st_v, &tm_v, 0, hh, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_q, &tm_q, 0, it.h, nk.x, &sm.ld_bar);
+    };
+    auto issue_kgv = [&](Item it, int2 nk) {
+        ptx::tma_load_3d(st_k, &tm_k, 0, it.h, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_g, &tm_g, 0, it.h, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_v, &tm_v, 0, it.h, nk.x, &sm.ld_bar);
+    };
+    auto issue_copies = [&](Item it, int2 nk) {
+        issue_q(it, nk);
+        issue_kgv(it, nk);
     };
     auto load_beta = [&](Item it, int2 nk) {
         const int hh = it.h;
@@ -759,7 +766,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             gP[op_index(rz, 8 * blk + j8, kChunk)] = __float2bfloat16(pz);
         }
     }
+    ptx::fence_proxy_async_smem();  // reads of qn above come before the copy into it
     __syncthreads();
+
+    if (kBf16In && tid == 0 && next.h < H) issue_q(next, rows_next);
 
     // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
     // 8 x 8 diagonal blocks by forward substitution (written whole, zeros above the
@@ -876,7 +886,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::bulk_s2g(gKT + KTH, st_kt1, KTH * 4);
         ptx::bulk_commit();
         if (!kBf16In) ptx::bulk_wait_read_all();  // fp32 inputs land where KT was staged
-        if (next.h < H) issue_copies(next, rows_next);  // lands while the epilogue runs
+        if (next.h < H) {  // lands while the epilogue runs
+            if (kBf16In) issue_kgv(next, rows_next);
+            else issue_copies(next, rows_next);
+        }
     }
     if (next.h < H) load_beta(next, rows_next);
     const bool ok = ptx::mbar_wait_or_abort(&sm.bar, phase, &sm.abort);
