@@ -40,10 +40,10 @@ namespace {
 
 constexpr int kThreads = 512;
 
-template <int DK, int DV>
+template <int DK, int DV, typename TIn>
 struct __align__(128) PrepSmem {
-    float qn[kChunk * DK];
-    float kn[kChunk * DK];
+    TIn qr[kChunk * DK];   // raw q rows as copied in; qh = qr * iq[row]
+    float kn[kChunk * DK]; // kh (fp32), widened in place from the raw rows
     float al[kChunk * DK];
     __nv_bfloat16 vs[kChunk * DV];
     float A[kChunk * (kChunk + 1)];
@@ -67,6 +67,7 @@ struct __align__(128) PrepSmem {
         float scratch[32 * 32];
     } ops;
     float bs[kChunk];
+    float iq[kChunk];  // inverse row norms of q (rows past the chunk end are zero)
     float gb[8 * DK];  // alpha(0..8b) per block start b and channel (kept for the w operand)
     float sb[8 * DK];  // alpha(8b+8..63) per block b and channel (kept for KT)
     uint64_t bar;
@@ -94,6 +95,12 @@ __device__ inline void unpack8<float>(const uint4* w, float (&x)[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = f[i];
 }
+
+// Two consecutive elements as fp32.
+__device__ inline float2 ld2(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ inline float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
 __device__ inline uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -126,6 +133,7 @@ __device__ inline float2 mul2(float2 a, float2 b) {
         : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
     return *reinterpret_cast<float2*>(&r);
 }
+__device__ inline float2 scale2(float2 a, float s) { return mul2(a, make_float2(s, s)); }
 __device__ inline float2 fma2(float2 a, float2 b, float2 c) {
     unsigned long long r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;"
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prep_tc_kernel(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const float* __restrict__ beta, uint8_t* __restrict__ ws) {
-    using Sm = PrepSmem<DK, DV>;
+    using Sm = PrepSmem<DK, DV, TIn>;
     constexpr int AP = kChunk + 1;
     constexpr int NB = DK + DV;  // columns of the w/u product
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -307,13 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int vk = tid % VPR, vsub = tid / VPR;
     // Raw inputs of an item arrive by tensor copies (TMA: one box of 64 token rows
     // of one head per tensor, rows past the end of the tensor read as zero) into
-    // shared regions that are dead while the previous item finishes: bf16 q and k in the
-    // upper halves of qn and kn (fp32 rows are written over them only after every
-    // thread has read its raw words), g into al (fp32 g) or the upper half of al
-    // (bf16 g), v into vs (bf16) or, as fp32, into the A and X arrays.
+    // shared regions that are dead while the previous item finishes: q into qr, where
+    // it stays (consumers scale it by the row norm), k into kn and g into al (bf16 k
+    // and g into the upper halves, widened in place to fp32 once every thread has
+    // read its raw words), v into vs (bf16) or, as fp32, into the A and X arrays.
     constexpr bool kBf16In = sizeof(TIn) == 2;
     constexpr bool kBf16G = sizeof(TG) == 2;
-    uint8_t* const st_q = reinterpret_cast<uint8_t*>(sm.qn) + (kBf16In ? kChunk * DK * 2 : 0);
+    uint8_t* const st_q = reinterpret_cast<uint8_t*>(sm.qr);
     uint8_t* const st_k = reinterpret_cast<uint8_t*>(sm.kn) + (kBf16In ? kChunk * DK * 2 : 0);
     uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.al) + (kBf16G ? kChunk * DK * 2 : 0);
     uint8_t* const st_v = kBf16In ? reinterpret_cast<uint8_t*>(sm.vs) : reinterpret_cast<uint8_t*>(sm.A);
@@ -322,11 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // KT staging for its bulk store (two halves of KTH floats).  bf16 inputs: the A
     // array (dead after the inverse) and, at dk = 128, the operand region past the
     // tcgen05 operands -- neither is touched by the next item's copies.  fp32 inputs
-    // (their v lands in A): the qn array, and the next item's copies are issued only
+    // (their v lands in A): the q array, and the next item's copies are issued only
     // once the store has read it.
     constexpr int KTH = DK * kChunk / 2;
     constexpr size_t kOpsT = sizeof(typename Sm::Ops::T);
-    float* const st_kt0 = kBf16In ? sm.A : sm.qn;
+    float* const st_kt0 = kBf16In ? sm.A : reinterpret_cast<float*>(sm.qr);
     float* const st_kt1 = (kBf16In && DK == 128)
                               ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&sm.ops) + kOpsT)
                               : st_kt0 + KTH;
@@ -397,30 +405,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int L = rows_cur.y;
         constexpr int QW = (int)sizeof(TIn) / 2;  // 16-byte words per 8 elements
         constexpr int GW = (int)sizeof(TG) / 2;
-        uint4 rq[NP][QW], rk[NP][QW], rg[NP][GW];
+        uint4 rk[NP][QW], rg[NP][GW];
+        float ikr[NP];
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = rsub + p * RP;
             const bool ok_r = r < L;
-            const uint4* wq = reinterpret_cast<const uint4*>(st_q + r * QB + ck * 8 * sizeof(TIn));
+            uint4* wq = reinterpret_cast<uint4*>(st_q + r * QB + ck * 8 * sizeof(TIn));
             const uint4* wk = reinterpret_cast<const uint4*>(st_k + r * QB + ck * 8 * sizeof(TIn));
             const uint4* wg = reinterpret_cast<const uint4*>(st_g + r * GB + ck * 8 * sizeof(TG));
+            uint4 rq[QW];
 #pragma unroll
             for (int w2 = 0; w2 < QW; ++w2) {
-                rq[p][w2] = ok_r ? wq[w2] : make_uint4(0, 0, 0, 0);
+                rq[w2] = ok_r ? wq[w2] : make_uint4(0, 0, 0, 0);
                 rk[p][w2] = ok_r ? wk[w2] : make_uint4(0, 0, 0, 0);
+                if (!ok_r) wq[w2] = make_uint4(0, 0, 0, 0);  // q rows past the chunk: zero
             }
 #pragma unroll
             for (int w2 = 0; w2 < GW; ++w2) rg[p][w2] = ok_r ? wg[w2] : make_uint4(0, 0, 0, 0);
-        }
-        __syncthreads();  // every raw word is read before fp32 rows overwrite them
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            const int r = rsub + p * RP;
-            float xq[8], xk[8], xg[8];
-            unpack8<TIn>(rq[p], xq);
+            float xq[8], xk[8];
+            unpack8<TIn>(rq, xq);
             unpack8<TIn>(rk[p], xk);
-            unpack8<TG>(rg[p], xg);
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -432,16 +437,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sq += __shfl_xor_sync(0xffffffffu, sq, o);
                 sk += __shfl_xor_sync(0xffffffffu, sk, o);
             }
-            const float iq = rsqrtf(sq + 1e-6f), ik = rsqrtf(sk + 1e-6f);
-            float* dq = &sm.qn[r * DK + ck * 8];
+            if (ck == 0) sm.iq[r] = rsqrtf(sq + 1e-6f);
+            ikr[p] = rsqrtf(sk + 1e-6f);
+        }
+        // raw bf16 k and g words are read before fp32 rows overwrite them
+        if (kBf16In || kBf16G) __syncthreads();
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = rsub + p * RP;
+            float xk[8], xg[8];
+            unpack8<TIn>(rk[p], xk);
+            unpack8<TG>(rg[p], xg);
             float* dk_ = &sm.kn[r * DK + ck * 8];
             float* da = &sm.al[r * DK + ck * 8];
 #pragma unroll
             for (int e = 0; e < 8; e += 4) {
-                *reinterpret_cast<float4*>(dq + e) = make_float4(xq[e] * iq, xq[e + 1] * iq,
-                                                                 xq[e + 2] * iq, xq[e + 3] * iq);
-                *reinterpret_cast<float4*>(dk_ + e) = make_float4(xk[e] * ik, xk[e + 1] * ik,
-                                                                  xk[e + 2] * ik, xk[e + 3] * ik);
+                *reinterpret_cast<float4*>(dk_ + e) = make_float4(xk[e] * ikr[p], xk[e + 1] * ikr[p],
+                                                                  xk[e + 2] * ikr[p], xk[e + 3] * ikr[p]);
                 *reinterpret_cast<float4*>(da + e) = make_float4(__expf(xg[e]), __expf(xg[e + 1]),
                                                                  __expf(xg[e + 2]), __expf(xg[e + 3]));
             }
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 8; ++u) {
                 al[u] = *reinterpret_cast<const float2*>(&sm.al[(r0 + u) * DK + ch]);
                 kq[u] = *reinterpret_cast<const float2*>(&sm.kn[(r0 + u) * DK + ch]);
-                qq[u] = *reinterpret_cast<const float2*>(&sm.qn[(r0 + u) * DK + ch]);
+                qq[u] = scale2(ld2(&sm.qr[(r0 + u) * DK + ch]), sm.iq[r0 + u]);
             }
             f[0] = make_float2(1.f, 1.f);
 #pragma unroll
@@ -695,13 +707,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc2A[9], acc2P[9];
 #pragma unroll
         for (int t = 0; t < 9; ++t) acc2A[t] = acc2P[t] = make_float2(0.f, 0.f);
+        const float iqa = sm.iq[ra], iqz = sm.iq[rz];
 #pragma unroll 1
         for (int i = 0; i < CPp; ++i) {
             const int ch = cg * CG + 2 * ((i + 2 * ((lane >> 2) & 1) + rp) & (CPp - 1));
             const float2 ka = *reinterpret_cast<const float2*>(&sm.kn[ra * DK + ch]);
-            const float2 qa = *reinterpret_cast<const float2*>(&sm.qn[ra * DK + ch]);
+            const float2 qa = scale2(ld2(&sm.qr[ra * DK + ch]), iqa);
             const float2 kz = *reinterpret_cast<const float2*>(&sm.kn[rz * DK + ch]);
-            const float2 qz = *reinterpret_cast<const float2*>(&sm.qn[rz * DK + ch]);
+            const float2 qz = scale2(ld2(&sm.qr[rz * DK + ch]), iqz);
             float2 f = make_float2(1.f, 1.f);
 #pragma unroll
             for (int t = 0; t < 9; ++t) {
@@ -980,7 +993,7 @@ template <int DK, int DV, typename TIn, typename TG>
 cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v, const void* g,
                      const float* beta, uint8_t* ws, cudaStream_t stream) {
     auto kern = prep_tc_kernel<DK, DV, TIn, TG>;
-    const size_t smem = sizeof(PrepSmem<DK, DV>);
+    const size_t smem = sizeof(PrepSmem<DK, DV, TIn>);
     const WsLayout W(d);
     const long long tokens = (long long)d.B * d.T;
     if (W.cmax == 0 || tokens == 0) return cudaSuccess;  // no chunk has a token
