@@ -6,7 +6,7 @@
  *
  * What it computes (the gated delta rule as the method defines it):
  *   "NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section 01 RESULTS
- *   (every kernel is judged against a token-by-token fp64 recurrence) and
+ *   (every kernel is checked against a token-by-token fp64 recurrence) and
  *   section 03 REWARD HACKING (q and k are L2-normalised; an initial state enters;
  *   cu_seqlens packs variable-length sequences);
  *   "Autoresearch on Kimi Delta Attention", section THE MECHANISM (a fixed-size
