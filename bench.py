@@ -142,16 +142,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _traffic_for(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if the kernel's source is
-    unchanged since it was captured (else None)."""
+def _traffic_for(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was captured on this
+    workload and the kernel's source is unchanged since (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         j = json.load(f)
     ent = j.get(kernel)
-    if not ent:
+    if not ent or ent.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "gated_delta_rule_25_gb300", "csrc", ent["source"])
     if not os.path.exists(src):
@@ -330,7 +330,7 @@ def run_decode(args):
                    "salt": salt},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for("decode"),
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for("decode", args.workload),
                      "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -516,7 +516,7 @@ def main():
         "kernels_ms": {KERNEL_NAMES[j] if j < len(KERNEL_NAMES) else f"kernel{j}": per_kernel[j]
                        for j in range(nl)},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for(dom_name),
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for(dom_name, args.workload),
                      "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
         "path_roofline": {"bytes_per_step": _path_bytes(x.tokens, H, D, D, nseq, gb),
                           "achieved_gbs": path_gbs, "frac": path_gbs / hbm},
