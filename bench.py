@@ -142,6 +142,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def whole_job_rate(local_ms_per_step: float, units_per_rank: int, world: int, device=None):
+    """Replicas: every rank times its own steps; the job takes as long as the slowest
+    rank (max over ranks), and processes world x units_per_rank units per step.
+    Returns (ms per step, units per second for the whole job)."""
+    t = torch.tensor([local_ms_per_step], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, world * units_per_rank / (ms * 1e-3)
+
+
 def _traffic_for(kernel: str, workload: str):
     """dram bytes per launch from the committed ncu summary, if it was captured on this
     workload and the kernel's source is unchanged since (else None)."""
@@ -425,11 +436,7 @@ def main():
             per_kernel[j] += row[j].elapsed_time(row[j + 1])
     per_kernel = [t / args.steps for t in per_kernel]
 
-    t_max = torch.tensor([elapsed_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    ms_step = float(t_max.item()) / args.steps
-    value = world * x.tokens / (ms_step * 1e-3)
+    ms_step, value = whole_job_rate(elapsed_ms / args.steps, x.tokens, world, dev)
 
     # parity after timing, on fresh inputs through the same buffers (sampled heads)
     x2, _ = make_workload(args.workload, 1, salt + 7919)
@@ -481,10 +488,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * x.tokens / (float(e_ms.item()) * 1e-3)
+    _, e2e_value = whole_job_rate(e0.elapsed_time(e1) / e2e_steps, x.tokens, world, dev)
 
     if rank != 0:
         if world > 1:
