@@ -1,5 +1,7 @@
-// Per-chunk factors of the chunkwise KDA forward on tensor cores: one CTA per
-// (chunk, head), 512 threads.
+// Per-chunk factors of the chunkwise KDA forward on tensor cores.  Persistent: one
+// 512-thread CTA per SM walks (chunk, head) items in steps of the grid size; the
+// next item's inputs arrive by TMA tensor copies while the current one finishes,
+// and the results leave by bulk copies from shared memory (phases P1-P7 below).
 //
 // For a chunk of L <= 64 tokens of one sequence and head ("Autoresearch on Kimi
 // Delta Attention", section THE MECHANISM: inside a block the work becomes matrix
