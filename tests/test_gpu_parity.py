@@ -90,6 +90,16 @@ def test_head_dims(kda, d):
     _assert_parity(x, *_gpu(kda, x))
 
 
+@pytest.mark.parametrize("d", [(64, 64), (64, 128), (128, 64), (128, 128)])
+def test_head_dims_many_chains(kda, d):
+    """More 32-column chains than SMs, so the state kernel takes 64-column value tiles."""
+    dk, dv = d
+    lens = [70, 1, 129, 64, 0, 33] * 13       # 78 sequences, ragged and empty ones included
+    x = gen.make_lengths(lens, seed=8, salt=SALT, H=4, dk=dk, dv=dv)
+    assert x.num_seqs * x.H * (dv // 32) > 152
+    _assert_parity(x, *_gpu(kda, x))
+
+
 def test_boundary_lengths(kda):
     x = gen.make_lengths([1, 63, 64, 65, 127, 128, 129, 0, 2], seed=5, salt=SALT, H=2, d=128)
     _assert_parity(x, *_gpu(kda, x))
