@@ -8,11 +8,12 @@ one kda_fwd over the whole batch: schedule, per-chunk factors, state recurrence.
 
 Prints one JSON line.  `value` = tokens/s over all ranks with inputs resident in
 HBM; `e2e` = the same metric through the public binding with pinned host buffers,
-host-to-device inputs and device-to-host outputs inside the timed region;
-`roofline` = the dominant kernel's algorithmic bytes per launch over its
-CUDA-event duration, against the measured HBM copy bandwidth.  The per-step input
-(336 MB) and factor workspace (~300 MB) exceed the 129 MB L2, so no L2 flush is
-inserted between steps.  `--impl reference` times the fp64 CPU oracle on this
+every step's host-to-device inputs and device-to-host outputs inside the timed
+region (steps pipelined over two buffer sets and three streams, as a serving loop
+would run them); `roofline` = the dominant kernel's algorithmic bytes per launch
+over its CUDA-event duration, against the measured HBM copy bandwidth.  The
+per-step input (337 MB) and factor workspace (438 MB) exceed the 129 MB L2, so no L2
+flush is inserted between steps.  `--impl reference` times the fp64 CPU oracle on this
 host's cores on the same workload (a bounded number of heads per step).
 """
 from __future__ import annotations
@@ -460,35 +461,58 @@ def main():
         parity = {"heads": hs, "o_rel_rmse": rel_rmse(o.cpu()[:, :, hs], o_ref),
                   "hT_rel_rmse": rel_rmse(hT.cpu()[:, hs], h_ref), "salt": x2.salt}
 
-    # end to end through the public binding: pinned host in, pinned host out
+    # end to end through the public binding: every step copies its inputs in from
+    # pinned host memory and its outputs back.  Steps are pipelined the way a serving
+    # loop would run them: two input/output buffer sets, copies in on one stream,
+    # the forward on the compute stream, copies out on a third, ordered by events.
     host_in = {n: getattr(x, n).pin_memory() for n in ("q", "k", "v", "g", "beta", "h0")}
-    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    h_host = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
-    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    o_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    h_host = [torch.empty(hT.shape, dtype=hT.dtype).pin_memory() for _ in range(2)]
+    dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in.items()} for _ in range(2)]
+    dev_out = [(o, hT), (torch.empty_like(o), torch.empty_like(hT))]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * h_host.element_size()
+    d2h = o_host[0].numel() * o_host[0].element_size() + h_host[0].numel() * h_host[0].element_size()
     e2e_steps = max(3, min(args.steps, 50))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        kda.fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["h0"],
-                xd.cu_seqlens, x.scale, o=o, hT=hT, workspace=ws)
-        o_host.copy_(o, non_blocking=True)
-        h_host.copy_(hT, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_done[b])          # the forward of step i-2 has read buffer b
+            for n, t in host_in.items():
+                dev_in[b][n].copy_(t, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])             # step i-2's outputs have left buffer b
+        ob, hb = dev_out[b]
+        kda.fwd(dev_in[b]["q"], dev_in[b]["k"], dev_in[b]["v"], dev_in[b]["g"], dev_in[b]["beta"],
+                dev_in[b]["h0"], xd.cu_seqlens, x.scale, o=ob, hT=hb, workspace=ws)
+        ev_done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            o_host[b].copy_(ob, non_blocking=True)
+            h_host[b].copy_(hb, non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(stream)
+    e1.record(s_out)                             # after the last step's outputs are on the host
     torch.cuda.synchronize(dev)
     _, e2e_value = whole_job_rate(e0.elapsed_time(e1) / e2e_steps, x.tokens, world, dev)
+    # the pipelined outputs are the forward's: the last step's o against the timed run's
+    e2e_ok = bool(torch.equal(o_host[(e2e_steps - 1) & 1].to(dev), dev_out[(e2e_steps - 1) & 1][0]))
 
     if rank != 0:
         if world > 1:
@@ -526,7 +550,9 @@ def main():
                           "achieved_gbs": path_gbs, "frac": path_gbs / hbm},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "pipelined": "two buffer sets; copies in, forward and copies out on three streams",
+                "outputs_match": e2e_ok},
         "parity": parity,
         "cpu_baseline": cpu,
     }
