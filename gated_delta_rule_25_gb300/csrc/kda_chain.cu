@@ -1,8 +1,9 @@
 // State recurrence across chunks on the tcgen05 tensor cores: one chain per
-// (sequence, head, NV-column value tile), NV = 32 or 64.  The state's value columns
-// evolve independently, so each value tile is a chain of its own; 64-column tiles
-// halve the number of chains (and the MMA issues per unit of work) when there are
-// more chains than SMs.
+// (sequence, head, NV-column value tile), NV = 16, 32 or 64.  The state's value
+// columns evolve independently, so each value tile is a chain of its own: 64-column
+// tiles halve the number of chains (and the MMA issues per unit of work) when there
+// are more chains than SMs, 16-column tiles put twice as many SMs to work when there
+// are few.
 //
 // For each chunk of the sequence, in order ("Autoresearch on Kimi Delta
 // Attention", section THE MECHANISM: the state moves sequentially between blocks
@@ -87,7 +88,7 @@ struct __align__(128) ChainSmem {
 // TMEM columns: D1 (GEMM1, then GEMM3 on top) double buffer [0, 2 NV), D2 [2 NV, 3 NV).
 template <int NV>
 struct Cols {
-    static constexpr uint32_t D1 = 0, D2 = 2 * NV, total = NV == 32 ? 128 : 256;
+    static constexpr uint32_t D1 = 0, D2 = 2 * NV, total = NV == 16 ? 64 : (NV == 32 ? 128 : 256);
 };
 
 // Element index of (n, k) in an N-major, unswizzled operand with N = NV rows:
@@ -476,13 +477,16 @@ cudaError_t launch_t(const Dims& d, const float* h0, float scale, void* o, float
     return cudaGetLastError();
 }
 
-// 64-column value tiles once 32-column chains outnumber the SMs: half the chains,
-// twice the work per MMA issue; otherwise 32-column tiles keep more SMs busy.
+// 64-column value tiles once 32-column chains outnumber the SMs (half the chains,
+// twice the work per MMA issue); 16-column tiles while twice the 32-column chains
+// still fit on the SMs (each chain is latency-bound, so more of them run at once);
+// 32-column tiles in between.
 template <int DK, int DV, typename TOut>
 cudaError_t launch_nv(const Dims& d, const float* h0, float scale, void* o, float* hT, uint8_t* ws,
                       cudaStream_t stream) {
     const long long chains32 = (long long)d.N * d.H * (DV / 32);
     if (chains32 > num_sms()) return launch_t<DK, DV, 64, TOut>(d, h0, scale, o, hT, ws, stream);
+    if (2 * chains32 <= num_sms()) return launch_t<DK, DV, 16, TOut>(d, h0, scale, o, hT, ws, stream);
     return launch_t<DK, DV, 32, TOut>(d, h0, scale, o, hT, ws, stream);
 }
 
