@@ -10,8 +10,9 @@
  *     o_t = scale * S^T qh
  * and hT[s,h] receives the final S.  The library computes this chunkwise (64
  * tokens per chunk): the state moves from chunk to chunk in order, in fp32; the
- * work inside a chunk is matrix products on the tensor cores with bf16 operands
- * and fp32 accumulators.
+ * work inside a chunk is matrix products on the tensor cores with fp32
+ * accumulators, bf16 operands for most, and tf32 inputs for the state update
+ * (whose rounding would persist in the state).
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers, row-major and contiguous:
