@@ -11,10 +11,6 @@
 namespace kda {
 namespace ptx {
 
-// Iterations before a barrier wait gives up (each try_wait also suspends for a
-// while in hardware, so this is far more than a healthy kernel ever waits).
-constexpr uint32_t kWaitLimit = 1u << 24;
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -48,13 +44,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
-}
-
-// Waits for the phase with the given parity to complete; false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
