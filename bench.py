@@ -384,7 +384,11 @@ def main():
     dev = torch.device("cuda", local)
 
     import __graft_entry__
+    if world > 1 and rank != 0:
+        torch.distributed.barrier()      # rank 0 builds first; the others then find it built
     __graft_entry__.build()
+    if world > 1 and rank == 0:
+        torch.distributed.barrier()
     import gated_delta_rule_25_gb300 as kda
 
     salt = gen.fresh_salt() + rank
