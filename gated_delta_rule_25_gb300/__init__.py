@@ -72,6 +72,8 @@ def load_library():
         lib.kda_fwd_noalloc.restype = i32
         lib.kda_fwd_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.kda_fwd_check.restype = i32
+        lib.kda_fwd_noalloc_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.kda_fwd_noalloc_check.restype = i32
         lib.kda_decode.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]
         lib.kda_decode.restype = i32
         lib.kda_status_string.argtypes = [i32]
@@ -103,6 +105,50 @@ def _check(t, name, dtype, shape, device):
         raise ValueError(f"{name}: must be contiguous")
 
 
+def _validate(q, k, v, g, beta, h0, cu_seqlens, o, hT, gate_bf16_ok: bool):
+    """Every dtype and shape check of the forward, before anything is launched.
+
+    Returns (B, T, H, dk, dv, N, device).  Dtypes and shapes are checked before the
+    device, so a wrong argument raises the same error with or without a GPU."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, dk]")
+    if v.dim() != 4:
+        raise ValueError("v must be [B, T, H, dv]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _check(q, "q", q.dtype, (B, T, H, dk), dev)
+    _check(k, "k", q.dtype, (B, T, H, dk), dev)
+    _check(v, "v", q.dtype, (B, T, H, dv), dev)
+    if g.dtype == torch.bfloat16:
+        if not gate_bf16_ok:
+            raise TypeError("g: this entry point takes an fp32 gate")
+        if q.dtype != torch.bfloat16:
+            raise TypeError("a bf16 gate needs bf16 q, k, v")
+    _check(g, "g", g.dtype if g.dtype == torch.bfloat16 else torch.float32, (B, T, H, dk), dev)
+    _check(beta, "beta", torch.float32, (B, T, H), dev)
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("varlen (cu_seqlens) needs B == 1")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a 1-D tensor of num_seqs + 1 offsets")
+        _check(cu_seqlens, "cu_seqlens", torch.int32, (cu_seqlens.numel(),), dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if h0 is not None:
+        _check(h0, "h0", torch.float32, (N, H, dk, dv), dev)
+    if o is not None:
+        _check(o, "o", q.dtype, (B, T, H, dv), dev)
+    if hT is not None:
+        _check(hT, "hT", torch.float32, (N, H, dk, dv), dev)
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    return B, T, H, dk, dv, N, dev
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
         beta: torch.Tensor, h0: Optional[torch.Tensor] = None,
         cu_seqlens: Optional[torch.Tensor] = None, scale: Optional[float] = None, *,
@@ -115,43 +161,16 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     capture with stable addresses).  ``check``: synchronise and raise on a device-side
     error.  ``events``: launch_count + 1 recorded torch.cuda.Event objects; each kernel
     launch is bracketed by two of them (per-kernel timing)."""
+    B, T, H, dk, dv, N, dev = _validate(q, k, v, g, beta, h0, cu_seqlens, o,
+                                        hT if output_final_state else None, True)
     lib = load_library()
-    if q.dim() != 4:
-        raise ValueError("q must be [B, T, H, dk]")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
-    if q.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("q, k, v must be bfloat16 or float32")
-    _check(k, "k", q.dtype, (B, T, H, dk), dev)
-    _check(v, "v", q.dtype, (B, T, H, dv), dev)
-    _check(q, "q", q.dtype, (B, T, H, dk), dev)
-    if g.dtype == torch.bfloat16 and q.dtype != torch.bfloat16:
-        raise TypeError("a bf16 gate needs bf16 q, k, v")
-    _check(g, "g", g.dtype if g.dtype == torch.bfloat16 else torch.float32, (B, T, H, dk), dev)
-    _check(beta, "beta", torch.float32, (B, T, H), dev)
-    if cu_seqlens is not None:
-        if B != 1:
-            raise ValueError("varlen (cu_seqlens) needs B == 1")
-        _check(cu_seqlens, "cu_seqlens", torch.int32, (cu_seqlens.numel(),), dev)
-        N = cu_seqlens.numel() - 1
-    else:
-        N = B
-    if h0 is not None:
-        _check(h0, "h0", torch.float32, (N, H, dk, dv), dev)
     if scale is None:
         scale = dk ** -0.5
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
-    else:
-        _check(o, "o", q.dtype, (B, T, H, dv), dev)
     if output_final_state:
         if hT is None:
             hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
-        else:
-            _check(hT, "hT", torch.float32, (N, H, dk, dv), dev)
     else:
         hT = None
     ws_bytes = int(lib.kda_fwd_workspace_size(B, T, H, dk, dv, N))
@@ -187,25 +206,22 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
 def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                 beta: torch.Tensor, h0: Optional[torch.Tensor] = None,
                 cu_seqlens: Optional[torch.Tensor] = None, scale: Optional[float] = None, *,
-                o: Optional[torch.Tensor] = None,
-                hT: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                o: Optional[torch.Tensor] = None, hT: Optional[torch.Tensor] = None,
+                check: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """The forward through ``kda_fwd_noalloc``: no workspace is passed, the library
     uses the device scratch array built into it (KDA_NOALLOC_SCRATCH_BYTES, 32 MiB).
 
     For callers that cannot allocate device memory where they run the forward
     (a plugin inside an engine that owns all device memory, a path where an
     allocation's latency or failure is not acceptable): pass preallocated ``o``
-    and ``hT``; the call then allocates nothing.  Problems too large for the
-    array raise KdaError with status KDA_ERR_TOO_LARGE.  Calls share the array,
-    so their work must not overlap on the GPU (order them on one stream)."""
+    and ``hT``; the call then allocates nothing.  The arguments get the same dtype
+    and shape checks as ``fwd``, except that the gate must be fp32.  Problems too
+    large for the array raise KdaError with status KDA_ERR_TOO_LARGE.  Calls share
+    the array, so their work must not overlap on the GPU (order them on one
+    stream).  ``check``: synchronise and raise if the device reported an error
+    (``kda_fwd_noalloc_check``)."""
+    B, T, H, dk, dv, N, dev = _validate(q, k, v, g, beta, h0, cu_seqlens, o, hT, False)
     lib = load_library()
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    dev = q.device
-    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
-    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
-        if t.device != dev or not t.is_contiguous():
-            raise ValueError(f"{name}: must be a contiguous tensor on {dev}")
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=dev)
     if hT is None:
@@ -219,6 +235,11 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
                              _ptr(hT), ctypes.c_void_p(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd_noalloc")
+    if check:
+        err = ctypes.c_uint32(0)
+        st = lib.kda_fwd_noalloc_check(ctypes.c_void_p(stream), ctypes.byref(err))
+        if st != KDA_OK:
+            raise KdaError(st, f"kda_fwd_noalloc_check (device error bits {err.value:#x})")
     return o, hT
 
 

@@ -59,3 +59,15 @@ extern "C" kda_status kda_fwd_noalloc(const void* q, const void* k, const void* 
     return kda_fwd(q, k, v, qkv_dtype, g, beta, h0, cu_seqlens, num_seqs, B, T, H, dk, dv, scale,
                    o, hT, scratch, (size_t)KDA_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+extern "C" kda_status kda_fwd_noalloc_check(kda_stream_t stream, uint32_t* device_error) {
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
+    kda::Header hdr{};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&hdr, scratch, sizeof(hdr), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (device_error) *device_error = hdr.error;
+    return hdr.error ? KDA_ERR_DEVICE : KDA_OK;
+}

@@ -165,8 +165,9 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
  *     between calls.  Calls whose work overlaps on the GPU (different streams
  *     without ordering, or host threads racing) corrupt each other's results:
  *     order them on one stream.
- *   - The device error word lives in the built-in array and is not readable here;
- *     callers that need kda_fwd_check use kda_fwd with their own workspace.
+ *   - Conditions only the device can see (malformed cu_seqlens, a bounded wait
+ *     that ran out) set the error word in the built-in array; read it with
+ *     kda_fwd_noalloc_check() after the call.
  * Statuses are kda_fwd's, plus KDA_ERR_TOO_LARGE.
  */
 kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
@@ -174,6 +175,15 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, kda_dtyp
                            const int32_t* cu_seqlens, int num_seqs,
                            int B, int T, int H, int dk, int dv, float scale,
                            void* o, float* hT, kda_stream_t stream);
+
+/*
+ * The kda_fwd_check of kda_fwd_noalloc: synchronises `stream`, then reads the
+ * device error word that the last kda_fwd_noalloc on the current device left in
+ * the built-in scratch array.  Returns KDA_OK, KDA_ERR_DEVICE (and *device_error,
+ * if not NULL, gets the KDA_DEVERR_* bits) or KDA_ERR_CUDA.  Allocates nothing.
+ * The word belongs to the last call on this device, whichever stream made it.
+ */
+kda_status kda_fwd_noalloc_check(kda_stream_t stream, uint32_t* device_error);
 
 /*
  * One recurrence step per sequence: single-token decode ("Autoresearch on Kimi

@@ -36,8 +36,34 @@ def test_noalloc_refuses_oversized_problems_without_touching_the_gpu(kda):
     assert lib.kda_status_string(st) == b"problem too large for the built-in no-allocation scratch"
 
 
+def test_noalloc_binding_checks_arguments_before_any_launch(kda):
+    """The binding checks every argument's dtype and shape before the C call (a wrong
+    dtype would otherwise be read with the wrong element size on the device).  CPU
+    tensors: each mistake raises before the device check is reached."""
+    x = gen.make_lengths([70, 5], seed=24, salt=1, H=2, d=64)
+    t = x.tensors()
+    with pytest.raises(TypeError):       # this entry point takes only an fp32 gate
+        kda.fwd_noalloc(**{**t, "g": t["g"].to(torch.bfloat16)})
+    with pytest.raises(TypeError):       # q, k, v dtypes must agree
+        kda.fwd_noalloc(**{**t, "k": t["k"].float()})
+    with pytest.raises(TypeError):
+        kda.fwd_noalloc(**{**t, "beta": t["beta"].double()})
+    with pytest.raises(TypeError):
+        kda.fwd_noalloc(**{**t, "cu_seqlens": t["cu_seqlens"].long()})
+    with pytest.raises(ValueError):      # an output buffer one token short
+        kda.fwd_noalloc(**t, o=torch.empty(1, x.T - 1, 2, 64, dtype=x.v.dtype))
+    with pytest.raises(ValueError):      # a final-state buffer for the wrong N
+        kda.fwd_noalloc(**t, hT=torch.empty(3, 2, 64, 64))
+    with pytest.raises(ValueError):
+        kda.fwd_noalloc(**{**t, "h0": t["h0"][:1].contiguous()})
+    with pytest.raises(ValueError):      # right dtypes and shapes, but not on a GPU
+        kda.fwd_noalloc(**t)
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_fwd_on_two_calls_in_a_row(kda):
+    """Both entry points run the same kernels on the same inputs, so the results are
+    bit-identical; a stale or shared-scratch bug would show as any differing element."""
     cases = [gen.make_lengths([200, 1, 67, 0, 150], seed=21, salt=gen.fresh_salt(), H=4, d=128),
              gen.make_cfg2(seed=22, salt=gen.fresh_salt(), T=384, H=6, B=2)]
     for x in cases:  # two calls in a row share the built-in scratch
@@ -45,17 +71,32 @@ def test_noalloc_matches_fwd_on_two_calls_in_a_row(kda):
         o_ref, h_ref = kda.fwd(**xd.tensors(), check=True)
         o_na = torch.empty_like(o_ref)
         h_na = torch.empty_like(h_ref)
-        kda.fwd_noalloc(**xd.tensors(), o=o_na, hT=h_na)
+        kda.fwd_noalloc(**xd.tensors(), o=o_na, hT=h_na, check=True)
         torch.cuda.synchronize()
-        assert torch.isfinite(o_na.float()).all() and torch.isfinite(h_na).all()
-        eo = rel_rmse(o_na.cpu(), o_ref.cpu().double())
-        eh = rel_rmse(h_na.cpu(), h_ref.cpu().double())
-        assert eo <= O_TOL and eh <= HT_TOL, (x.name, eo, eh)
+        assert torch.equal(o_na, o_ref) and torch.equal(h_na, h_ref), x.name
+        # and both within the parity gates of the oracle-checked path
+        assert rel_rmse(o_na.cpu(), o_ref.cpu().double()) <= O_TOL
+        assert rel_rmse(h_na.cpu(), h_ref.cpu().double()) <= HT_TOL
+
+
+@pytest.mark.gpu
+def test_noalloc_check_reports_malformed_cu_seqlens(kda):
+    x = gen.make_lengths([10, 20, 34], seed=25, salt=gen.fresh_salt(), H=2, d=64)
+    xd = x.to("cuda")
+    xd.cu_seqlens = torch.tensor([0, 20, 10, 64], dtype=torch.int32, device="cuda")
+    with pytest.raises(kda.KdaError) as e:
+        kda.fwd_noalloc(**xd.tensors(), check=True)
+    assert e.value.status == 6
+    # the next well-formed call clears the word
+    good = x.to("cuda")
+    o, hT = kda.fwd_noalloc(**good.tensors(), check=True)
+    o_ref, h_ref = kda.fwd(**good.tensors())
+    assert torch.equal(o, o_ref) and torch.equal(hT, h_ref)
 
 
 @pytest.mark.gpu
 def test_noalloc_raises_on_oversized_problem(kda):
-    x = gen.make_cfg2(seed=23, T=2048, H=32)  # ~150 MB of factors: above the 32 MiB array
+    x = gen.make_cfg2(seed=23, T=2048, H=32)  # 32 chunks x 32 heads of factors: above the array
     xd = x.to("cuda")
     with pytest.raises(kda.KdaError) as e:
         kda.fwd_noalloc(**xd.tensors())
