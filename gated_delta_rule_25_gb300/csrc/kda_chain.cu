@@ -50,6 +50,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kStages = 2;
+constexpr uint32_t kAMajorMN = 1u << 15;  // instruction-descriptor bit: A is M-major
 constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
 
 // GEMM2's B operand: U^T (NV value columns x 64 chunk rows) in fp32, K-major core
@@ -65,7 +66,7 @@ __device__ inline int u32_index(int n, int r) {
 
 template <int DK, int NV>
 struct __align__(128) ChainStage {
-    __nv_bfloat16 WQ[2 * kChunk * DK];  // row-block-major operand layout, 128 x DK: w, then QG
+    __nv_bfloat16 WQ[2 * kChunk * DK];  // M-major operand, 128 x DK: w, then QG
     float KT[DK * kChunk];           // tf32 operand layout, DK x 64
     __nv_bfloat16 P[kChunk * kChunk];
     float U0[kChunk * NV];           // NV/32 slabs of u, each [8 column groups][64 rows][4]
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ch = acc_row<DK>(w, l);     // key channel of this thread's state row
         const int ur = 32 * w + l;            // D1 row (lane): w S rows 0-63, output rows 64-127
         const uint32_t sop = ptx::smem_u32(sm.Sop), uop32 = ptx::smem_u32(sm.Uop32);
-        constexpr uint32_t id_w = ptx::idesc_bf16(128, NV) | kBMajorMN;
+        constexpr uint32_t id_w = ptx::idesc_bf16(128, NV) | kAMajorMN | kBMajorMN;
         constexpr uint32_t id_k = ptx::idesc_tf32(DK, NV);   // both K-major
         float S[NV];
 #pragma unroll

@@ -1,0 +1,1024 @@
+// Per-chunk factors of the chunkwise KDA forward, every chunk product on tcgen05.
+// Persistent: one 512-thread CTA per SM walks (chunk, head) items in steps of the
+// grid size.  The next item's q, k, g arrive by TMA tensor copies while the current
+// item is still in its products, its v tile lands straight in the tensor-core
+// operand layout, and every result leaves by coalesced 16-byte stores from
+// registers (phases P1-P7 below).
+//
+// For a chunk of L <= 64 tokens of one sequence and head ("Autoresearch on Kimi
+// Delta Attention", section THE MECHANISM: inside a block the work becomes matrix
+// products; "NVIDIA Kernel Design Agents optimize Kimi Delta Attention", section 03
+// REWARD HACKING: L2 normalisation of q and k, the cumulative decay inside each
+// 64-token chunk, the triangular inverse):
+//   qh, kh   = rows of q, k over sqrt(|x|^2 + eps)                  (fp32)
+//   alpha    = exp(g)                                              (one exp per element)
+//   A_ij     = beta_i sum_c kh_ic kh_jc D_c(i, j)                     j < i
+//   P_ij     = sum_c qh_ic kh_jc D_c(i, j)                            j <= i
+//   with D_c(i, j) = exp(Gamma_ic - Gamma_jc) = alpha_c(j+1) ... alpha_c(i)
+//   X        = (I + A)^-1                                           (fp32, blocked)
+//   u        = X Diag(beta) v                                        (tcgen05, M=64 N=dv K=64)
+//   w^T      = (kh * gamma)^T (X Diag(beta))^T                       (tcgen05, M=dk N=64 K=64)
+//   QG = qh * gamma,  KT = (kh * gamma_L / gamma)^T,  GL = gamma_L,  gamma = exp(Gamma)
+// X Diag(beta) enters both products split into bf16 hi + lo (two MMA passes).
+//
+// Decay factors without overflow.  Every decay factor is a product of alphas over
+// a run of consecutive tokens, so it lies in [0, 1]: deep decays underflow to zero
+// and nothing overflows (the pages' section 03 describes kernels that formed
+// exp(Gamma) / exp(Gamma') and produced NaN).  A and P are split by levels: a pair
+// (i, j), j < i, belongs to the level s = 2^l of the highest bit in which i and j
+// differ, so that inside an aligned block of 2s rows i lies in the upper half and j
+// in the lower, and the half boundary m separates them.  With m as reference,
+//   D(i, j) = D(i, m) D(m, j),   D(i, m) = alpha(m+1 .. i),   D(m, j) = alpha(j+1 .. m),
+// both in [0, 1], so every level is one plain matrix product of row-scaled and
+// column-scaled keys.  The six levels (s = 1 .. 32) each hold 32 rows and 32
+// columns; two levels share one M = 128, N = 64 tensor-core product (rows
+// [kh R; qh R] of both levels, columns kh C of both), whose two diagonal 32 x 32
+// blocks are the wanted results and whose off-diagonal blocks are ignored.
+#include <cuda.h>          // CUtensorMap (the encoder itself is fetched at run time)
+#include <cudaTypedefs.h>  // the encoder's function-pointer type
+
+#include "kda_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr uint32_t kAMajorMN = 1u << 15;  // instruction-descriptor bit: A is M-major
+constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
+constexpr int AP = kChunk + 1;            // row stride of the fp32 A and X arrays
+
+// Once the level products are done, the operand ring holds the inverse's arrays.
+constexpr int kOffA = 0;                              // A (fp32, 64 x 65)
+constexpr int kOffX = kChunk * AP * 4;                // X (fp32, 64 x 65)
+constexpr int kOffScr = 2 * kChunk * AP * 4;          // inverse scratch (32 x 32 fp32)
+constexpr int kInvBytes = kOffScr + 32 * 32 * 4;
+constexpr int kOffXop = 0;                            // X Diag(beta), bf16 hi (over A)
+constexpr int kOffXlo = kChunk * kChunk * 2;          // and its remainder lo
+
+template <int DK, int DV, typename TIn>
+struct FactorCfg {
+    static constexpr int NBUF = sizeof(TIn) == 2 ? 2 : 1;  // level operand buffers
+    static constexpr int PAIR = 128 * DK * 2 + 64 * DK * 2; // [kh R; qh R] x 2 levels + kh C x 2
+    static constexpr int RING0 = NBUF * PAIR > kInvBytes ? NBUF * PAIR : kInvBytes;
+    // fp32 inputs: the fp32 v tile also lands in the ring before it is converted
+    static constexpr int RING1 = (sizeof(TIn) == 4 && kChunk * DV * 4 > RING0) ? kChunk * DV * 4 : RING0;
+    static constexpr int RING = (RING1 + 1023) / 1024 * 1024;
+};
+
+template <int DK, int DV, typename TIn>
+struct __align__(1024) FactorSmem {
+    using C = FactorCfg<DK, DV, TIn>;
+    uint8_t ring[C::RING];               // level operands, then A, X, X Diag(beta) hi/lo
+    TIn qr[kChunk * DK];                 // raw q rows as copied in; qh = qr * iq[row]
+    TIn kr[kChunk * DK];                 // raw k rows; kh = kr * ik[row]
+    float al[kChunk * DK];               // alpha = exp(g) (g is copied in here)
+    __nv_bfloat16 vs[kChunk * DV];       // v, N-major operand: [DV/8][64 rows][8 columns]
+    __nv_bfloat16 kg[DK * kChunk];       // (kh * gamma)^T, K-major operand (DK x 64)
+    __nv_bfloat16 pst[kChunk * kChunk];  // P staged in its operand layout
+    float blk_a[8 * DK];                 // alpha at the first row of each 8-row block
+    float blk_t[8 * DK];                 // product of alpha over rows 1..7 of each block
+    float diag[2 * kChunk];              // qh_i . kh_i, one partial sum per channel half
+    float bs[kChunk];                    // beta (zero past the chunk end)
+    float iq[kChunk], ik[kChunk];        // inverse row norms (zero past the chunk end)
+    uint64_t ld_bar, v_bar, lv_bar[3], wu_bar, drain_bar;
+    uint32_t tmem;
+    int abort;
+};
+
+// Byte offset of (rank m, channel c) in an M-major (MN-major) operand with K = DK:
+// core matrices of 8 channels (16-byte rows of 8 consecutive ranks), channel-
+// adjacent cores 128 B apart (descriptor leading byte offset 128), rank-adjacent
+// cores DK/8 * 128 B apart (stride byte offset).
+template <int DK>
+__device__ __forceinline__ uint32_t mn_off(int m, int c) {
+    return (uint32_t)((((m >> 3) * (DK >> 3) + (c >> 3)) << 7) + ((c & 7) << 4) + ((m & 7) << 1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                      pack_bf16(x[6], x[7]));
+}
+
+// Four values (ranks m .. m+3, m % 4 == 0) or eight (m % 8 == 0) of one channel.
+template <int DK>
+__device__ __forceinline__ void st4(uint8_t* base, int m, int c, float a, float b, float x, float y) {
+    *reinterpret_cast<uint2*>(base + mn_off<DK>(m, c)) = make_uint2(pack_bf16(a, b), pack_bf16(x, y));
+}
+template <int DK>
+__device__ __forceinline__ void st8(uint8_t* base, int m, int c, const float (&v)[8]) {
+    *reinterpret_cast<uint4*>(base + mn_off<DK>(m, c)) = pack8(v);
+}
+
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(float x) { return x; }
+
+// 8 elements from 16-byte words: one word of bf16, or two of fp32.
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4* w, float (&x)[8]);
+template <>
+__device__ __forceinline__ void unpack8<__nv_bfloat16>(const uint4* w, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+template <>
+__device__ __forceinline__ void unpack8<float>(const uint4* w, float (&x)[8]) {
+    const float* f = reinterpret_cast<const float*>(w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = f[i];
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma1688_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// C (16 x 8 tile at rows cr, cols cc of an N x N block, row stride ldc) = P Q over
+// K = N, P and Q read from fp32 shared memory (row strides ldp, ldq), tf32 inputs,
+// fp32 accumulation; sign -1 negates.  One warp.  LOWER_P / LOWER_Q: that operand
+// is lower triangular and its strict upper triangle, never written, reads as zero.
+template <int N, bool LOWER_P, bool LOWER_Q>
+__device__ __forceinline__ void tile_mm_tf32(const float* P, int ldp, const float* Q, int ldq,
+                                             float* C, int ldc, int cr, int cc, float sign,
+                                             int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    auto pv = [&](int r, int k) { return (LOWER_P && k > r) ? 0.f : P[r * ldp + k]; };
+    auto qv = [&](int k, int n) { return (LOWER_Q && n > k) ? 0.f : Q[k * ldq + n]; };
+#pragma unroll
+    for (int k0 = 0; k0 < N; k0 += 8) {
+        uint32_t a[4];
+        a[0] = to_tf32(pv(cr + gq, k0 + tq));
+        a[1] = to_tf32(pv(cr + gq + 8, k0 + tq));
+        a[2] = to_tf32(pv(cr + gq, k0 + tq + 4));
+        a[3] = to_tf32(pv(cr + gq + 8, k0 + tq + 4));
+        const uint32_t b0 = to_tf32(qv(k0 + tq, cc + gq));
+        const uint32_t b1 = to_tf32(qv(k0 + tq + 4, cc + gq));
+        mma1688_tf32(acc, a, b0, b1);
+    }
+    C[(cr + gq) * ldc + cc + 2 * tq] = sign * acc[0];
+    C[(cr + gq) * ldc + cc + 2 * tq + 1] = sign * acc[1];
+    C[(cr + gq + 8) * ldc + cc + 2 * tq] = sign * acc[2];
+    C[(cr + gq + 8) * ldc + cc + 2 * tq + 1] = sign * acc[3];
+}
+
+// Tensor-core join for n = 16, 32: one 16 x 8 tile of T = A21 X11, then of
+// X21 = -X22 T, per warp.  Ends with the CTA synchronised.
+template <int N>
+__device__ __forceinline__ void inv_join_tc(float* X, const float* A, float* T, int warp, int lane) {
+    constexpr int PAIRS = kChunk / (2 * N);
+    constexpr int TILES = (N / 16) * (N / 8);  // tiles per pair
+    for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
+        const int pidx = t / TILES, tt = t % TILES;
+        const int r1 = 2 * pidx * N, r2 = r1 + N;
+        const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
+        tile_mm_tf32<N, false, true>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T + pidx * N * N,
+                                     N, cr, cc, 1.f, lane);
+    }
+    __syncthreads();
+    for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
+        const int pidx = t / TILES, tt = t % TILES;
+        const int r1 = 2 * pidx * N, r2 = r1 + N;
+        const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
+        tile_mm_tf32<N, true, false>(X + r2 * AP + r2, AP, T + pidx * N * N, N, X + r2 * AP + r1, AP,
+                                     cr, cc, -1.f, lane);
+    }
+    __syncthreads();
+}
+
+// Joins pairs of inverted n x n diagonal blocks of X = (I + A)^-1 (row stride
+// kChunk + 1): X21 = -X22 (A21 X11).  The 8 x 8 diagonal blocks of X are written
+// whole (zeros above their diagonal), so the products run over full blocks.  Ends
+// with the CTA synchronised.
+template <int N>
+__device__ __forceinline__ void inv_join(float* X, const float* A, float* T, int tid) {
+    constexpr int OUT = (kChunk / (2 * N)) * N * N;
+    constexpr int PER = (OUT + kThreads - 1) / kThreads;
+#pragma unroll
+    for (int qq = 0; qq < PER; ++qq) {
+        const int e = tid + qq * kThreads;
+        if (e < OUT) {
+            const int pidx = e / (N * N), i = (e / N) % N, j = e % N;
+            const int r1 = 2 * pidx * N, r2 = r1 + N;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < N; m += 2) {
+                a0 = fmaf(A[(r2 + i) * AP + r1 + m], X[(r1 + m) * AP + r1 + j], a0);
+                a1 = fmaf(A[(r2 + i) * AP + r1 + m + 1], X[(r1 + m + 1) * AP + r1 + j], a1);
+            }
+            T[e] = a0 + a1;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int qq = 0; qq < PER; ++qq) {
+        const int e = tid + qq * kThreads;
+        if (e < OUT) {
+            const int pidx = e / (N * N), i = (e / N) % N, j = e % N;
+            const int r1 = 2 * pidx * N, r2 = r1 + N;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < N; m += 2) {
+                a0 = fmaf(X[(r2 + i) * AP + r2 + m], T[pidx * N * N + m * N + j], a0);
+                a1 = fmaf(X[(r2 + i) * AP + r2 + m + 1], T[pidx * N * N + (m + 1) * N + j], a1);
+            }
+            X[(r2 + i) * AP + r1 + j] = -(a0 + a1);
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void raise_timeout(uint8_t* ws, volatile int* abort) {
+    *abort = 1;
+    atomicOr(reinterpret_cast<unsigned int*>(ws), kDevErrTimeout);
+}
+
+// Issues the level-pair product D[tmem] = Aop Bop^T (M = 128, N = 64, K = DK, both
+// operands M/N-major bf16) from one operand buffer, then commits to `bar`.
+template <int DK>
+__device__ __forceinline__ void issue_level_pair(uint32_t tmem, const uint8_t* buf, uint64_t* bar) {
+    constexpr uint32_t id = ptx::idesc_bf16(128, 64) | kAMajorMN | kBMajorMN;
+    constexpr uint32_t sbo = (DK / 8) * 128;
+    const uint32_t a = ptx::smem_u32(buf), b = a + 128 * DK * 2;
+    const uint64_t ad = ptx::smem_desc(a, 128, sbo), bd = ptx::smem_desc(b, 128, sbo);
+#pragma unroll
+    for (int kk = 0; kk < DK / 16; ++kk)  // K = 16 per step: two 128-byte core columns
+        ptx::mma_bf16(tmem, ad + (uint64_t)((kk * 256) >> 4), bd + (uint64_t)((kk * 256) >> 4), id,
+                      kk > 0);
+    ptx::mma_commit(bar);
+}
+
+template <int DK, int DV, typename TIn, typename TG>
+__global__ void __launch_bounds__(kThreads, 1)
+    factor_kernel(Dims d, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                  const float* __restrict__ beta, uint8_t* __restrict__ ws) {
+    using Sm = FactorSmem<DK, DV, TIn>;
+    using Cf = FactorCfg<DK, DV, TIn>;
+    constexpr bool kBf16In = sizeof(TIn) == 2;
+    constexpr bool kBf16G = sizeof(TG) == 2;
+    constexpr int CPT = DK / 64;  // channels per thread in the level phase
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
+
+    const WsLayout W(d);
+    const Header* hdr = reinterpret_cast<const Header*>(ws + W.header);
+    const int4* chunk_tab = reinterpret_cast<const int4*>(ws + W.chunks);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = d.H;
+    const FactorLayout F(DK, DV);
+    volatile int* abort = &sm.abort;
+
+    if (tid == 0) {
+        ptx::mbar_init(&sm.ld_bar, 1);
+        ptx::mbar_init(&sm.v_bar, 1);
+        for (int i = 0; i < 3; ++i) ptx::mbar_init(&sm.lv_bar[i], 1);
+        ptx::mbar_init(&sm.wu_bar, 1);
+        ptx::mbar_init(&sm.drain_bar, 1);
+        sm.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&sm.tmem, 256);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+
+    // Persistent: items are (chunk, head) pairs over the schedule's chunks, item
+    // i = h * total + c, taken in steps of the grid size (32-bit, no division in the
+    // loop: the step is split once into whole heads and a chunk remainder).
+    const int total = hdr->total_chunks;
+    struct Item { int c, h; };
+    const int step_c = total > 0 ? (int)(gridDim.x % (unsigned)total) : 0;
+    const int step_h = total > 0 ? (int)(gridDim.x / (unsigned)total) : H;
+    auto advance = [&](Item a) {
+        a.c += step_c;
+        a.h += step_h;
+        if (a.c >= total) { a.c -= total; ++a.h; }
+        return a;
+    };
+    auto rows_of = [&](Item it) {  // {first token row, valid rows} (zeros past the last item)
+        if (it.h >= H) return make_int2(0, 0);
+        const int4 t = chunk_tab[it.c];
+        return make_int2(t.y, t.z);
+    };
+
+    // Tensor copies (one thread).  q, k, g complete on ld_bar; v on v_bar (bf16
+    // inputs: it is needed only by the last products, so it may arrive late), or
+    // with the others on ld_bar into the ring (fp32 inputs, converted in P1).
+    constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * sizeof(TG), VB = DV * sizeof(TIn);
+    uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.al) + (kBf16G ? kChunk * DK * 2 : 0);
+    // phases of ld_bar / v_bar issued and seen complete (thread 0), so that copies
+    // still in flight when the CTA leaves early can be waited for
+    uint32_t ld_issued = 0, ld_done = 0, v_issued = 0, v_done = 0;
+    auto issue_qkg = [&](Item it, int2 nk) {
+        ptx::mbar_arrive_expect_tx(&sm.ld_bar, (uint32_t)kChunk * (2 * QB + GB + (kBf16In ? 0 : VB)));
+        ptx::tma_load_3d(sm.qr, &tm_q, 0, it.h, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(sm.kr, &tm_k, 0, it.h, nk.x, &sm.ld_bar);
+        ptx::tma_load_3d(st_g, &tm_g, 0, it.h, nk.x, &sm.ld_bar);
+        if (!kBf16In) ptx::tma_load_3d(sm.ring, &tm_v, 0, it.h, nk.x, &sm.ld_bar);
+        ++ld_issued;
+    };
+    auto issue_v = [&](Item it, int2 nk) {  // bf16 inputs only
+        ptx::mbar_arrive_expect_tx(&sm.v_bar, (uint32_t)kChunk * DV * 2);
+        ptx::tma_load_4d(sm.vs, &tm_v, 0, nk.x, it.h, 0, &sm.v_bar);
+        ++v_issued;
+    };
+    float rb = 0.f;  // beta of this thread's row of the next item (threads < 64)
+    auto load_beta = [&](Item it, int2 nk) {
+        rb = (tid < kChunk && tid < nk.y) ? beta[(size_t)(nk.x + tid) * H + it.h] : 0.f;
+    };
+
+    Item item = total > 0 ? Item{(int)(blockIdx.x % (unsigned)total), (int)(blockIdx.x / (unsigned)total)}
+                          : Item{0, H};
+    int2 rows_cur = rows_of(item);
+    if (item.h < H) {
+        if (tid == 0) {
+            issue_qkg(item, rows_cur);
+            if (kBf16In) issue_v(item, rows_cur);
+        }
+        load_beta(item, rows_cur);
+    }
+    uint32_t par = 0;  // every per-item barrier completes once per item
+    while (item.h < H) {
+    const int c = item.c, h = item.h;
+    const Item next = advance(item), after = advance(next);
+    const int2 rows_next = rows_of(next), rows_after = rows_of(after);
+    uint8_t* const fb = ws + W.factors + ((size_t)c * H + h) * W.factor_bytes;
+    uint8_t* const gWQ = fb + F.wq;  // [w; QG], M-major, 128 x DK bf16
+    float* const gKT = reinterpret_cast<float*>(fb + F.kt);
+    __nv_bfloat16* const gP = reinterpret_cast<__nv_bfloat16*>(fb + F.p);
+    float* const gU = reinterpret_cast<float*>(fb + F.u0);
+    float* const gGL = reinterpret_cast<float*>(fb + F.gl);
+    const int L = rows_cur.y;
+
+    // ------------------------------------------------------------ P1: load
+    // inverse row norms of q and k, alpha = exp(g), beta; rows past the chunk end
+    // get zero norms (so qh = kh = 0 there), alpha = 1 and beta = 0
+    {
+        if (ptx::mbar_wait_or_abort(&sm.ld_bar, par, abort)) {
+            if (tid == 0) ++ld_done;
+        } else {
+            raise_timeout(ws, abort);
+        }
+        constexpr int CPR = DK / 8, RP = kThreads / CPR, NP = kChunk / RP;
+        constexpr int QW = (int)sizeof(TIn) / 2, GW = (int)sizeof(TG) / 2;
+        const int ck = tid % CPR, rsub = tid / CPR;
+        uint4 rg[NP][GW];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = rsub + p * RP;
+            const bool ok_r = r < L;
+            const uint4* wq = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.qr) + r * QB + ck * 8 * sizeof(TIn));
+            const uint4* wk = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.kr) + r * QB + ck * 8 * sizeof(TIn));
+            const uint4* wg = reinterpret_cast<const uint4*>(st_g + r * GB + ck * 8 * sizeof(TG));
+            uint4 rq[QW], rk[QW];
+#pragma unroll
+            for (int w2 = 0; w2 < QW; ++w2) {
+                rq[w2] = wq[w2];
+                rk[w2] = wk[w2];
+            }
+#pragma unroll
+            for (int w2 = 0; w2 < GW; ++w2) rg[p][w2] = wg[w2];
+            float xq[8], xk[8];
+            unpack8<TIn>(rq, xq);
+            unpack8<TIn>(rk, xk);
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sq = fmaf(xq[e], xq[e], sq);
+                sk = fmaf(xk[e], xk[e], sk);
+            }
+#pragma unroll
+            for (int o = 1; o < CPR; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            if (ck == 0) {
+                sm.iq[r] = ok_r ? rsqrtf(sq + 1e-6f) : 0.f;
+                sm.ik[r] = ok_r ? rsqrtf(sk + 1e-6f) : 0.f;
+            }
+        }
+        if (kBf16G) __syncthreads();  // raw bf16 g words are read before fp32 alpha overwrites them
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            const int r = rsub + p * RP;
+            float xg[8];
+            unpack8<TG>(rg[p], xg);
+            float* da = &sm.al[r * DK + ck * 8];
+            const bool ok_r = r < L;
+#pragma unroll
+            for (int e = 0; e < 8; e += 4)
+                *reinterpret_cast<float4*>(da + e) =
+                    ok_r ? make_float4(__expf(xg[e]), __expf(xg[e + 1]), __expf(xg[e + 2]), __expf(xg[e + 3]))
+                         : make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+        if (!kBf16In) {  // fp32 v (in the ring) -> the bf16 N-major operand, zero past the end
+            constexpr int VC = DV / 8;
+            for (int e = tid; e < kChunk * VC; e += kThreads) {
+                const int r = e / VC, cg = e % VC;
+                float xv[8];
+                unpack8<TIn>(reinterpret_cast<const uint4*>(sm.ring + r * VB + cg * 8 * sizeof(TIn)), xv);
+                if (r >= L) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) xv[u] = 0.f;
+                }
+                *reinterpret_cast<uint4*>(&sm.vs[(cg * kChunk + r) * 8]) = pack8(xv);
+            }
+        }
+        if (tid < kChunk) sm.bs[tid] = rb;
+    }
+    __syncthreads();
+
+    // Warm L2 with the inputs of the item after next, so that its tensor copies
+    // (issued during the next item) find them there.
+    if (tid == 64 && after.h < H) {
+        const int hy = after.h;
+        ptx::tma_prefetch_3d(&tm_q, 0, hy, rows_after.x);
+        ptx::tma_prefetch_3d(&tm_k, 0, hy, rows_after.x);
+        ptx::tma_prefetch_3d(&tm_g, 0, hy, rows_after.x);
+        if (kBf16In) ptx::tma_prefetch_4d(&tm_v, 0, rows_after.x, hy, 0);
+        else ptx::tma_prefetch_3d(&tm_v, 0, hy, rows_after.x);
+    }
+
+    // ------------------------------------------ P2: level operands, QG, KT, kh gamma
+    // Thread: 8-row block b = warp / 2 (rows 8b .. 8b+7) of CPT channels
+    // c_j = (warp % 2) * DK/2 + lane + 32 j; lanes hold consecutive channels, so every
+    // 16-byte operand row a warp writes is contiguous with its neighbours'.
+    {
+        const int b = warp >> 1, hf = warp & 1;
+        float a[CPT][8], kh[CPT][8], qh[CPT][8];
+        float dg[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dg[u] = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int cc = hf * (DK / 2) + lane + 32 * j;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int r = 8 * b + u;
+                a[j][u] = sm.al[r * DK + cc];
+                kh[j][u] = to_f(sm.kr[r * DK + cc]) * sm.ik[r];
+                qh[j][u] = to_f(sm.qr[r * DK + cc]) * sm.iq[r];
+                dg[u] = fmaf(qh[j][u], kh[j][u], dg[u]);
+            }
+            float t8 = a[j][1];
+#pragma unroll
+            for (int u = 2; u < 8; ++u) t8 *= a[j][u];
+            sm.blk_a[b * DK + cc] = a[j][0];
+            sm.blk_t[b * DK + cc] = t8;
+        }
+        // level pair 0: s = 1 (rows [kh R; qh R] at ranks 0-63, columns at 0-31) and
+        // s = 2 (ranks 64-127, columns 32-63); all factors are local to the block
+        uint8_t* const p0 = sm.ring;
+        uint8_t* const p0b = sm.ring + 128 * DK * 2;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int cc = hf * (DK / 2) + lane + 32 * j;
+            const float* x = a[j];
+            const float* k = kh[j];
+            const float* q = qh[j];
+            const int m = 4 * b;
+            // s = 1: rows 1, 3, 5, 7 (factor 1); columns 0, 2, 4, 6 (factor alpha of the next row)
+            st4<DK>(p0, m, cc, k[1], k[3], k[5], k[7]);
+            st4<DK>(p0, 32 + m, cc, q[1], q[3], q[5], q[7]);
+            st4<DK>(p0b, m, cc, k[0] * x[1], k[2] * x[3], k[4] * x[5], k[6] * x[7]);
+            // s = 2: rows 2, 3, 6, 7 (factors 1, a3, 1, a7); columns 0, 1, 4, 5 (to rows 2 / 6)
+            st4<DK>(p0, 64 + m, cc, k[2], k[3] * x[3], k[6], k[7] * x[7]);
+            st4<DK>(p0, 96 + m, cc, q[2], q[3] * x[3], q[6], q[7] * x[7]);
+            st4<DK>(p0b, 32 + m, cc, k[0] * (x[1] * x[2]), k[1] * x[2], k[4] * (x[5] * x[6]), k[5] * x[6]);
+        }
+        // qh . kh of the 8 rows: reduce over the warp's 32 channels (halving, 9
+        // shuffles); lane l ends with row (l >> 2) & 7
+        {
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+            float h4[4], h2[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float send = b4 ? dg[i] : dg[i + 4];
+                h4[i] = (b4 ? dg[i + 4] : dg[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float send = b3 ? h4[i] : h4[i + 2];
+                h2[i] = (b3 ? h4[i + 2] : h4[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+            const float send = b2 ? h2[0] : h2[1];
+            float h1 = (b2 ? h2[1] : h2[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+            h1 += __shfl_xor_sync(0xffffffffu, h1, 2);
+            h1 += __shfl_xor_sync(0xffffffffu, h1, 1);
+            if ((lane & 3) == 0) sm.diag[hf * kChunk + 8 * b + ((lane >> 2) & 7)] = h1;
+        }
+        ptx::fence_proxy_async_smem();  // operand writes (and the input reads) before async-proxy use
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+        if (tid == 0 && !*abort) {
+            issue_level_pair<DK>(tmem + 0, sm.ring, &sm.lv_bar[0]);
+            // q, k and g of this item are in registers now: the next item's copies may land
+            if (kBf16In && next.h < H) issue_qkg(next, rows_next);
+        }
+
+        // per-channel block scalars: ba = alpha at a block's first row, bt = alpha
+        // over its rows 1..7, e = ba bt = alpha over the whole block (register
+        // copies are indexed by constants only; the block's neighbours' values that
+        // depend on this warp's block come straight from shared memory)
+        auto load_blk = [&](int cc, float (&ba)[8], float (&bt)[8]) {
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb) {
+                ba[bb] = sm.blk_a[bb * DK + cc];
+                bt[bb] = sm.blk_t[bb * DK + cc];
+            }
+        };
+        // level pair 1: s = 4 (local) and s = 8 (odd blocks: prefix from the block
+        // start; even blocks: suffix up to the next block's first row)
+        uint8_t* const p1 = Cf::NBUF == 2 ? sm.ring + Cf::PAIR : sm.ring;
+        if (Cf::NBUF == 1) {
+            if (!ptx::mbar_wait_or_abort(&sm.lv_bar[0], par, abort)) raise_timeout(ws, abort);
+        }
+        uint8_t* const p1b = p1 + 128 * DK * 2;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int cc = hf * (DK / 2) + lane + 32 * j;
+            const float* x = a[j];
+            const float* k = kh[j];
+            const float* q = qh[j];
+            float ba[8], bt[8];
+            load_blk(cc, ba, bt);
+            const int m = 4 * b;
+            // s = 4: rows 4-7 (factors 1, a5, a5a6, a5a6a7), columns 0-3 (suffixes to row 4)
+            const float r5 = x[5], r6 = r5 * x[6], r7 = r6 * x[7];
+            st4<DK>(p1, m, cc, k[4], k[5] * r5, k[6] * r6, k[7] * r7);
+            st4<DK>(p1, 32 + m, cc, q[4], q[5] * r5, q[6] * r6, q[7] * r7);
+            const float c3 = x[4], c2 = x[3] * c3, c1 = x[2] * c2, c0 = x[1] * c1;
+            st4<DK>(p1b, m, cc, k[0] * c0, k[1] * c1, k[2] * c2, k[3] * c3);
+            // s = 8
+            float pre[8], suf[8];
+            pre[0] = 1.f;
+#pragma unroll
+            for (int u = 1; u < 8; ++u) pre[u] = pre[u - 1] * x[u];
+            suf[7] = 1.f;
+#pragma unroll
+            for (int u = 6; u >= 0; --u) suf[u] = suf[u + 1] * x[u + 1];
+            const int m8 = (b >> 1) * 8;
+            if (b & 1) {
+                float vk[8], vq[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    vk[u] = k[u] * pre[u];
+                    vq[u] = q[u] * pre[u];
+                }
+                st8<DK>(p1, 64 + m8, cc, vk);
+                st8<DK>(p1, 96 + m8, cc, vq);
+            } else {
+                const float an = sm.blk_a[(b + 1) * DK + cc];
+                float vc[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) vc[u] = k[u] * (suf[u] * an);
+                st8<DK>(p1b, 32 + m8, cc, vc);
+            }
+            // whole-chunk factors: gamma_r = (alpha over rows 0..r), gamma_L / gamma_r
+            // = (alpha over rows r+1..63)
+            float gin = 1.f, sout = 1.f;
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb) {
+                const float e = ba[bb] * bt[bb];
+                if (bb < b) gin *= e;
+                if (bb > b) sout *= e;
+            }
+            const float g0 = gin * x[0];
+            float vg[8], vk[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float gam = g0 * pre[u];
+                vg[u] = q[u] * gam;
+                vk[u] = k[u] * gam;
+            }
+            // QG: rows 64 + 8b .. of the [w; QG] tile (global, M-major)
+            *reinterpret_cast<uint4*>(gWQ + mn_off<DK>(kChunk + 8 * b, cc)) = pack8(vg);
+            // (kh gamma)^T for the w product: K-major operand, 8 chunk rows of channel cc
+            *reinterpret_cast<uint4*>(&sm.kg[op_index(cc, 8 * b, DK)]) = pack8(vk);
+            // KT (fp32, tf32 operand layout): kh * gamma_L / gamma
+            float kt[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kt[u] = k[u] * (suf[u] * sout);
+            *reinterpret_cast<float4*>(&gKT[op_index32(cc, 8 * b, DK)]) = make_float4(kt[0], kt[1], kt[2], kt[3]);
+            *reinterpret_cast<float4*>(&gKT[op_index32(cc, 8 * b + 4, DK)]) = make_float4(kt[4], kt[5], kt[6], kt[7]);
+            if (b == 7) gGL[cc] = g0 * pre[7];
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + 64, p1, &sm.lv_bar[1]);
+
+        // level pair 2: s = 16 and s = 32, into the buffer of pair 0 once its
+        // product has completed (with one buffer: once pair 1's has)
+        if (!ptx::mbar_wait_or_abort(&sm.lv_bar[Cf::NBUF == 2 ? 0 : 1], par, abort)) raise_timeout(ws, abort);
+        uint8_t* const p2 = sm.ring;
+        uint8_t* const p2b = sm.ring + 128 * DK * 2;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int cc = hf * (DK / 2) + lane + 32 * j;
+            const float* x = a[j];
+            const float* k = kh[j];
+            const float* q = qh[j];
+            float pre[8], suf[8];
+            pre[0] = 1.f;
+#pragma unroll
+            for (int u = 1; u < 8; ++u) pre[u] = pre[u - 1] * x[u];
+            suf[7] = 1.f;
+#pragma unroll
+            for (int u = 6; u >= 0; --u) suf[u] = suf[u + 1] * x[u + 1];
+            float ba[8], bt[8], e[8];
+            load_blk(cc, ba, bt);
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb) e[bb] = ba[bb] * bt[bb];
+            // s = 16: blocks 4p, 4p+1 are the lower half (columns), 4p+2, 4p+3 the upper
+            {
+                const int bq = b & 3;
+                const int m16 = (b >> 2) * 16 + (b & 1) * 8;
+                if (bq >= 2) {
+                    const float cr = bq == 2 ? 1.f : sm.blk_t[(b - 1) * DK + cc] * sm.blk_a[b * DK + cc];
+                    float vk[8], vq[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        vk[u] = k[u] * (cr * pre[u]);
+                        vq[u] = q[u] * (cr * pre[u]);
+                    }
+                    st8<DK>(p2, m16, cc, vk);
+                    st8<DK>(p2, 32 + m16, cc, vq);
+                } else {
+                    const float cl = bq == 1 ? sm.blk_a[(b + 1) * DK + cc]
+                                            : sm.blk_a[(b + 1) * DK + cc] * sm.blk_t[(b + 1) * DK + cc] *
+                                                  sm.blk_a[(b + 2) * DK + cc];
+                    float vc[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) vc[u] = k[u] * (suf[u] * cl);
+                    st8<DK>(p2b, m16, cc, vc);
+                }
+            }
+            // s = 32: blocks 0-3 are the lower half, 4-7 the upper
+            {
+                const int m32 = (b & 3) * 8;
+                if (b >= 4) {
+                    float cr = 1.f;
+                    if (b > 4) {
+                        cr = bt[4];
+#pragma unroll
+                        for (int bb = 5; bb < 8; ++bb)
+                            if (bb < b) cr *= e[bb];
+                        cr *= sm.blk_a[b * DK + cc];
+                    }
+                    float vk[8], vq[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        vk[u] = k[u] * (cr * pre[u]);
+                        vq[u] = q[u] * (cr * pre[u]);
+                    }
+                    st8<DK>(p2, 64 + m32, cc, vk);
+                    st8<DK>(p2, 96 + m32, cc, vq);
+                } else {
+                    float cl = ba[4];
+#pragma unroll
+                    for (int bb = 1; bb < 4; ++bb)
+                        if (bb > b) cl *= e[bb];
+                    float vc[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) vc[u] = k[u] * (suf[u] * cl);
+                    st8<DK>(p2b, 32 + m32, cc, vc);
+                }
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + 128, p2, &sm.lv_bar[2]);
+    }
+
+    // ------------------------------------------ P3: A and P out of tensor memory
+    // Warps 0-11: pair p = warp / 4 and lane quarter q = warp % 4: rows kh R (A) of
+    // level 2p + q/2 for even q, qh R (P) for odd q; 32 columns per level.  Warps
+    // 12-15: the diagonal of P and its zeros above the diagonal.
+    {
+        bool ok = ptx::mbar_wait_or_abort(&sm.lv_bar[1], par, abort);
+        ok = ptx::mbar_wait_or_abort(&sm.lv_bar[2], par, abort) && ok;
+        if (!ok) raise_timeout(ws, abort);
+        ptx::tc_fence_after();
+        float* const A = reinterpret_cast<float*>(sm.ring + kOffA);
+        if (warp < 12) {
+            const int p = warp >> 2, q = warp & 3;
+            const int lg = 2 * p + (q >> 1), s = 1 << lg;
+            float v0[16], v1[16];
+            const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + 64 * p + 32 * (q >> 1);
+            ptx::tmem_ld16(col, v0);
+            ptx::tmem_ld16(col + 16, v1);
+            ptx::tmem_ld_wait();
+            auto v = [&](int n) { return n < 16 ? v0[n] : v1[n - 16]; };
+            const int blk = lane >> lg;                      // the 2s-block of this row
+            const int i = (blk << (lg + 1)) + s + (lane & (s - 1));
+            if ((q & 1) == 0) {
+                const float bi = sm.bs[i];
+#pragma unroll
+                for (int n = 0; n < 32; ++n)
+                    if ((n >> lg) == blk) A[i * AP + (blk << (lg + 1)) + (n & (s - 1))] = bi * v(n);
+            } else {
+#pragma unroll
+                for (int n = 0; n < 32; ++n)
+                    if ((n >> lg) == blk) sm.pst[op_index(i, (blk << (lg + 1)) + (n & (s - 1)), kChunk)] = __float2bfloat16(v(n));
+            }
+        } else {
+            const int t = tid - 384, i = t & 63;
+            if (t < 64) {  // the diagonal and the zeros after it in its 8-column group
+                sm.pst[op_index(i, i, kChunk)] = __float2bfloat16(sm.diag[i] + sm.diag[kChunk + i]);
+                for (int j = i + 1; j < ((i >> 3) + 1) * 8; ++j) sm.pst[op_index(i, j, kChunk)] = __float2bfloat16(0.f);
+            } else {       // whole 8-column groups above the diagonal
+                for (int jb = (i >> 3) + 1; jb < 8; ++jb)
+                    *reinterpret_cast<uint4*>(&sm.pst[op_index(i, 8 * jb, kChunk)]) = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    // P leaves: 8 KB, 16 bytes per thread
+    reinterpret_cast<uint4*>(gP)[tid] = reinterpret_cast<const uint4*>(sm.pst)[tid];
+
+    // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
+    // 8 x 8 diagonal blocks by forward substitution (written whole, zeros above the
+    // diagonal), then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two inverted n x n
+    // blocks into one 2n x 2n block (n = 8 on CUDA cores, n = 16 and 32 with mma.sync
+    // on tf32 inputs and fp32 accumulation).  Entries of X above the diagonal outside
+    // the 8 x 8 blocks are never written; the joins read them as zero, and nothing
+    // else reads them.  Only entries of A strictly below the diagonal are read.
+    {
+        float* const A = reinterpret_cast<float*>(sm.ring + kOffA);
+        float* const X = reinterpret_cast<float*>(sm.ring + kOffX);
+        float* const T = reinterpret_cast<float*>(sm.ring + kOffScr);
+        if (tid < 64) {
+            const int base = 8 * (tid >> 3), jc = tid & 7;
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float acc = (i == jc) ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    if (m < i) acc -= A[(base + i) * AP + base + m] * x[m];
+                x[i] = (i < jc) ? 0.f : acc;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) X[(base + i) * AP + base + jc] = x[i];
+        }
+        __syncthreads();
+        inv_join<8>(X, A, T, tid);
+        inv_join_tc<16>(X, A, T, warp, lane);
+        inv_join_tc<32>(X, A, T, warp, lane);
+    }
+
+    // ------------------------------------- P6: X Diag(beta) as bf16 hi + lo operands
+    {
+        const float* X = reinterpret_cast<const float*>(sm.ring + kOffX);
+        __nv_bfloat16* xop = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXop);
+        __nv_bfloat16* xlo = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXlo);
+        const int i = tid >> 3, jb = (tid & 7) * 8;  // 64 rows x 8 groups = 512 tasks
+        float x[8], lo[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = jb + u;
+            x[u] = (j <= i) ? X[i * AP + j] * sm.bs[j] : 0.f;
+        }
+        const uint4 hi = pack8(x);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hi);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(h2[u]);
+            lo[2 * u] = x[2 * u] - f.x;
+            lo[2 * u + 1] = x[2 * u + 1] - f.y;
+        }
+        *reinterpret_cast<uint4*>(&xop[op_index(i, jb, kChunk)]) = hi;
+        *reinterpret_cast<uint4*>(&xlo[op_index(i, jb, kChunk)]) = pack8(lo);
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    // ------------------------------------------------- P7: u and w^T on tcgen05
+    if (tid == 0) {
+        bool okv = true;
+        if (kBf16In) {
+            okv = ptx::mbar_wait_or_abort(&sm.v_bar, par, abort);
+            if (okv) ++v_done;
+            else raise_timeout(ws, abort);
+        }
+        ptx::tc_fence_after();
+        if (okv && !*abort) {
+            const uint32_t xa[2] = {ptx::smem_u32(sm.ring + kOffXop), ptx::smem_u32(sm.ring + kOffXlo)};
+            const uint32_t va = ptx::smem_u32(sm.vs), ka = ptx::smem_u32(sm.kg);
+            constexpr uint32_t id_u = ptx::idesc_bf16(kChunk, DV) | kBMajorMN;
+            constexpr uint32_t id_w = ptx::idesc_bf16(DK, kChunk);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)  // u = (X Diag(beta)) v: columns 64 ..
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk)
+                    ptx::mma_bf16(tmem + 64, ptx::smem_desc(xa[part] + kk * 2048, 1024, 128),
+                                  ptx::smem_desc(va + kk * 256, 128, 1024), id_u, part > 0 || kk > 0);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)  // w^T = (kh gamma)^T (X Diag(beta))^T: columns 0-63
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk)
+                    ptx::mma_bf16(tmem + 0, ptx::smem_desc(ka + kk * 2 * (DK / 8) * 128, (DK / 8) * 128, 128),
+                                  ptx::smem_desc(xa[part] + kk * 2048, 1024, 128), id_w, part > 0 || kk > 0);
+        }
+        ptx::mma_commit(&sm.wu_bar);  // (also when nothing was issued: the phase still completes)
+    }
+    if (next.h < H) load_beta(next, rows_next);
+    if (!ptx::mbar_wait_or_abort(&sm.wu_bar, par, abort)) raise_timeout(ws, abort);
+    ptx::tc_fence_after();
+    if (tid == 0 && next.h < H && !*abort) {  // v (and, for fp32 inputs, everything) of the next item
+        if (kBf16In) issue_v(next, rows_next);
+        else issue_qkg(next, rows_next);
+    }
+    {
+        const int q = warp & 3, cg = warp >> 2;
+        // w^T: lane = channel (dk = 64: lanes 0-15 of each quarter), columns = chunk rows
+        {
+            float x[16];
+            ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * cg, x);
+            ptx::tmem_ld_wait();
+            const int cc = DK == 128 ? 32 * q + lane : 16 * q + lane;
+            if (DK == 128 || lane < 16) {
+                float y0[8], y1[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    y0[u] = x[u];
+                    y1[u] = x[8 + u];
+                }
+                *reinterpret_cast<uint4*>(gWQ + mn_off<DK>(16 * cg, cc)) = pack8(y0);
+                *reinterpret_cast<uint4*>(gWQ + mn_off<DK>(16 * cg + 8, cc)) = pack8(y1);
+            }
+        }
+        // u: lanes 0-15 of each quarter = chunk rows 16 q .., columns DV/4 per warp
+        {
+            constexpr int NC = DV / 4;
+            const int row = 16 * q + lane;
+#pragma unroll
+            for (int i = 0; i < NC / 16; ++i) {
+                float x[16];
+                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 + cg * NC + 16 * i, x);
+                ptx::tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const int n = cg * NC + 16 * i + 4 * u4;
+                        *reinterpret_cast<float4*>(&gU[u0_index(row, n)]) =
+                            make_float4(x[4 * u4], x[4 * u4 + 1], x[4 * u4 + 2], x[4 * u4 + 3]);
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*abort) break;
+    par ^= 1u;
+    item = next;
+    rows_cur = rows_next;
+    }  // items
+
+    // Leave cleanly: copies still in flight land, issued MMAs complete, then TMEM goes.
+    if (tid == 0) {
+        volatile int never = 0;
+        for (uint32_t k2 = ld_done; k2 < ld_issued; ++k2) ptx::mbar_wait_or_abort(&sm.ld_bar, k2 & 1u, &never);
+        for (uint32_t k2 = v_done; k2 < v_issued; ++k2) ptx::mbar_wait_or_abort(&sm.v_bar, k2 & 1u, &never);
+        ptx::mma_commit(&sm.drain_bar);
+        ptx::mbar_wait_or_abort(&sm.drain_bar, 0, &never);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 256);
+    }
+}
+
+// The driver's tensor-map encoder, fetched once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// Tensor map of a [tokens, H, D] row-major tensor with a box of 64 tokens x 1 head
+// x D channels (one copy brings one chunk of one head, rows in order).
+bool encode_rows(CUtensorMap* m, const void* base, bool f32, int D, int H, long long tokens) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {D * es, (cuuint64_t)H * D * es};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kChunk};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of a bf16 [tokens, H, D] tensor seen as {8 channels, tokens, H, D/8
+// channel groups} (strides: a token row, a head, 16 bytes), with a box of 8 x 64
+// tokens x 1 x D/8: one copy lands a chunk of one head as [D/8][64 rows][8], the
+// N-major core-matrix layout of a tensor-core operand.
+bool encode_groups(CUtensorMap* m, const void* base, int D, int H, long long tokens) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {8, (cuuint64_t)tokens, (cuuint64_t)H, (cuuint64_t)(D / 8)};
+    const cuuint64_t strides[3] = {(cuuint64_t)H * D * 2, (cuuint64_t)D * 2, 16};
+    const cuuint32_t box[4] = {8, (cuuint32_t)kChunk, 1, (cuuint32_t)(D / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DK, int DV, typename TIn, typename TG>
+cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v, const void* g,
+                     const float* beta, uint8_t* ws, cudaStream_t stream) {
+    using Sm = FactorSmem<DK, DV, TIn>;
+    static_assert(sizeof(Sm) <= 227 * 1024, "factor kernel shared memory");
+    static_assert(offsetof(Sm, qr) % 128 == 0 && offsetof(Sm, kr) % 128 == 0 &&
+                      offsetof(Sm, al) % 128 == 0 && offsetof(Sm, vs) % 128 == 0 &&
+                      offsetof(Sm, kg) % 128 == 0,
+                  "tensor-copy and operand destinations are 128-byte aligned");
+    auto kern = factor_kernel<DK, DV, TIn, TG>;
+    const size_t smem = sizeof(Sm);
+    const WsLayout W(d);
+    const long long tokens = (long long)d.B * d.T;
+    if (W.cmax == 0 || tokens == 0) return cudaSuccess;  // no chunk has a token
+    cudaError_t e = ensure_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    constexpr bool f32 = sizeof(TIn) == 4;
+    CUtensorMap tq, tk, tv, tg;
+    const bool okv = f32 ? encode_rows(&tv, v, true, DV, d.H, tokens) : encode_groups(&tv, v, DV, d.H, tokens);
+    if (!encode_rows(&tq, q, f32, DK, d.H, tokens) || !encode_rows(&tk, k, f32, DK, d.H, tokens) || !okv ||
+        !encode_rows(&tg, g, sizeof(TG) == 4, DK, d.H, tokens))
+        return cudaErrorInvalidValue;
+    const long long items = W.cmax * d.H;
+    const unsigned grid = (unsigned)(items < num_sms() ? items : num_sms());  // persistent
+    kern<<<grid, kThreads, smem, stream>>>(d, tq, tk, tv, tg, beta, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,
+                           const void* v, const void* g, const float* beta, uint8_t* ws,
+                           cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+#define KDA_FACTOR_CASE(DK_, DV_)                                                                 \
+    if (d.dk == DK_ && d.dv == DV_) {                                                             \
+        if (!qkv_bf16) return g_bf16 ? cudaErrorInvalidValue                                      \
+                                     : launch_t<DK_, DV_, float, float>(d, q, k, v, g, beta, ws, stream); \
+        return g_bf16 ? launch_t<DK_, DV_, bf, bf>(d, q, k, v, g, beta, ws, stream)                \
+                      : launch_t<DK_, DV_, bf, float>(d, q, k, v, g, beta, ws, stream);            \
+    }
+    KDA_FACTOR_CASE(64, 64)
+    KDA_FACTOR_CASE(64, 128)
+    KDA_FACTOR_CASE(128, 64)
+    KDA_FACTOR_CASE(128, 128)
+#undef KDA_FACTOR_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

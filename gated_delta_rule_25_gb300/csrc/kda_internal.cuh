@@ -8,10 +8,9 @@
 //   factors         per (chunk, head): the factors of the chunkwise form
 //
 // Per (chunk, head) factor block, every part a multiple of 256 bytes:
-//   WQ  [128 x dk] bf16, row-block-major operand layout: rows 0-63
+//   WQ  [128 x dk] bf16, M-major operand layout: rows 0-63
 //                                       w = (I + A)^-1 Diag(beta) (kh * exp(Gamma)), rows
-//                                       64-127 qh * exp(Gamma) (one M = 128 operand whose
-//                                       halves are contiguous 64 x dk blocks)
+//                                       64-127 qh * exp(Gamma) (one M = 128 operand)
 //   KT  [dk x 64] fp32, tf32 operand layout  (kh * exp(Gamma_last - Gamma))^T
 //   P   [64 x 64] bf16, operand layout  sum_c qh_ic kh_jc exp(Gamma_ic - Gamma_jc), j <= i
 //   U0  [dv/32][8][64][4] fp32          u = (I + A)^-1 Diag(beta) v, in 32-column
@@ -26,6 +25,10 @@
 // * 128.  A bulk copy of the block lands in shared memory ready for tcgen05.mma,
 // with descriptor leading byte offset (between core matrices adjacent in K) = R/8 *
 // 128 and stride byte offset (between core matrices adjacent in rows) = 128.
+// "M-major operand layout" (WQ): core matrices of 8 K-columns x 16 contiguous bytes
+// (8 bf16 elements of M), core matrix (row block mb, k block kb) at byte ((mb *
+// dk/8) + kb) * 128; descriptor leading byte offset (K-adjacent) 128, stride byte
+// offset (M-adjacent) dk/8 * 128, and the instruction's A-major bit set.
 #pragma once
 
 #include <cstddef>
@@ -98,13 +101,6 @@ struct WsLayout {
 // Element index of (r, k) in an R x K bf16 tile stored in the operand layout.
 __host__ __device__ inline int op_index(int r, int k, int R) {
     return (((k >> 3) * (R >> 3) + (r >> 3)) << 6) + ((r & 7) << 3) + (k & 7);
-}
-
-// Element index of (r, k) in an R x K bf16 tile in the row-block-major operand
-// layout: the same core matrices, K-adjacent ones contiguous (descriptor leading
-// byte offset 128, stride byte offset K/8 * 128), so each 8-row block is one run.
-__host__ __device__ inline int op_index_rm(int r, int k, int K) {
-    return (((r >> 3) * (K >> 3) + (k >> 3)) << 6) + ((r & 7) << 3) + (k & 7);
 }
 
 // Element index of (r, k) in an R x K fp32 (tf32 operand) tile in the operand layout.

@@ -103,6 +103,22 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1
                  : "memory");
 }
 
+// The same for a 4-D tensor map (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst_smem)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // Shared -> global bulk copy (both addresses 16-byte aligned, bytes a multiple of
 // 16), tracked in this thread's bulk group; commit, then wait for the group's
 // shared-memory reads (.read) or for its completion.
