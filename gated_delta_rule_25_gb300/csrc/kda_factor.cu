@@ -53,7 +53,8 @@ constexpr int AP = kChunk + 1;            // row stride of the fp32 A and X arra
 constexpr int kOffA = 0;                              // A (fp32, 64 x 65)
 constexpr int kOffX = kChunk * AP * 4;                // X (fp32, 64 x 65)
 constexpr int kOffScr = 2 * kChunk * AP * 4;          // inverse scratch (32 x 32 fp32)
-constexpr int kInvBytes = kOffScr + 32 * 32 * 4;
+constexpr int kOffPst = kOffScr + 32 * 32 * 4;        // P staging (fp32, 64 x 65)
+constexpr int kInvBytes = kOffPst + kChunk * AP * 4;
 constexpr int kOffXop = 0;                            // X Diag(beta), bf16 hi (over A)
 constexpr int kOffXlo = kChunk * kChunk * 2;          // and its remainder lo
 
@@ -76,7 +77,6 @@ struct __align__(1024) FactorSmem {
     float al[kChunk * DK];               // alpha = exp(g) (g is copied in here)
     __nv_bfloat16 vs[kChunk * DV];       // v, N-major operand: [DV/8][64 rows][8 columns]
     __nv_bfloat16 kg[DK * kChunk];       // (kh * gamma)^T, K-major operand (DK x 64)
-    __nv_bfloat16 pst[kChunk * kChunk];  // P staged in its operand layout
     float blk_a[8 * DK];                 // alpha at the first row of each 8-row block
     float blk_t[8 * DK];                 // product of alpha over rows 1..7 of each block
     float diag[2 * kChunk];              // qh_i . kh_i, one partial sum per channel half
@@ -723,14 +723,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------ P3: A and P out of tensor memory
     // Warps 0-11: pair p = warp / 4 and lane quarter q = warp % 4: rows kh R (A) of
-    // level 2p + q/2 for even q, qh R (P) for odd q; 32 columns per level.  Warps
-    // 12-15: the diagonal of P and its zeros above the diagonal.
+    // level 2p + q/2 for even q, qh R (P) for odd q; 32 columns per level.  Lane r
+    // holds row i of its level; its columns n in the same 2s-block are j = n + blk s.
+    // A and P land row-major in fp32 (row stride 65: the lanes' rows hit distinct
+    // banks).
     {
         bool ok = ptx::mbar_wait_or_abort(&sm.lv_bar[1], par, abort);
         ok = ptx::mbar_wait_or_abort(&sm.lv_bar[2], par, abort) && ok;
         if (!ok) raise_timeout(ws, abort);
         ptx::tc_fence_after();
         float* const A = reinterpret_cast<float*>(sm.ring + kOffA);
+        float* const Pst = reinterpret_cast<float*>(sm.ring + kOffPst);
         if (warp < 12) {
             const int p = warp >> 2, q = warp & 3;
             const int lg = 2 * p + (q >> 1), s = 1 << lg;
@@ -742,31 +745,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto v = [&](int n) { return n < 16 ? v0[n] : v1[n - 16]; };
             const int blk = lane >> lg;                      // the 2s-block of this row
             const int i = (blk << (lg + 1)) + s + (lane & (s - 1));
-            if ((q & 1) == 0) {
-                const float bi = sm.bs[i];
+            float* const row = ((q & 1) == 0 ? A : Pst) + i * AP + (blk << lg);  // + n = column j
+            const float sc = (q & 1) == 0 ? sm.bs[i] : 1.f;
 #pragma unroll
-                for (int n = 0; n < 32; ++n)
-                    if ((n >> lg) == blk) A[i * AP + (blk << (lg + 1)) + (n & (s - 1))] = bi * v(n);
-            } else {
-#pragma unroll
-                for (int n = 0; n < 32; ++n)
-                    if ((n >> lg) == blk) sm.pst[op_index(i, (blk << (lg + 1)) + (n & (s - 1)), kChunk)] = __float2bfloat16(v(n));
-            }
-        } else {
-            const int t = tid - 384, i = t & 63;
-            if (t < 64) {  // the diagonal and the zeros after it in its 8-column group
-                sm.pst[op_index(i, i, kChunk)] = __float2bfloat16(sm.diag[i] + sm.diag[kChunk + i]);
-                for (int j = i + 1; j < ((i >> 3) + 1) * 8; ++j) sm.pst[op_index(i, j, kChunk)] = __float2bfloat16(0.f);
-            } else {       // whole 8-column groups above the diagonal
-                for (int jb = (i >> 3) + 1; jb < 8; ++jb)
-                    *reinterpret_cast<uint4*>(&sm.pst[op_index(i, 8 * jb, kChunk)]) = make_uint4(0, 0, 0, 0);
-            }
+            for (int n = 0; n < 32; ++n)
+                if ((n >> lg) == blk) row[n] = sc * v(n);
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // P leaves: 8 KB, 16 bytes per thread
-    reinterpret_cast<uint4*>(gP)[tid] = reinterpret_cast<const uint4*>(sm.pst)[tid];
+    // P leaves in its operand layout, 16 bytes per thread: row i, columns 8 jb ..;
+    // the diagonal (qh_i . kh_i) and the zeros above it are filled in here
+    {
+        const float* Pst = reinterpret_cast<const float*>(sm.ring + kOffPst);
+        const int i = tid >> 3, jb = tid & 7;
+        const float dv = sm.diag[i] + sm.diag[kChunk + i];
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = 8 * jb + u;
+            x[u] = j < i ? Pst[i * AP + j] : (j == i ? dv : 0.f);
+        }
+        *reinterpret_cast<uint4*>(&gP[op_index(i, 8 * jb, kChunk)]) = pack8(x);
+    }
 
     // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
     // 8 x 8 diagonal blocks by forward substitution (written whole, zeros above the
@@ -804,7 +805,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* X = reinterpret_cast<const float*>(sm.ring + kOffX);
         __nv_bfloat16* xop = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXop);
         __nv_bfloat16* xlo = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXlo);
-        const int i = tid >> 3, jb = (tid & 7) * 8;  // 64 rows x 8 groups = 512 tasks
+        // 64 rows x 8 groups: a warp takes 32 consecutive rows of one group, so its
+        // X reads (row stride 65) and operand stores (rows of a group are adjacent
+        // 16-byte core rows) are free of bank conflicts
+        const int i = tid & 63, jb = (tid >> 6) * 8;
         float x[8], lo[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -837,22 +841,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         if (okv && !*abort) {
-            const uint32_t xa[2] = {ptx::smem_u32(sm.ring + kOffXop), ptx::smem_u32(sm.ring + kOffXlo)};
             const uint32_t va = ptx::smem_u32(sm.vs), ka = ptx::smem_u32(sm.kg);
             constexpr uint32_t id_u = ptx::idesc_bf16(kChunk, DV) | kBMajorMN;
             constexpr uint32_t id_w = ptx::idesc_bf16(DK, kChunk);
+            const uint64_t xd[2] = {ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXop), 1024, 128),
+                                    ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXlo), 1024, 128)};
+            const uint64_t vb = ptx::smem_desc(va, 128, 1024);
+            const uint64_t kd = ptx::smem_desc(ka, (DK / 8) * 128, 128);
+            constexpr uint64_t kstep = (uint64_t)((2 * (DK / 8) * 128) >> 4);
 #pragma unroll
             for (int part = 0; part < 2; ++part)  // u = (X Diag(beta)) v: columns 64 ..
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16(tmem + 64, ptx::smem_desc(xa[part] + kk * 2048, 1024, 128),
-                                  ptx::smem_desc(va + kk * 256, 128, 1024), id_u, part > 0 || kk > 0);
+                    ptx::mma_bf16(tmem + 64, xd[part] + (uint64_t)(kk * 128), vb + (uint64_t)(kk * 16), id_u,
+                                  part > 0 || kk > 0);
 #pragma unroll
             for (int part = 0; part < 2; ++part)  // w^T = (kh gamma)^T (X Diag(beta))^T: columns 0-63
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16(tmem + 0, ptx::smem_desc(ka + kk * 2 * (DK / 8) * 128, (DK / 8) * 128, 128),
-                                  ptx::smem_desc(xa[part] + kk * 2048, 1024, 128), id_w, part > 0 || kk > 0);
+                    ptx::mma_bf16(tmem + 0, kd + kk * kstep, xd[part] + (uint64_t)(kk * 128), id_w,
+                                  part > 0 || kk > 0);
         }
         ptx::mma_commit(&sm.wu_bar);  // (also when nothing was issued: the phase still completes)
     }
