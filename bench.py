@@ -60,9 +60,10 @@ def make_workload(name: str, seed: int, salt: int):
     if name.startswith("cfg5-"):
         _, kind, hs, total = name.split("-")
         H_, total_ = int(hs[1:]), int(total)
-        x = gen.make_cfg5(H_, total_, kind == "varlen", seed=seed, salt=salt)
+        x = gen.make_cfg5(H_, total_, kind == "varlen", seed=seed, salt=salt, drawn_heads=2)
         desc = (f"throughput sweep: {kind} {total_} tokens, H={H_}, dk=dv=128, bf16 "
-                f"({'B=' + str(total_ // 8192) + ' x 8192' if kind == 'fixed' else str(x.num_seqs) + ' sequences'})")
+                f"({'B=' + str(total_ // 8192) + ' x 8192' if kind == 'fixed' else str(x.num_seqs) + ' sequences'}; "
+                "heads 0-1 drawn from the recipe, the others token-rolled copies of them)")
         return x, desc
     raise ValueError(f"unknown workload {name}")
 

@@ -40,3 +40,19 @@ def test_cfg2_gate_range():
     a = np.exp(x.g.numpy())
     assert a.min() >= 1e-4 * (1 - 1e-6) and a.max() < 1.0
     assert x.q.dtype == torch.bfloat16 and x.g.dtype == torch.float32
+
+
+def test_cfg5_filled_heads_are_distinct_rolls_of_drawn_ones():
+    x = gen.make_cfg5(5, 8192, False, seed=1, salt=2, drawn_heads=2)
+    y = gen.make_cfg5(2, 8192, False, seed=1, salt=2)  # the same draws, two heads
+    assert torch.equal(x.q[:, :, :2], y.q) and torch.equal(x.g[:, :, :2], y.g)
+    for h in range(2, 5):
+        shift = 37 * (h // 2)
+        assert torch.equal(x.q[:, :, h], torch.roll(x.q[:, :, h % 2], shift, dims=1))
+        assert torch.equal(x.beta[:, :, h], torch.roll(x.beta[:, :, h % 2], shift, dims=1))
+        assert torch.equal(x.h0[:, h], torch.roll(x.h0[:, h % 2], shift, dims=1))
+    for a in range(5):
+        for b in range(a):
+            assert not torch.equal(x.k[:, :, a], x.k[:, :, b])
+    z = gen.make_cfg5(3, 8192, True, seed=1, salt=2, drawn_heads=2)
+    assert z.cu_seqlens is not None and z.q.shape == (1, 8192, 3, 128)
