@@ -74,7 +74,7 @@ struct __align__(1024) FactorSmem {
     uint8_t ring[C::RING];               // level operands, then A, X, X Diag(beta) hi/lo
     TIn qr[kChunk * DK];                 // raw q rows as copied in; qh = qr * iq[row]
     TIn kr[kChunk * DK];                 // raw k rows; kh = kr * ik[row]
-    float al[kChunk * DK];               // alpha = exp(g) (g is copied in here)
+    float gr[kChunk * DK];               // raw g rows as copied in (fp32, or bf16 in the first half)
     __nv_bfloat16 vs[kChunk * DV];       // v, N-major operand: [DV/8][64 rows][8 columns]
     __nv_bfloat16 kg[DK * kChunk];       // (kh * gamma)^T, K-major operand (DK x 64)
     float blk_a[8 * DK];                 // alpha at the first row of each 8-row block
@@ -277,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Sm = FactorSmem<DK, DV, TIn>;
     using Cf = FactorCfg<DK, DV, TIn>;
     constexpr bool kBf16In = sizeof(TIn) == 2;
-    constexpr bool kBf16G = sizeof(TG) == 2;
     constexpr int CPT = DK / 64;  // channels per thread in the level phase
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
@@ -300,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
-        ptx::tmem_alloc(&sm.tmem, 256);
+        ptx::tmem_alloc(&sm.tmem, 512);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -331,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // inputs: it is needed only by the last products, so it may arrive late), or
     // with the others on ld_bar into the ring (fp32 inputs, converted in P1).
     constexpr uint32_t QB = DK * sizeof(TIn), GB = DK * sizeof(TG), VB = DV * sizeof(TIn);
-    uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.al) + (kBf16G ? kChunk * DK * 2 : 0);
+    uint8_t* const st_g = reinterpret_cast<uint8_t*>(sm.gr);
     // phases of ld_bar / v_bar issued and seen complete (thread 0), so that copies
     // still in flight when the CTA leaves early can be waited for
     uint32_t ld_issued = 0, ld_done = 0, v_issued = 0, v_done = 0;
@@ -364,7 +363,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_beta(item, rows_cur);
     }
     uint32_t par = 0;  // every per-item barrier completes once per item
+    // Tensor memory: item n works in columns [256 (n % 2), + 192) (level products,
+    // then u and w^T), so that its u and w^T can wait there while item n + 1 runs;
+    // they leave during item n + 1's last products (or after the last item).
+    auto epilogue = [&](uint32_t reg, uint8_t* wq_dst, float* u_dst) {
+        const int q = warp & 3, cg = warp >> 2;
+        // w^T: lane = channel (dk = 64: lanes 0-15 of each quarter), columns = chunk rows
+        {
+            float x[16];
+            ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + reg + 16 * cg, x);
+            ptx::tmem_ld_wait();
+            const int cc = DK == 128 ? 32 * q + lane : 16 * q + lane;
+            if (DK == 128 || lane < 16) {
+                float y0[8], y1[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    y0[u] = x[u];
+                    y1[u] = x[8 + u];
+                }
+                *reinterpret_cast<uint4*>(wq_dst + mn_off<DK>(16 * cg, cc)) = pack8(y0);
+                *reinterpret_cast<uint4*>(wq_dst + mn_off<DK>(16 * cg + 8, cc)) = pack8(y1);
+            }
+        }
+        // u: lanes 0-15 of each quarter = chunk rows 16 q .., columns DV/4 per warp
+        {
+            constexpr int NC = DV / 4;
+            const int row = 16 * q + lane;
+#pragma unroll
+            for (int i = 0; i < NC / 16; ++i) {
+                float x[16];
+                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + reg + 64 + cg * NC + 16 * i, x);
+                ptx::tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const int n = cg * NC + 16 * i + 4 * u4;
+                        *reinterpret_cast<float4*>(&u_dst[u0_index(row, n)]) =
+                            make_float4(x[4 * u4], x[4 * u4 + 1], x[4 * u4 + 2], x[4 * u4 + 3]);
+                    }
+                }
+            }
+        }
+    };
+    bool have_prev = false;
+    uint32_t prev_reg = 0;
+    uint8_t* prev_wq = nullptr;
+    float* prev_u = nullptr;
     while (item.h < H) {
+    const uint32_t reg = par ? 256u : 0u;
     const int c = item.c, h = item.h;
     const Item next = advance(item), after = advance(next);
     const int2 rows_next = rows_of(next), rows_after = rows_of(after);
@@ -377,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = rows_cur.y;
 
     // ------------------------------------------------------------ P1: load
-    // inverse row norms of q and k, alpha = exp(g), beta; rows past the chunk end
-    // get zero norms (so qh = kh = 0 there), alpha = 1 and beta = 0
+    // inverse row norms of q and k, and beta; rows past the chunk end get zero norms
+    // (so qh = kh = 0 there) and beta = 0
     {
         if (ptx::mbar_wait_or_abort(&sm.ld_bar, par, abort)) {
             if (tid == 0) ++ld_done;
@@ -386,24 +432,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             raise_timeout(ws, abort);
         }
         constexpr int CPR = DK / 8, RP = kThreads / CPR, NP = kChunk / RP;
-        constexpr int QW = (int)sizeof(TIn) / 2, GW = (int)sizeof(TG) / 2;
+        constexpr int QW = (int)sizeof(TIn) / 2;
         const int ck = tid % CPR, rsub = tid / CPR;
-        uint4 rg[NP][GW];
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int r = rsub + p * RP;
             const bool ok_r = r < L;
             const uint4* wq = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.qr) + r * QB + ck * 8 * sizeof(TIn));
             const uint4* wk = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.kr) + r * QB + ck * 8 * sizeof(TIn));
-            const uint4* wg = reinterpret_cast<const uint4*>(st_g + r * GB + ck * 8 * sizeof(TG));
             uint4 rq[QW], rk[QW];
 #pragma unroll
             for (int w2 = 0; w2 < QW; ++w2) {
                 rq[w2] = wq[w2];
                 rk[w2] = wk[w2];
             }
-#pragma unroll
-            for (int w2 = 0; w2 < GW; ++w2) rg[p][w2] = wg[w2];
             float xq[8], xk[8];
             unpack8<TIn>(rq, xq);
             unpack8<TIn>(rk, xk);
@@ -422,20 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm.iq[r] = ok_r ? rsqrtf(sq + 1e-6f) : 0.f;
                 sm.ik[r] = ok_r ? rsqrtf(sk + 1e-6f) : 0.f;
             }
-        }
-        if (kBf16G) __syncthreads();  // raw bf16 g words are read before fp32 alpha overwrites them
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            const int r = rsub + p * RP;
-            float xg[8];
-            unpack8<TG>(rg[p], xg);
-            float* da = &sm.al[r * DK + ck * 8];
-            const bool ok_r = r < L;
-#pragma unroll
-            for (int e = 0; e < 8; e += 4)
-                *reinterpret_cast<float4*>(da + e) =
-                    ok_r ? make_float4(__expf(xg[e]), __expf(xg[e + 1]), __expf(xg[e + 2]), __expf(xg[e + 3]))
-                         : make_float4(1.f, 1.f, 1.f, 1.f);
         }
         if (!kBf16In) {  // fp32 v (in the ring) -> the bf16 N-major operand, zero past the end
             constexpr int VC = DV / 8;
@@ -481,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int r = 8 * b + u;
-                a[j][u] = sm.al[r * DK + cc];
+                a[j][u] = r < L ? __expf(to_f(reinterpret_cast<const TG*>(sm.gr)[r * DK + cc])) : 1.f;
                 kh[j][u] = to_f(sm.kr[r * DK + cc]) * sm.ik[r];
                 qh[j][u] = to_f(sm.qr[r * DK + cc]) * sm.iq[r];
                 dg[u] = fmaf(qh[j][u], kh[j][u], dg[u]);
@@ -538,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         ptx::tc_fence_after();
         if (tid == 0 && !*abort) {
-            issue_level_pair<DK>(tmem + 0, sm.ring, &sm.lv_bar[0]);
+            issue_level_pair<DK>(tmem + reg + 0, sm.ring, &sm.lv_bar[0]);
             // q, k and g of this item are in registers now: the next item's copies may land
             if (kBf16In && next.h < H) issue_qkg(next, rows_next);
         }
@@ -634,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
-        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + 64, p1, &sm.lv_bar[1]);
+        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + reg + 64, p1, &sm.lv_bar[1]);
 
         // level pair 2: s = 16 and s = 32, into the buffer of pair 0 once its
         // product has completed (with one buffer: once pair 1's has)
@@ -718,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
-        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + 128, p2, &sm.lv_bar[2]);
+        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + reg + 128, p2, &sm.lv_bar[2]);
     }
 
     // ------------------------------------------ P3: A and P out of tensor memory
@@ -738,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p = warp >> 2, q = warp & 3;
             const int lg = 2 * p + (q >> 1), s = 1 << lg;
             float v0[16], v1[16];
-            const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + 64 * p + 32 * (q >> 1);
+            const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + reg + 64 * p + 32 * (q >> 1);
             ptx::tmem_ld16(col, v0);
             ptx::tmem_ld16(col + 16, v1);
             ptx::tmem_ld_wait();
@@ -754,21 +782,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // P leaves in its operand layout, 16 bytes per thread: row i, columns 8 jb ..;
-    // the diagonal (qh_i . kh_i) and the zeros above it are filled in here
-    {
-        const float* Pst = reinterpret_cast<const float*>(sm.ring + kOffPst);
-        const int i = tid >> 3, jb = tid & 7;
-        const float dv = sm.diag[i] + sm.diag[kChunk + i];
-        float x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int j = 8 * jb + u;
-            x[u] = j < i ? Pst[i * AP + j] : (j == i ? dv : 0.f);
-        }
-        *reinterpret_cast<uint4*>(&gP[op_index(i, 8 * jb, kChunk)]) = pack8(x);
-    }
-
     // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
     // 8 x 8 diagonal blocks by forward substitution (written whole, zeros above the
     // diagonal), then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two inverted n x n
@@ -853,63 +866,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int part = 0; part < 2; ++part)  // u = (X Diag(beta)) v: columns 64 ..
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16(tmem + 64, xd[part] + (uint64_t)(kk * 128), vb + (uint64_t)(kk * 16), id_u,
+                    ptx::mma_bf16(tmem + reg + 64, xd[part] + (uint64_t)(kk * 128), vb + (uint64_t)(kk * 16), id_u,
                                   part > 0 || kk > 0);
 #pragma unroll
             for (int part = 0; part < 2; ++part)  // w^T = (kh gamma)^T (X Diag(beta))^T: columns 0-63
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16(tmem + 0, kd + kk * kstep, xd[part] + (uint64_t)(kk * 128), id_w,
+                    ptx::mma_bf16(tmem + reg + 0, kd + kk * kstep, xd[part] + (uint64_t)(kk * 128), id_w,
                                   part > 0 || kk > 0);
         }
         ptx::mma_commit(&sm.wu_bar);  // (also when nothing was issued: the phase still completes)
     }
     if (next.h < H) load_beta(next, rows_next);
+    // while those products run: P of this item, u and w^T of the previous one
+    // P leaves in its operand layout, 16 bytes per thread: row i, columns 8 jb ..;
+    // the diagonal (qh_i . kh_i) and the zeros above it are filled in here
+    {
+        const float* Pst = reinterpret_cast<const float*>(sm.ring + kOffPst);
+        const int i = tid >> 3, jb = tid & 7;
+        const float dv = sm.diag[i] + sm.diag[kChunk + i];
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = 8 * jb + u;
+            x[u] = j < i ? Pst[i * AP + j] : (j == i ? dv : 0.f);
+        }
+        *reinterpret_cast<uint4*>(&gP[op_index(i, 8 * jb, kChunk)]) = pack8(x);
+    }
+
+    if (have_prev) epilogue(prev_reg, prev_wq, prev_u);
     if (!ptx::mbar_wait_or_abort(&sm.wu_bar, par, abort)) raise_timeout(ws, abort);
     ptx::tc_fence_after();
     if (tid == 0 && next.h < H && !*abort) {  // v (and, for fp32 inputs, everything) of the next item
         if (kBf16In) issue_v(next, rows_next);
         else issue_qkg(next, rows_next);
     }
-    {
-        const int q = warp & 3, cg = warp >> 2;
-        // w^T: lane = channel (dk = 64: lanes 0-15 of each quarter), columns = chunk rows
-        {
-            float x[16];
-            ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * cg, x);
-            ptx::tmem_ld_wait();
-            const int cc = DK == 128 ? 32 * q + lane : 16 * q + lane;
-            if (DK == 128 || lane < 16) {
-                float y0[8], y1[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    y0[u] = x[u];
-                    y1[u] = x[8 + u];
-                }
-                *reinterpret_cast<uint4*>(gWQ + mn_off<DK>(16 * cg, cc)) = pack8(y0);
-                *reinterpret_cast<uint4*>(gWQ + mn_off<DK>(16 * cg + 8, cc)) = pack8(y1);
-            }
-        }
-        // u: lanes 0-15 of each quarter = chunk rows 16 q .., columns DV/4 per warp
-        {
-            constexpr int NC = DV / 4;
-            const int row = 16 * q + lane;
-#pragma unroll
-            for (int i = 0; i < NC / 16; ++i) {
-                float x[16];
-                ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 64 + cg * NC + 16 * i, x);
-                ptx::tmem_ld_wait();
-                if (lane < 16) {
-#pragma unroll
-                    for (int u4 = 0; u4 < 4; ++u4) {
-                        const int n = cg * NC + 16 * i + 4 * u4;
-                        *reinterpret_cast<float4*>(&gU[u0_index(row, n)]) =
-                            make_float4(x[4 * u4], x[4 * u4 + 1], x[4 * u4 + 2], x[4 * u4 + 3]);
-                    }
-                }
-            }
-        }
-    }
+    have_prev = true;
+    prev_reg = reg;
+    prev_wq = gWQ;
+    prev_u = gU;
     ptx::tc_fence_before();
     __syncthreads();
     if (*abort) break;
@@ -917,6 +912,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     item = next;
     rows_cur = rows_next;
     }  // items
+
+    if (have_prev) {  // u and w^T of the last item
+        ptx::tc_fence_after();
+        epilogue(prev_reg, prev_wq, prev_u);
+    }
 
     // Leave cleanly: copies still in flight land, issued MMAs complete, then TMEM goes.
     if (tid == 0) {
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 0) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 256);
+        ptx::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -986,7 +986,7 @@ cudaError_t launch_t(const Dims& d, const void* q, const void* k, const void* v,
     using Sm = FactorSmem<DK, DV, TIn>;
     static_assert(sizeof(Sm) <= 227 * 1024, "factor kernel shared memory");
     static_assert(offsetof(Sm, qr) % 128 == 0 && offsetof(Sm, kr) % 128 == 0 &&
-                      offsetof(Sm, al) % 128 == 0 && offsetof(Sm, vs) % 128 == 0 &&
+                      offsetof(Sm, gr) % 128 == 0 && offsetof(Sm, vs) % 128 == 0 &&
                       offsetof(Sm, kg) % 128 == 0,
                   "tensor-copy and operand destinations are 128-byte aligned");
     auto kern = factor_kernel<DK, DV, TIn, TG>;
