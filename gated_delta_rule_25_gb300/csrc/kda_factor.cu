@@ -45,6 +45,8 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kIssuer2 = 256;  // the second tensor-core issuing thread (lane 0 of warp 8)
+constexpr int kIssuer3 = 384;  // the third (lane 0 of warp 12)
 constexpr uint32_t kAMajorMN = 1u << 15;  // instruction-descriptor bit: A is M-major
 constexpr uint32_t kBMajorMN = 1u << 16;  // instruction-descriptor bit: B is N-major
 constexpr int AP = kChunk + 1;            // row stride of the fp32 A and X arrays
@@ -293,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&sm.ld_bar, 1);
         ptx::mbar_init(&sm.v_bar, 1);
         for (int i = 0; i < 3; ++i) ptx::mbar_init(&sm.lv_bar[i], 1);
-        ptx::mbar_init(&sm.wu_bar, 1);
-        ptx::mbar_init(&sm.drain_bar, 1);
+        ptx::mbar_init(&sm.wu_bar, 2);  // u and w^T, two issuing threads
+        ptx::mbar_init(&sm.drain_bar, 3);
         sm.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -746,7 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncthreads();
         ptx::tc_fence_after();
-        if (tid == 0 && !*abort) issue_level_pair<DK>(tmem + reg + 128, p2, &sm.lv_bar[2]);
+        // (warp 12 has no part in P3, so its issue time hides there)
+        if (tid == kIssuer3 && !*abort) issue_level_pair<DK>(tmem + reg + 128, p2, &sm.lv_bar[2]);
     }
 
     // ------------------------------------------ P3: A and P out of tensor memory
@@ -845,35 +848,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
 
     // ------------------------------------------------- P7: u and w^T on tcgen05
-    if (tid == 0) {
+    // Two issuing threads (each tcgen05.mma costs its issuer ~85 cycles): thread 0
+    // issues u (it needs v) into columns reg + 64 .., thread kIssuer2 issues w^T into
+    // columns reg + 0 ..
+    if (tid == 0 || tid == kIssuer2) {
         bool okv = true;
-        if (kBf16In) {
+        if (kBf16In && tid == 0) {
             okv = ptx::mbar_wait_or_abort(&sm.v_bar, par, abort);
             if (okv) ++v_done;
             else raise_timeout(ws, abort);
         }
         ptx::tc_fence_after();
         if (okv && !*abort) {
-            const uint32_t va = ptx::smem_u32(sm.vs), ka = ptx::smem_u32(sm.kg);
-            constexpr uint32_t id_u = ptx::idesc_bf16(kChunk, DV) | kBMajorMN;
-            constexpr uint32_t id_w = ptx::idesc_bf16(DK, kChunk);
             const uint64_t xd[2] = {ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXop), 1024, 128),
                                     ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXlo), 1024, 128)};
-            const uint64_t vb = ptx::smem_desc(va, 128, 1024);
-            const uint64_t kd = ptx::smem_desc(ka, (DK / 8) * 128, 128);
-            constexpr uint64_t kstep = (uint64_t)((2 * (DK / 8) * 128) >> 4);
+            if (tid == 0) {  // u = (X Diag(beta)) v, hi then lo
+                constexpr uint32_t id_u = ptx::idesc_bf16(kChunk, DV) | kBMajorMN;
+                const uint64_t vb = ptx::smem_desc(ptx::smem_u32(sm.vs), 128, 1024);
 #pragma unroll
-            for (int part = 0; part < 2; ++part)  // u = (X Diag(beta)) v: columns 64 ..
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16(tmem + reg + 64, xd[part] + (uint64_t)(kk * 128), vb + (uint64_t)(kk * 16), id_u,
-                                  part > 0 || kk > 0);
+                    for (int kk = 0; kk < kChunk / 16; ++kk)
+                        ptx::mma_bf16(tmem + reg + 64, xd[part] + (uint64_t)(kk * 128), vb + (uint64_t)(kk * 16),
+                                      id_u, part > 0 || kk > 0);
+            } else {         // w^T = (kh gamma)^T (X Diag(beta))^T, hi then lo
+                constexpr uint32_t id_w = ptx::idesc_bf16(DK, kChunk);
+                const uint64_t kd = ptx::smem_desc(ptx::smem_u32(sm.kg), (DK / 8) * 128, 128);
+                constexpr uint64_t kstep = (uint64_t)((2 * (DK / 8) * 128) >> 4);
 #pragma unroll
-            for (int part = 0; part < 2; ++part)  // w^T = (kh gamma)^T (X Diag(beta))^T: columns 0-63
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16(tmem + reg + 0, kd + kk * kstep, xd[part] + (uint64_t)(kk * 128), id_w,
-                                  part > 0 || kk > 0);
+                    for (int kk = 0; kk < kChunk / 16; ++kk)
+                        ptx::mma_bf16(tmem + reg + 0, kd + kk * kstep, xd[part] + (uint64_t)(kk * 128), id_w,
+                                      part > 0 || kk > 0);
+            }
         }
         ptx::mma_commit(&sm.wu_bar);  // (also when nothing was issued: the phase still completes)
     }
@@ -919,12 +927,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // Leave cleanly: copies still in flight land, issued MMAs complete, then TMEM goes.
-    if (tid == 0) {
+    {
         volatile int never = 0;
-        for (uint32_t k2 = ld_done; k2 < ld_issued; ++k2) ptx::mbar_wait_or_abort(&sm.ld_bar, k2 & 1u, &never);
-        for (uint32_t k2 = v_done; k2 < v_issued; ++k2) ptx::mbar_wait_or_abort(&sm.v_bar, k2 & 1u, &never);
-        ptx::mma_commit(&sm.drain_bar);
-        ptx::mbar_wait_or_abort(&sm.drain_bar, 0, &never);
+        if (tid == 0) {
+            for (uint32_t k2 = ld_done; k2 < ld_issued; ++k2) ptx::mbar_wait_or_abort(&sm.ld_bar, k2 & 1u, &never);
+            for (uint32_t k2 = v_done; k2 < v_issued; ++k2) ptx::mbar_wait_or_abort(&sm.v_bar, k2 & 1u, &never);
+        }
+        if (tid == 0 || tid == kIssuer2 || tid == kIssuer3) ptx::mma_commit(&sm.drain_bar);  // each issuer's own products
+        if (tid == 0) ptx::mbar_wait_or_abort(&sm.drain_bar, 0, &never);
     }
     ptx::tc_fence_before();
     __syncthreads();
