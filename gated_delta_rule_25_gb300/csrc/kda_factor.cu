@@ -37,6 +37,8 @@
 #include <cuda.h>          // CUtensorMap (the encoder itself is fetched at run time)
 #include <cudaTypedefs.h>  // the encoder's function-pointer type
 
+#include <type_traits>
+
 #include "kda_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -77,8 +79,12 @@ struct __align__(1024) FactorSmem {
     TIn qr[kChunk * DK];                 // raw q rows as copied in; qh = qr * iq[row]
     TIn kr[kChunk * DK];                 // raw k rows; kh = kr * ik[row]
     float gr[kChunk * DK];               // raw g rows as copied in (fp32, or bf16 in the first half)
-    __nv_bfloat16 vs[kChunk * DV];       // v, N-major operand: [DV/8][64 rows][8 columns]
-    __nv_bfloat16 kg[DK * kChunk];       // (kh * gamma)^T, K-major operand (DK x 64)
+    // v: bf16 inputs, the N-major bf16 operand [DV/8][64 rows][8 columns]; fp32
+    // inputs, the K-major tf32 operand (DV x 64, 4 chunk rows per 16-byte core row)
+    std::conditional_t<sizeof(TIn) == 2, __nv_bfloat16, float> vs[kChunk * DV];
+    // (kh * gamma)^T, K-major bf16 operand (DK x 64); with fp32 inputs it is a tf32
+    // operand in the q staging, dead by then, and this array is unused
+    __nv_bfloat16 kg[sizeof(TIn) == 2 ? DK * kChunk : 8];
     float blk_a[8 * DK];                 // alpha at the first row of each 8-row block
     float blk_t[8 * DK];                 // product of alpha over rows 1..7 of each block
     float diag[2 * kChunk];              // qh_i . kh_i, one partial sum per channel half
@@ -467,17 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm.ik[r] = ok_r ? rsqrtf(sk + 1e-6f) : 0.f;
             }
         }
-        if (!kBf16In) {  // fp32 v (in the ring) -> the bf16 N-major operand, zero past the end
-            constexpr int VC = DV / 8;
-            for (int e = tid; e < kChunk * VC; e += kThreads) {
-                const int r = e / VC, cg = e % VC;
-                float xv[8];
-                unpack8<TIn>(reinterpret_cast<const uint4*>(sm.ring + r * VB + cg * 8 * sizeof(TIn)), xv);
-                if (r >= L) {
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) xv[u] = 0.f;
-                }
-                *reinterpret_cast<uint4*>(&sm.vs[(cg * kChunk + r) * 8]) = pack8(xv);
+        if constexpr (!kBf16In) {  // fp32 v (in the ring) -> the tf32 K-major operand, zero past the end
+            const float* vr = reinterpret_cast<const float*>(sm.ring);
+            for (int e = tid; e < (kChunk / 4) * DV; e += kThreads) {
+                const int n = e % DV, r4 = 4 * (e / DV);  // a warp: 32 consecutive columns
+                float4 x4;
+                x4.x = r4 < L ? vr[r4 * DV + n] : 0.f;
+                x4.y = r4 + 1 < L ? vr[(r4 + 1) * DV + n] : 0.f;
+                x4.z = r4 + 2 < L ? vr[(r4 + 2) * DV + n] : 0.f;
+                x4.w = r4 + 3 < L ? vr[(r4 + 3) * DV + n] : 0.f;
+                *reinterpret_cast<float4*>(&sm.vs[op_index32(n, r4, DV)]) = x4;
             }
         }
         if (tid < kChunk) sm.bs[tid] = rb;
@@ -651,7 +656,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // QG: rows 64 + 8b .. of the [w; QG] tile (global, M-major)
             *reinterpret_cast<uint4*>(gWQ + mn_off<DK>(kChunk + 8 * b, cc)) = pack8(vg);
             // (kh gamma)^T for the w product: K-major operand, 8 chunk rows of channel cc
-            *reinterpret_cast<uint4*>(&sm.kg[op_index(cc, 8 * b, DK)]) = pack8(vk);
+            // (fp32 inputs: tf32, in the q staging, whose reads all came before the
+            // barrier above)
+            if constexpr (kBf16In) {
+                *reinterpret_cast<uint4*>(&sm.kg[op_index(cc, 8 * b, DK)]) = pack8(vk);
+            } else {
+                float* kgf = reinterpret_cast<float*>(sm.qr);
+                *reinterpret_cast<float4*>(&kgf[op_index32(cc, 8 * b, DK)]) = make_float4(vk[0], vk[1], vk[2], vk[3]);
+                *reinterpret_cast<float4*>(&kgf[op_index32(cc, 8 * b + 4, DK)]) = make_float4(vk[4], vk[5], vk[6], vk[7]);
+            }
             // KT (fp32, tf32 operand layout): kh * gamma_L / gamma
             float kt[8];
 #pragma unroll
@@ -816,11 +829,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv_join_tc<32>(X, A, T, warp, lane);
     }
 
-    // ------------------------------------- P6: X Diag(beta) as bf16 hi + lo operands
+    // ------------------------------------- P6: X Diag(beta) as hi + lo operands
+    // (bf16 with bf16 inputs; tf32 with fp32 inputs, whose u and w run on tf32:
+    // the hi part in the ring, the lo part in the k staging, dead by then)
     {
         const float* X = reinterpret_cast<const float*>(sm.ring + kOffX);
-        __nv_bfloat16* xop = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXop);
-        __nv_bfloat16* xlo = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXlo);
         // 64 rows x 8 groups: a warp takes 32 consecutive rows of one group, so its
         // X reads (row stride 65) and operand stores (rows of a group are adjacent
         // 16-byte core rows) are free of bank conflicts
@@ -831,16 +844,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = jb + u;
             x[u] = (j <= i) ? X[i * AP + j] * sm.bs[j] : 0.f;
         }
-        const uint4 hi = pack8(x);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hi);
+        if constexpr (kBf16In) {
+            __nv_bfloat16* xop = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXop);
+            __nv_bfloat16* xlo = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXlo);
+            const uint4 hi = pack8(x);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hi);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 f = __bfloat1622float2(h2[u]);
-            lo[2 * u] = x[2 * u] - f.x;
-            lo[2 * u + 1] = x[2 * u + 1] - f.y;
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                lo[2 * u] = x[2 * u] - f.x;
+                lo[2 * u + 1] = x[2 * u + 1] - f.y;
+            }
+            *reinterpret_cast<uint4*>(&xop[op_index(i, jb, kChunk)]) = hi;
+            *reinterpret_cast<uint4*>(&xlo[op_index(i, jb, kChunk)]) = pack8(lo);
+        } else {
+            float* xop = reinterpret_cast<float*>(sm.ring + kOffXop);
+            float* xlo = reinterpret_cast<float*>(sm.kr);
+            float hi[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                hi[u] = __uint_as_float(to_tf32(x[u]));
+                lo[u] = __uint_as_float(to_tf32(x[u] - hi[u]));
+            }
+#pragma unroll
+            for (int h4 = 0; h4 < 8; h4 += 4) {
+                *reinterpret_cast<float4*>(&xop[op_index32(i, jb + h4, kChunk)]) =
+                    make_float4(hi[h4], hi[h4 + 1], hi[h4 + 2], hi[h4 + 3]);
+                *reinterpret_cast<float4*>(&xlo[op_index32(i, jb + h4, kChunk)]) =
+                    make_float4(lo[h4], lo[h4 + 1], lo[h4 + 2], lo[h4 + 3]);
+            }
         }
-        *reinterpret_cast<uint4*>(&xop[op_index(i, jb, kChunk)]) = hi;
-        *reinterpret_cast<uint4*>(&xlo[op_index(i, jb, kChunk)]) = pack8(lo);
         ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
@@ -859,7 +892,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             else raise_timeout(ws, abort);
         }
         ptx::tc_fence_after();
-        if (okv && !*abort) {
+        if (okv && !*abort && !kBf16In) {  // fp32 inputs: tf32 products, K = 8 per step
+            const uint64_t xd[2] = {ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXop), 1024, 128),
+                                    ptx::smem_desc(ptx::smem_u32(sm.kr), 1024, 128)};
+            if (tid == 0) {  // u = (X Diag(beta)) v, hi then lo
+                constexpr uint32_t id_u = ptx::idesc_tf32(kChunk, DV);
+                const uint64_t vb = ptx::smem_desc(ptx::smem_u32(sm.vs), (DV / 8) * 128, 128);
+                constexpr uint64_t vstep = (uint64_t)((2 * (DV / 8) * 128) >> 4);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 8; ++kk)
+                        ptx::mma_tf32(tmem + reg + 64, xd[part] + (uint64_t)(kk * 128), vb + kk * vstep, id_u,
+                                      part > 0 || kk > 0);
+            } else {         // w^T = (kh gamma)^T (X Diag(beta))^T, hi then lo
+                constexpr uint32_t id_w = ptx::idesc_tf32(DK, kChunk);
+                const uint64_t kd = ptx::smem_desc(ptx::smem_u32(sm.qr), (DK / 8) * 128, 128);
+                constexpr uint64_t kstep = (uint64_t)((2 * (DK / 8) * 128) >> 4);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 8; ++kk)
+                        ptx::mma_tf32(tmem + reg + 0, kd + kk * kstep, xd[part] + (uint64_t)(kk * 128), id_w,
+                                      part > 0 || kk > 0);
+            }
+        }
+        if (okv && !*abort && kBf16In) {
             const uint64_t xd[2] = {ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXop), 1024, 128),
                                     ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXlo), 1024, 128)};
             if (tid == 0) {  // u = (X Diag(beta)) v, hi then lo

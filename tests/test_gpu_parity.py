@@ -237,3 +237,22 @@ def test_malformed_cu_seqlens_reports_device_error(kda):
     assert e.value.status == 6
     # the context stays usable
     _assert_parity(x, *_gpu(kda, x))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp32_inputs_run_u_and_w_on_tf32(kda, d):
+    """fp32 q, k, v (BASELINE config 1) compute u = X Diag(beta) v and w on tf32
+    operands.  Against the fp64 oracle on the fp32 values, that path is more accurate
+    than casting the same values to bf16 and running the bf16 path, which rounds v
+    and kh gamma to bf16 operands (as fp32 inputs were computed before)."""
+    x32 = gen.make_cfg1(seed=15, salt=SALT, T=512, H=2, d=d)
+    o32, h32 = _gpu(kda, x32)
+    o_ref, h_ref = oracle.kda_recurrence_fp64(**x32.tensors())
+    x16 = gen.make_cfg1(seed=15, salt=SALT, T=512, H=2, d=d, dtype=torch.bfloat16)
+    o16, h16 = _gpu(kda, x16)
+    eo32, eh32 = rel_rmse(o32, o_ref), rel_rmse(h32, h_ref)
+    eo16, eh16 = rel_rmse(o16, o_ref), rel_rmse(h16, h_ref)
+    msg = f"fp32 path o {eo32:.2e} hT {eh32:.2e}; bf16 cast o {eo16:.2e} hT {eh16:.2e}"
+    assert eo32 <= O_TOL and eh32 <= HT_TOL, msg
+    # measured over five salts: hT ratio 0.43-0.49, o ratio 0.63-0.66
+    assert eh32 < 0.7 * eh16 and eo32 < 0.8 * eo16, msg
