@@ -88,7 +88,7 @@ struct __align__(1024) FactorSmem {
     float blk_a[8 * DK];                 // alpha at the first row of each 8-row block
     float blk_t[8 * DK];                 // product of alpha over rows 1..7 of each block
     float diag[2 * kChunk];              // qh_i . kh_i, one partial sum per channel half
-    float bs[kChunk];                    // beta (zero past the chunk end)
+    float bs[2][kChunk];                 // beta (zero past the chunk end), alternate items
     float iq[kChunk], ik[kChunk];        // inverse row norms (zero past the chunk end)
     uint64_t ld_bar, v_bar, lv_bar[3], wu_bar, drain_bar;
     uint32_t tmem;
@@ -191,70 +191,32 @@ __device__ __forceinline__ void tile_mm_tf32(const float* P, int ldp, const floa
     C[(cr + gq + 8) * ldc + cc + 2 * tq + 1] = sign * acc[3];
 }
 
-// Tensor-core join for n = 16, 32: one 16 x 8 tile of T = A21 X11, then of
-// X21 = -X22 T, per warp.  Ends with the CTA synchronised.
-template <int N>
-__device__ __forceinline__ void inv_join_tc(float* X, const float* A, float* T, int warp, int lane) {
-    constexpr int PAIRS = kChunk / (2 * N);
-    constexpr int TILES = (N / 16) * (N / 8);  // tiles per pair
-    for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
-        const int pidx = t / TILES, tt = t % TILES;
-        const int r1 = 2 * pidx * N, r2 = r1 + N;
-        const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
-        tile_mm_tf32<N, false, true>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T + pidx * N * N,
-                                     N, cr, cc, 1.f, lane);
-    }
-    __syncthreads();
-    for (int t = warp; t < PAIRS * TILES; t += kThreads / 32) {
-        const int pidx = t / TILES, tt = t % TILES;
-        const int r1 = 2 * pidx * N, r2 = r1 + N;
-        const int cr = (tt / (N / 8)) * 16, cc = (tt % (N / 8)) * 8;
-        tile_mm_tf32<N, true, false>(X + r2 * AP + r2, AP, T + pidx * N * N, N, X + r2 * AP + r1, AP,
-                                     cr, cc, -1.f, lane);
-    }
-    __syncthreads();
+// Barrier of the first n threads of the CTA (id 1-15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Joins pairs of inverted n x n diagonal blocks of X = (I + A)^-1 (row stride
-// kChunk + 1): X21 = -X22 (A21 X11).  The 8 x 8 diagonal blocks of X are written
-// whole (zeros above their diagonal), so the products run over full blocks.  Ends
-// with the CTA synchronised.
-template <int N>
-__device__ __forceinline__ void inv_join(float* X, const float* A, float* T, int tid) {
-    constexpr int OUT = (kChunk / (2 * N)) * N * N;
-    constexpr int PER = (OUT + kThreads - 1) / kThreads;
-#pragma unroll
-    for (int qq = 0; qq < PER; ++qq) {
-        const int e = tid + qq * kThreads;
-        if (e < OUT) {
-            const int pidx = e / (N * N), i = (e / N) % N, j = e % N;
-            const int r1 = 2 * pidx * N, r2 = r1 + N;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < N; m += 2) {
-                a0 = fmaf(A[(r2 + i) * AP + r1 + m], X[(r1 + m) * AP + r1 + j], a0);
-                a1 = fmaf(A[(r2 + i) * AP + r1 + m + 1], X[(r1 + m + 1) * AP + r1 + j], a1);
-            }
-            T[e] = a0 + a1;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int qq = 0; qq < PER; ++qq) {
-        const int e = tid + qq * kThreads;
-        if (e < OUT) {
-            const int pidx = e / (N * N), i = (e / N) % N, j = e % N;
-            const int r1 = 2 * pidx * N, r2 = r1 + N;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < N; m += 2) {
-                a0 = fmaf(X[(r2 + i) * AP + r2 + m], T[pidx * N * N + m * N + j], a0);
-                a1 = fmaf(X[(r2 + i) * AP + r2 + m + 1], T[pidx * N * N + (m + 1) * N + j], a1);
-            }
-            X[(r2 + i) * AP + r1 + j] = -(a0 + a1);
-        }
-    }
-    __syncthreads();
+// Warps 0-7 join the two inverted 32 x 32 diagonal blocks: one 16 x 8 tile of
+// T = A21 X11 per warp, a barrier of the eight warps, one tile of X21 = -X22 T.
+// No trailing barrier (the caller's follows).
+__device__ __forceinline__ void inv_join64(float* X, const float* A, float* T, int warp, int lane) {
+    constexpr int N = 32;
+    const int cr = (warp >> 2) * 16, cc = (warp & 3) * 8;
+    tile_mm_tf32<N, false, true>(A + N * AP, AP, X, AP, T, N, cr, cc, 1.f, lane);
+    named_sync(2, 256);
+    tile_mm_tf32<N, true, false>(X + N * AP + N, AP, T, N, X + N * AP, AP, cr, cc, -1.f, lane);
+}
+
+// One warp joins the two inverted 16 x 16 diagonal blocks of the 32-block at rows
+// 32 p ..: T = A21 X11, then X21 = -X22 T (two 16 x 8 tiles per product, ordered
+// by __syncwarp, no CTA barrier).
+__device__ __forceinline__ void inv_join16_warp(float* X, const float* A, float* T, int p, int lane) {
+    const int r1 = 32 * p, r2 = r1 + 16;
+    tile_mm_tf32<16, false, true>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T, 16, 0, 0, 1.f, lane);
+    tile_mm_tf32<16, false, true>(A + r2 * AP + r1, AP, X + r1 * AP + r1, AP, T, 16, 0, 8, 1.f, lane);
+    __syncwarp();
+    tile_mm_tf32<16, true, false>(X + r2 * AP + r2, AP, T, 16, X + r2 * AP + r1, AP, 0, 0, -1.f, lane);
+    tile_mm_tf32<16, true, false>(X + r2 * AP + r2, AP, T, 16, X + r2 * AP + r1, AP, 0, 8, -1.f, lane);
 }
 
 __device__ __forceinline__ void raise_timeout(uint8_t* ws, volatile int* abort) {
@@ -355,9 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_4d(sm.vs, &tm_v, 0, nk.x, it.h, 0, &sm.v_bar);
         ++v_issued;
     };
-    float rb = 0.f;  // beta of this thread's row of the next item (threads < 64)
-    auto load_beta = [&](Item it, int2 nk) {
-        rb = (tid < kChunk && tid < nk.y) ? beta[(size_t)(nk.x + tid) * H + it.h] : 0.f;
+    // beta of row t of an item, for the thread that will be thread t of that item's P1
+    float rb = 0.f;
+    auto load_beta = [&](Item it, int2 nk, int t) {
+        rb = (t >= 0 && t < kChunk && t < nk.y) ? beta[(size_t)(nk.x + t) * H + it.h] : 0.f;
     };
 
     Item item = total > 0 ? Item{(int)(blockIdx.x % (unsigned)total), (int)(blockIdx.x / (unsigned)total)}
@@ -368,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_qkg(item, rows_cur);
             if (kBf16In) issue_v(item, rows_cur);
         }
-        load_beta(item, rows_cur);
+        load_beta(item, rows_cur, tid);
     }
     uint32_t par = 0;  // every per-item barrier completes once per item
     // Tensor memory: item n works in columns [256 (n % 2), + 192) (level products,
@@ -413,6 +376,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     };
+    // ------------------------------------------------------------ P1: load
+    // Row norms of q and k, and beta, of the item with L valid rows whose copies
+    // complete phase pp of ld_bar, by threads t = 0 .. NT-1 of the CTA (all of them,
+    // or warps 8-15 while warps 0-7 invert the previous item's matrix); no barrier
+    // inside.  Rows past the chunk end get zero norms (so qh = kh = 0 there) and beta
+    // = 0.  beta of this thread's row arrived in rb (load_beta).
+    auto p1 = [&](const int L, const uint32_t pp, const int t, auto nt_c, float* bsdst) {
+        {
+            if (ptx::mbar_wait_or_abort(&sm.ld_bar, pp, abort)) {
+                if (tid == 0) ++ld_done;
+            } else {
+                raise_timeout(ws, abort);
+            }
+            constexpr int NT = decltype(nt_c)::value;  // threads taking part
+            constexpr int CPR = DK / 8, RP = NT / CPR, NP = kChunk / RP;
+            constexpr int QW = (int)sizeof(TIn) / 2;
+            const int ck = t % CPR, rsub = t / CPR;
+    #pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                const int r = rsub + p * RP;
+                const bool ok_r = r < L;
+                const uint4* wq = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.qr) + r * QB + ck * 8 * sizeof(TIn));
+                const uint4* wk = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.kr) + r * QB + ck * 8 * sizeof(TIn));
+                uint4 rq[QW], rk[QW];
+    #pragma unroll
+                for (int w2 = 0; w2 < QW; ++w2) {
+                    rq[w2] = wq[w2];
+                    rk[w2] = wk[w2];
+                }
+                float xq[8], xk[8];
+                unpack8<TIn>(rq, xq);
+                unpack8<TIn>(rk, xk);
+                float sq = 0.f, sk = 0.f;
+    #pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sq = fmaf(xq[e], xq[e], sq);
+                    sk = fmaf(xk[e], xk[e], sk);
+                }
+    #pragma unroll
+                for (int o = 1; o < CPR; o <<= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                }
+                if (ck == 0) {
+                    sm.iq[r] = ok_r ? rsqrtf(sq + 1e-6f) : 0.f;
+                    sm.ik[r] = ok_r ? rsqrtf(sk + 1e-6f) : 0.f;
+                }
+            }
+            if constexpr (!kBf16In) {  // fp32 v (in the ring) -> the tf32 K-major operand, zero past the end
+                const float* vr = reinterpret_cast<const float*>(sm.ring);
+                for (int e = t; e < (kChunk / 4) * DV; e += NT) {
+                    const int n = e % DV, r4 = 4 * (e / DV);  // a warp: 32 consecutive columns
+                    float4 x4;
+                    x4.x = r4 < L ? vr[r4 * DV + n] : 0.f;
+                    x4.y = r4 + 1 < L ? vr[(r4 + 1) * DV + n] : 0.f;
+                    x4.z = r4 + 2 < L ? vr[(r4 + 2) * DV + n] : 0.f;
+                    x4.w = r4 + 3 < L ? vr[(r4 + 3) * DV + n] : 0.f;
+                    *reinterpret_cast<float4*>(&sm.vs[op_index32(n, r4, DV)]) = x4;
+                }
+            }
+            if (t < kChunk) bsdst[t] = rb;
+        }
+    };
+    // Warm L2 with an item's inputs, so that its tensor copies find them there.
+    auto warm_l2 = [&](Item y, int2 ry) {
+        if (y.h < H) {
+            ptx::tma_prefetch_3d(&tm_q, 0, y.h, ry.x);
+            ptx::tma_prefetch_3d(&tm_k, 0, y.h, ry.x);
+            ptx::tma_prefetch_3d(&tm_g, 0, y.h, ry.x);
+            if (kBf16In) ptx::tma_prefetch_4d(&tm_v, 0, ry.x, y.h, 0);
+            else ptx::tma_prefetch_3d(&tm_v, 0, y.h, ry.x);
+        }
+    };
+    using AllThreads = std::integral_constant<int, kThreads>;
+    using HalfThreads = std::integral_constant<int, kThreads / 2>;
+    // bf16 inputs: the next item's P1 runs on warps 8-15 while warps 0-7 invert this
+    // item's matrix; fp32 inputs: at the start of each item (its v tile lands in the
+    // ring, which the inversion uses)
+    bool p1_done = false;
+
     bool have_prev = false;
     uint32_t prev_reg = 0;
     uint8_t* prev_wq = nullptr;
@@ -430,75 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* const gGL = reinterpret_cast<float*>(fb + F.gl);
     const int L = rows_cur.y;
 
-    // ------------------------------------------------------------ P1: load
-    // inverse row norms of q and k, and beta; rows past the chunk end get zero norms
-    // (so qh = kh = 0 there) and beta = 0
-    {
-        if (ptx::mbar_wait_or_abort(&sm.ld_bar, par, abort)) {
-            if (tid == 0) ++ld_done;
-        } else {
-            raise_timeout(ws, abort);
-        }
-        constexpr int CPR = DK / 8, RP = kThreads / CPR, NP = kChunk / RP;
-        constexpr int QW = (int)sizeof(TIn) / 2;
-        const int ck = tid % CPR, rsub = tid / CPR;
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-            const int r = rsub + p * RP;
-            const bool ok_r = r < L;
-            const uint4* wq = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.qr) + r * QB + ck * 8 * sizeof(TIn));
-            const uint4* wk = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.kr) + r * QB + ck * 8 * sizeof(TIn));
-            uint4 rq[QW], rk[QW];
-#pragma unroll
-            for (int w2 = 0; w2 < QW; ++w2) {
-                rq[w2] = wq[w2];
-                rk[w2] = wk[w2];
-            }
-            float xq[8], xk[8];
-            unpack8<TIn>(rq, xq);
-            unpack8<TIn>(rk, xk);
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sq = fmaf(xq[e], xq[e], sq);
-                sk = fmaf(xk[e], xk[e], sk);
-            }
-#pragma unroll
-            for (int o = 1; o < CPR; o <<= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            if (ck == 0) {
-                sm.iq[r] = ok_r ? rsqrtf(sq + 1e-6f) : 0.f;
-                sm.ik[r] = ok_r ? rsqrtf(sk + 1e-6f) : 0.f;
-            }
-        }
-        if constexpr (!kBf16In) {  // fp32 v (in the ring) -> the tf32 K-major operand, zero past the end
-            const float* vr = reinterpret_cast<const float*>(sm.ring);
-            for (int e = tid; e < (kChunk / 4) * DV; e += kThreads) {
-                const int n = e % DV, r4 = 4 * (e / DV);  // a warp: 32 consecutive columns
-                float4 x4;
-                x4.x = r4 < L ? vr[r4 * DV + n] : 0.f;
-                x4.y = r4 + 1 < L ? vr[(r4 + 1) * DV + n] : 0.f;
-                x4.z = r4 + 2 < L ? vr[(r4 + 2) * DV + n] : 0.f;
-                x4.w = r4 + 3 < L ? vr[(r4 + 3) * DV + n] : 0.f;
-                *reinterpret_cast<float4*>(&sm.vs[op_index32(n, r4, DV)]) = x4;
-            }
-        }
-        if (tid < kChunk) sm.bs[tid] = rb;
+    if (!p1_done) {
+        p1(L, par, tid, AllThreads{}, sm.bs[par]);
+        __syncthreads();
+        if (tid == 64) warm_l2(after, rows_after);
     }
-    __syncthreads();
-
-    // Warm L2 with the inputs of the item after next, so that its tensor copies
-    // (issued during the next item) find them there.
-    if (tid == 64 && after.h < H) {
-        const int hy = after.h;
-        ptx::tma_prefetch_3d(&tm_q, 0, hy, rows_after.x);
-        ptx::tma_prefetch_3d(&tm_k, 0, hy, rows_after.x);
-        ptx::tma_prefetch_3d(&tm_g, 0, hy, rows_after.x);
-        if (kBf16In) ptx::tma_prefetch_4d(&tm_v, 0, rows_after.x, hy, 0);
-        else ptx::tma_prefetch_3d(&tm_v, 0, hy, rows_after.x);
-    }
+    p1_done = false;
+    // rb: beta of the next item, for its P1 (run by warps 8-15 with bf16 inputs)
+    if (next.h < H) load_beta(next, rows_next, kBf16In ? tid - kThreads / 2 : tid);
 
     // ------------------------------------------ P2: level operands, QG, KT, kh gamma
     // Thread: 8-row block b = warp / 2 (rows 8b .. 8b+7) of CPT channels
@@ -790,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int blk = lane >> lg;                      // the 2s-block of this row
             const int i = (blk << (lg + 1)) + s + (lane & (s - 1));
             float* const row = ((q & 1) == 0 ? A : Pst) + i * AP + (blk << lg);  // + n = column j
-            const float sc = (q & 1) == 0 ? sm.bs[i] : 1.f;
+            const float sc = (q & 1) == 0 ? sm.bs[par][i] : 1.f;
 #pragma unroll
             for (int n = 0; n < 32; ++n)
                 if ((n >> lg) == blk) row[n] = sc * v(n);
@@ -799,34 +781,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     // ------------------------------------- P5: X = (I + A)^-1 by recursive doubling
-    // 8 x 8 diagonal blocks by forward substitution (written whole, zeros above the
-    // diagonal), then for n = 8, 16, 32: X21 = -X22 (A21 X11) joins two inverted n x n
-    // blocks into one 2n x 2n block (n = 8 on CUDA cores, n = 16 and 32 with mma.sync
-    // on tf32 inputs and fp32 accumulation).  Entries of X above the diagonal outside
-    // the 8 x 8 blocks are never written; the joins read them as zero, and nothing
-    // else reads them.  Only entries of A strictly below the diagonal are read.
+    // The four 16 x 16 diagonal blocks by forward substitution in fp32 registers
+    // (warp w, lanes 0-15: the columns of block w; right-looking, so each step's
+    // dependent chain is one FMA; written whole, zeros above the diagonal).  Then
+    // X21 = -X22 (A21 X11) joins two inverted blocks into one twice as large: 16 -> 32
+    // by one warp per 32-block on its own, 32 -> 64 by eight warps (mma.sync on tf32
+    // inputs, fp32 accumulation).  The upper-right block of each joined 32-block is
+    // never written; the 64-join reads it as zero.  Only entries of A strictly below
+    // the diagonal are read.
     {
         float* const A = reinterpret_cast<float*>(sm.ring + kOffA);
         float* const X = reinterpret_cast<float*>(sm.ring + kOffX);
         float* const T = reinterpret_cast<float*>(sm.ring + kOffScr);
-        if (tid < 64) {
-            const int base = 8 * (tid >> 3), jc = tid & 7;
-            float x[8];
+        if (warp < 8) {
+            if (warp < 4) {
+                if (lane < 16) {
+                    const int base = 16 * warp, jc = lane;
+                    float x[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float acc = (i == jc) ? 1.f : 0.f;
+                    for (int i = 0; i < 16; ++i) x[i] = (i == jc) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    if (m < i) acc -= A[(base + i) * AP + base + m] * x[m];
-                x[i] = (i < jc) ? 0.f : acc;
+                    for (int m = 0; m < 15; ++m) {  // x[m] is final: remove its share from the rows below
+                        const float xm = x[m];
+#pragma unroll
+                        for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-A[(base + i) * AP + base + m], xm, x[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) X[(base + i) * AP + base + jc] = x[i];
+                }
+                named_sync(3, 128);  // warps 0-3: the four 16-blocks
+                if (warp < 2) inv_join16_warp(X, A, T + 256 * warp, warp, lane);
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) X[(base + i) * AP + base + jc] = x[i];
+            named_sync(2, 256);      // warps 0-7: the two 32-blocks
+            inv_join64(X, A, T, warp, lane);
+        } else if (kBf16In && next.h < H) {
+            p1(rows_next.y, par ^ 1u, tid - kThreads / 2, HalfThreads{}, sm.bs[par ^ 1u]);
+            if (tid == kThreads / 2 + 64) {
+                const Item y = advance(after);
+                warm_l2(y, rows_of(y));
+            }
         }
         __syncthreads();
-        inv_join<8>(X, A, T, tid);
-        inv_join_tc<16>(X, A, T, warp, lane);
-        inv_join_tc<32>(X, A, T, warp, lane);
+        if (kBf16In && next.h < H) {
+            p1_done = true;
+            if (tid == 0 && !*abort) ++ld_done;  // warps 8-15 saw the next item's copies land
+        }
     }
 
     // ------------------------------------- P6: X Diag(beta) as hi + lo operands
@@ -842,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int j = jb + u;
-            x[u] = (j <= i) ? X[i * AP + j] * sm.bs[j] : 0.f;
+            x[u] = (j <= i) ? X[i * AP + j] * sm.bs[par][j] : 0.f;
         }
         if constexpr (kBf16In) {
             __nv_bfloat16* xop = reinterpret_cast<__nv_bfloat16*>(sm.ring + kOffXop);
@@ -943,7 +942,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mma_commit(&sm.wu_bar);  // (also when nothing was issued: the phase still completes)
     }
-    if (next.h < H) load_beta(next, rows_next);
     // while those products run: P of this item, u and w^T of the previous one
     // P leaves in its operand layout, 16 bytes per thread: row i, columns 8 jb ..;
     // the diagonal (qh_i . kh_i) and the zeros above it are filled in here
