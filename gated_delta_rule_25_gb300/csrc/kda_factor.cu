@@ -390,38 +390,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 raise_timeout(ws, abort);
             }
             constexpr int NT = decltype(nt_c)::value;  // threads taking part
-            constexpr int CPR = DK / 8, RP = NT / CPR, NP = kChunk / RP;
-            constexpr int QW = (int)sizeof(TIn) / 2;
+            // CH channels a thread (16, or 8 when every thread is needed for a row),
+            // CPR threads a row, NP rows a thread; all loads first, then the NP
+            // independent reductions side by side
+            constexpr int CPR = DK / 16 > NT / kChunk ? DK / 16 : NT / kChunk;
+            constexpr int CH = DK / CPR, RP = NT / CPR, NP = kChunk / RP;
+            static_assert(CH % 8 == 0 && NP >= 1, "row split");
+            constexpr int QW = CH * (int)sizeof(TIn) / 16;  // 16-byte words a thread reads
+            static_assert(QW * CPR * 16 == (int)QB, "a row is read once");
             const int ck = t % CPR, rsub = t / CPR;
+            float sq[NP], sk[NP];
     #pragma unroll
             for (int p = 0; p < NP; ++p) {
                 const int r = rsub + p * RP;
-                const bool ok_r = r < L;
-                const uint4* wq = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.qr) + r * QB + ck * 8 * sizeof(TIn));
-                const uint4* wk = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.kr) + r * QB + ck * 8 * sizeof(TIn));
+                // word ck + w2 * CPR of the row: each load of a warp is contiguous
+                const uint4* wq = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.qr) + r * QB) + ck;
+                const uint4* wk = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(sm.kr) + r * QB) + ck;
                 uint4 rq[QW], rk[QW];
     #pragma unroll
                 for (int w2 = 0; w2 < QW; ++w2) {
-                    rq[w2] = wq[w2];
-                    rk[w2] = wk[w2];
+                    rq[w2] = wq[w2 * CPR];
+                    rk[w2] = wk[w2 * CPR];
                 }
-                float xq[8], xk[8];
-                unpack8<TIn>(rq, xq);
-                unpack8<TIn>(rk, xk);
-                float sq = 0.f, sk = 0.f;
+                sq[p] = 0.f;
+                sk[p] = 0.f;
     #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    sq = fmaf(xq[e], xq[e], sq);
-                    sk = fmaf(xk[e], xk[e], sk);
-                }
+                for (int h8 = 0; h8 < CH / 8; ++h8) {
+                    float xq[8], xk[8];
+                    unpack8<TIn>(rq + h8 * (QW * 8 / CH), xq);
+                    unpack8<TIn>(rk + h8 * (QW * 8 / CH), xk);
     #pragma unroll
-                for (int o = 1; o < CPR; o <<= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                    for (int e = 0; e < 8; ++e) {
+                        sq[p] = fmaf(xq[e], xq[e], sq[p]);
+                        sk[p] = fmaf(xk[e], xk[e], sk[p]);
+                    }
                 }
-                if (ck == 0) {
-                    sm.iq[r] = ok_r ? rsqrtf(sq + 1e-6f) : 0.f;
-                    sm.ik[r] = ok_r ? rsqrtf(sk + 1e-6f) : 0.f;
+            }
+    #pragma unroll
+            for (int o = 1; o < CPR; o <<= 1) {
+    #pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    sq[p] += __shfl_xor_sync(0xffffffffu, sq[p], o);
+                    sk[p] += __shfl_xor_sync(0xffffffffu, sk[p], o);
+                }
+            }
+            if (ck == 0) {
+    #pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    const int r = rsub + p * RP;
+                    sm.iq[r] = r < L ? rsqrtf(sq[p] + 1e-6f) : 0.f;
+                    sm.ik[r] = r < L ? rsqrtf(sk[p] + 1e-6f) : 0.f;
                 }
             }
             if constexpr (!kBf16In) {  // fp32 v (in the ring) -> the tf32 K-major operand, zero past the end
