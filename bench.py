@@ -42,7 +42,8 @@ WORKLOADS = {
     "cfg3": "varlen 8192 tokens in 8 sequences (uniform split, one of length 1), H=32, dk=dv=128, bf16",
     "cfg4": "varlen skewed 8192 tokens in 32 sequences (one ~5000), H=32, d=128, extreme-value probes",
 }
-KERNEL_NAMES = ["schedule", "factors", "state_recurrence"]
+KERNEL_NAMES = {"fused": ["schedule", "plan", "fused"],
+                "split": ["schedule", "factors", "state_recurrence"]}
 
 
 def make_workload(name: str, seed: int, salt: int):
@@ -86,6 +87,8 @@ def _algorithmic_bytes(kernel: str, tokens: int, heads: int, dk: int, dv: int, n
         return th * (2 * dk * 2 + dv * 2 + dk * g_bytes + 4)
     if kernel == "state_recurrence":  # writes o; reads h0, writes hT
         return th * dv * 2 + 2 * nseq * heads * dk * dv * 4
+    if kernel == "fused":         # the whole path: both of the above
+        return _path_bytes(tokens, heads, dk, dv, nseq, g_bytes)
     return 0
 
 
@@ -361,6 +364,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pipeline", default="fused", choices=["fused", "split"],
+                    help="fused: factor production and state chains in one kernel (default); "
+                         "split: a factor kernel, then a state kernel")
     ap.add_argument("--workload", default="cfg2",
                     help="cfg2 (the headline workload), cfg2-gbf16 (bf16 gate), cfg3, cfg4, "
                          "cfg5-{fixed|varlen}-H{16|32|64}-{total}, "
@@ -391,6 +397,7 @@ def main():
     if world > 1 and rank == 0:
         torch.distributed.barrier()
     import gated_delta_rule_25_gb300 as kda
+    kda.set_pipeline(args.pipeline)
 
     salt = gen.fresh_salt() + rank
     x, desc = make_workload(args.workload, 0, salt)
@@ -401,6 +408,8 @@ def main():
     hT = torch.empty_like(xd.h0)
     ws = torch.empty(kda.workspace_size(B, T, H, D, D, nseq) + 256, dtype=torch.uint8, device=dev)
     nl = kda.launch_count(B, T, H, D, D, nseq)
+    pipeline = "fused" if kda.uses_fused(B, T, H, D, D, nseq) else "split"
+    names = KERNEL_NAMES[pipeline]
     stream = torch.cuda.current_stream(dev)
 
     def step(events=None):
@@ -528,7 +537,7 @@ def main():
     in_mb = sum(t.numel() * t.element_size() for t in (x.q, x.k, x.v, x.g, x.beta)) / 1e6
     ws_mb = ws.numel() / 1e6
     dom = int(np.argmax(per_kernel))
-    dom_name = KERNEL_NAMES[dom] if dom < len(KERNEL_NAMES) else f"kernel{dom}"
+    dom_name = names[dom] if dom < len(names) else f"kernel{dom}"
     gb = x.g.element_size()
     alg = _algorithmic_bytes(dom_name, x.tokens, H, D, D, nseq, gb)
     achieved = alg / (per_kernel[dom] * 1e-3) / 1e9
@@ -544,9 +553,9 @@ def main():
         "config": {"workload": desc, "name": args.workload, "tokens_per_step": x.tokens,
                    "heads": H, "dk": D, "dv": D,
                    "l2": f"no flush: {in_mb:.0f} MB of inputs and {ws_mb:.0f} MB of factors per step vs the 129 MB L2",
-                   "salt": salt},
+                   "salt": salt, "pipeline": pipeline},
         "gpu_launches": nl * args.steps,
-        "kernels_ms": {KERNEL_NAMES[j] if j < len(KERNEL_NAMES) else f"kernel{j}": per_kernel[j]
+        "kernels_ms": {names[j] if j < len(names) else f"kernel{j}": per_kernel[j]
                        for j in range(nl)},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": _traffic_for(dom_name, args.workload),

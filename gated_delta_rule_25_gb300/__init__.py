@@ -78,6 +78,12 @@ def load_library():
         lib.kda_decode.restype = i32
         lib.kda_status_string.argtypes = [i32]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_set_pipeline.argtypes = [i32]
+        lib.kda_set_pipeline.restype = None
+        lib.kda_get_pipeline.argtypes = []
+        lib.kda_get_pipeline.restype = i32
+        lib.kda_fwd_uses_fused.argtypes = [i32] * 6
+        lib.kda_fwd_uses_fused.restype = i32
         _lib = lib
         return lib
 
@@ -88,6 +94,28 @@ def workspace_size(B: int, T: int, H: int, dk: int, dv: int, num_seqs: int) -> i
 
 def launch_count(B: int, T: int, H: int, dk: int, dv: int, num_seqs: int) -> int:
     return int(load_library().kda_fwd_launch_count(B, T, H, dk, dv, num_seqs))
+
+
+PIPELINES = {"fused": 0, "split": 1}
+
+
+def set_pipeline(name: str) -> None:
+    """Selects the forward's pipeline, process-wide: "fused" (default; one
+    cooperative kernel producing factors and running the state chains at once,
+    where the sizes allow) or "split" (a factor kernel, then a state kernel)."""
+    if name not in PIPELINES:
+        raise ValueError(f"pipeline must be one of {sorted(PIPELINES)}, got {name!r}")
+    load_library().kda_set_pipeline(PIPELINES[name])
+
+
+def get_pipeline() -> str:
+    v = int(load_library().kda_get_pipeline())
+    return next(k for k, x in PIPELINES.items() if x == v)
+
+
+def uses_fused(B: int, T: int, H: int, dk: int, dv: int, num_seqs: int) -> bool:
+    """True if fwd takes the fused pipeline for these sizes (current setting, device)."""
+    return bool(load_library().kda_fwd_uses_fused(B, T, H, dk, dv, num_seqs))
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -244,7 +272,7 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
 
 
 __all__ = ["fwd", "fwd_noalloc", "workspace_size", "launch_count", "load_library", "KdaError",
-           "LIB_PATH"]
+           "LIB_PATH", "set_pipeline", "get_pipeline", "uses_fused"]
 
 
 def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,

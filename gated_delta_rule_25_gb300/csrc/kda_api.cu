@@ -1,5 +1,6 @@
 // C ABI of the KDA prefill forward: argument checks, workspace carving, launches.
 // Declarations and the contract are in include/kda.h.
+#include <atomic>
 #include <cmath>
 #include <map>
 #include <mutex>
@@ -43,6 +44,8 @@ int num_sms() {
 
 namespace {
 
+std::atomic<int> g_pipeline{KDA_PIPELINE_FUSED};
+
 bool valid_head_dim(int x) { return x == 64 || x == 128; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -77,7 +80,19 @@ size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs)
 
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
     (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)num_seqs;
-    return 3;  // schedule, factors, state recurrence
+    return 3;  // schedule, plan, fused; or schedule, factors, state recurrence
+}
+
+void kda_set_pipeline(kda_pipeline pipeline) {
+    g_pipeline.store(pipeline == KDA_PIPELINE_SPLIT ? KDA_PIPELINE_SPLIT : KDA_PIPELINE_FUSED);
+}
+
+kda_pipeline kda_get_pipeline(void) { return static_cast<kda_pipeline>(g_pipeline.load()); }
+
+int kda_fwd_uses_fused(int B, int T, int H, int dk, int dv, int num_seqs) {
+    kda::Dims d;
+    if (make_dims(B, T, H, dk, dv, num_seqs, B == 1 && num_seqs != B, d) != KDA_OK) return 0;
+    return g_pipeline.load() == KDA_PIPELINE_FUSED && kda::fused_grid(d) > 0 ? 1 : 0;
 }
 
 }  // extern "C"
@@ -117,9 +132,20 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         if (!events) return true;
         return cudaEventRecord(static_cast<cudaEvent_t>(events[ev++]), s) == cudaSuccess;
     };
+    const bool gbf = g_dtype == KDA_BF16;
+    const int grid = g_pipeline.load() == KDA_PIPELINE_FUSED ? kda::fused_grid(d) : 0;
+    if (grid > 0) {
+        if (!mark() || kda::launch_schedule_fused(d, cu_seqlens, ws, grid, kda::fused_ratio(d, bf16), s) !=
+                           cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (!mark() || kda::launch_plan(d, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark()) return KDA_ERR_CUDA;
+        const cudaError_t ce = kda::launch_fused(d, bf16, gbf, q, k, v, g, beta, h0, scale, o, hT, ws, s);
+        if (ce != cudaSuccess || !mark()) return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
     if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
-    if (!mark() || kda::launch_prep_tc(d, bf16, g_dtype == KDA_BF16, q, k, v, g, beta, ws, s) !=
-                       cudaSuccess)
+    if (!mark() || kda::launch_prep_tc(d, bf16, gbf, q, k, v, g, beta, ws, s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (!mark()) return KDA_ERR_CUDA;
     const cudaError_t ce = kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);

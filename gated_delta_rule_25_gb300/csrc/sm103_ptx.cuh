@@ -60,6 +60,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // No healthy wait in these kernels comes near this (nanoseconds).
 constexpr uint64_t kWaitNs = 500ull * 1000 * 1000;
 
+// Tests the phase without sleeping (for waits on a latency-critical path).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait_or_abort's spinning form: polls without sleeping (checking *abort and
+// the time every 64 polls), for the short waits on a chain of dependent steps.
+__device__ __forceinline__ bool mbar_spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort);
+
 // Waits for the phase with the given parity; gives up (false) after kWaitNs, or
 // at once when another thread of the CTA has raised *abort.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
@@ -70,6 +87,19 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
         if ((i & 3u) == 3u) {  // each failed test may have slept: check often
             if (*abort) return false;
             uint64_t t = globaltimer_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kWaitNs) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_spin_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u) {
+            if (*abort) return false;
+            const uint64_t t = globaltimer_ns();
             if (t0 == 0) t0 = t;
             else if (t - t0 > kWaitNs) return false;
         }
@@ -222,6 +252,27 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A in tensor memory (row m in lane m, K along
+// the columns: one tf32 or two bf16 elements per 32-bit column), B by descriptor.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
 // The two forms of the MMA with a constant accumulate flag.
 __device__ __forceinline__ void mma_bf16_first(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t idesc) {
@@ -272,6 +323,91 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bits, 16 (8) consecutive columns from this warp's 32 threads:
+// thread i writes lane (warp's lane quarter base + i), columns [col, col + 16 (8)).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+          "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+          "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+// Waits until this thread's tensor-memory stores are done (before the MMAs that
+// read them are issued, after a thread barrier).
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- flags between CTAs
+// Publishes what this CTA wrote to global memory (the other threads' stores are
+// ordered before this call by a CTA barrier): a proxy fence, so that bulk copies in
+// other CTAs see the data, then *flag = 1 with release semantics at GPU scope.
+__device__ __forceinline__ void flag_publish(uint32_t* flag) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// After relaxed loads that saw flags set by flag_publish: makes them acquire (the
+// fence-acquire pattern) and orders the published data before this thread's later
+// bulk copies.
+__device__ __forceinline__ void fence_acquire_for_bulk() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits (relaxed loads) until *flag != 0; the caller then calls
+// fence_acquire_for_bulk.  False after kWaitNs, or at once when *abort or *error is
+// raised.
+__device__ __forceinline__ bool flag_spin(const uint32_t* flag, const volatile uint32_t* error,
+                                          volatile int* abort) {
+    uint64_t t0 = 0;
+    for (;;) {
+        if (ld_relaxed_gpu(flag) != 0) return true;
+        if (*abort || *error) return false;
+        const uint64_t t = globaltimer_ns();
+        if (t0 == 0) t0 = t;
+        else if (t - t0 > kWaitNs) return false;
+        __nanosleep(100);
+    }
+}
+
+// Waits until *flag != 0 (acquire, GPU scope), then a proxy fence, so that this
+// thread's later bulk copies read what the flag published.  Gives up (false) after
+// kWaitNs, or at once when *abort (this CTA) or *error (the device error word, set
+// by any CTA) is raised.
+__device__ __forceinline__ bool flag_wait(const uint32_t* flag, const volatile uint32_t* error,
+                                          volatile int* abort) {
+    uint64_t t0 = 0;
+    for (;;) {
+        if (ld_acquire_gpu(flag) != 0) break;
+        if (*abort || *error) return false;
+        const uint64_t t = globaltimer_ns();
+        if (t0 == 0) t0 = t;
+        else if (t - t0 > kWaitNs) return false;
+        __nanosleep(100);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 }  // namespace ptx

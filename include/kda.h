@@ -103,7 +103,8 @@ kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* d
 /* Static, human-readable name of a status. */
 const char* kda_status_string(kda_status status);
 
-/* Number of kernel launches kda_fwd enqueues for these sizes (for launch counts). */
+/* Number of kernel launches kda_fwd enqueues for these sizes (for launch counts):
+ * 3 in either pipeline (schedule, plan, fused; or schedule, factors, state). */
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /*
@@ -136,6 +137,28 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
                             void* o, float* hT,
                             void* workspace, size_t workspace_bytes, kda_stream_t stream,
                             void* const* events);
+
+/*
+ * Pipelines of the forward (both compute the same operation; their kernels differ,
+ * so results may differ in the last bits):
+ *   KDA_PIPELINE_FUSED (default): a schedule kernel, a plan kernel, then one
+ *     persistent cooperative kernel in which some CTAs produce the per-chunk
+ *     factors and the others run the state recurrence over whole (sequence, head)
+ *     chains, consuming each chunk's factors as soon as they are published.  Taken
+ *     for batches of at most 2048 sequences and 65536 (sequence, head) pairs on a
+ *     device with at least 2 SMs; other sizes take the split pipeline.
+ *   KDA_PIPELINE_SPLIT: a schedule kernel, a factor kernel over every chunk, then
+ *     a state kernel over (sequence, head, value-column tile) chains.
+ * The setting is process-wide (an atomic; calls already enqueued keep theirs); it
+ * exists for measurement and testing.
+ */
+typedef enum { KDA_PIPELINE_FUSED = 0, KDA_PIPELINE_SPLIT = 1 } kda_pipeline;
+void kda_set_pipeline(kda_pipeline pipeline);
+kda_pipeline kda_get_pipeline(void);
+
+/* 1 if kda_fwd takes the fused pipeline for these sizes under the current setting
+ * (on the current device), else 0. */
+int kda_fwd_uses_fused(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /* Size of the device scratch array built into the library for kda_fwd_noalloc. */
 #define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
