@@ -42,7 +42,7 @@ WORKLOADS = {
     "cfg3": "varlen 8192 tokens in 8 sequences (uniform split, one of length 1), H=32, dk=dv=128, bf16",
     "cfg4": "varlen skewed 8192 tokens in 32 sequences (one ~5000), H=32, d=128, extreme-value probes",
 }
-KERNEL_NAMES = {"fused": ["schedule", "plan", "fused"],
+KERNEL_NAMES = {"fused": ["schedule", "fused"],
                 "split": ["schedule", "factors", "state_recurrence"]}
 
 

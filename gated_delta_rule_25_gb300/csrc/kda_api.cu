@@ -79,8 +79,8 @@ size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs)
 }
 
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
-    (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)num_seqs;
-    return 3;  // schedule, plan, fused; or schedule, factors, state recurrence
+    // schedule, fused; or schedule, factors, state recurrence
+    return kda_fwd_uses_fused(B, T, H, dk, dv, num_seqs) ? 2 : 3;
 }
 
 void kda_set_pipeline(kda_pipeline pipeline) {
@@ -138,7 +138,6 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         if (!mark() || kda::launch_schedule_fused(d, cu_seqlens, ws, grid, kda::fused_ratio(d, bf16), s) !=
                            cudaSuccess)
             return KDA_ERR_CUDA;
-        if (!mark() || kda::launch_plan(d, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
         if (!mark()) return KDA_ERR_CUDA;
         const cudaError_t ce = kda::launch_fused(d, bf16, gbf, q, k, v, g, beta, h0, scale, o, hT, ws, s);
         if (ce != cudaSuccess || !mark()) return KDA_ERR_CUDA;

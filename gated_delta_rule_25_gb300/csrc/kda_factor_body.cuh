@@ -260,7 +260,9 @@ __device__ __forceinline__ void issue_level_pair(uint32_t tmem, const uint8_t* b
 // kernel's dynamic shared memory (1024-byte aligned, sizeof(FactorSmem) bytes).
 // UT: u leaves as [64/4][dv][4] fp32 (a float4 of 4 consecutive rows per value
 // column, columns fastest: a warp of consecutive columns reads 4 rows of each with
-// one contiguous 512-byte load) instead of the slabbed U0 layout.
+// one contiguous 512-byte load) instead of the slabbed U0 layout; with bf16 inputs
+// and dv = 128 the product itself is transposed (u^T, M = dv), so that every
+// thread leaves with four 16-byte stores.
 template <int DK, int DV, typename TIn, typename TG, bool UT>
 __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tmq, const CUtensorMap* tmk,
                                             const CUtensorMap* tmv, const CUtensorMap* tmg,
@@ -270,6 +272,8 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
     using Sm = FactorSmem<DK, DV, TIn>;
     using Cf = FactorCfg<DK, DV, TIn>;
     constexpr bool kBf16In = sizeof(TIn) == 2;
+    // u^T straight from the tensor cores (bf16 inputs, dv = 128: the M = dv product)
+    constexpr bool kUTmma = UT && kBf16In && DV == 128;
     constexpr int CPT = DK / 64;  // channels per thread in the level phase
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
 
@@ -381,6 +385,18 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
                 *reinterpret_cast<uint4*>(wq_dst + mn_off<DK>(16 * cg, cc)) = pack8(y0);
                 *reinterpret_cast<uint4*>(wq_dst + mn_off<DK>(16 * cg + 8, cc)) = pack8(y1);
             }
+        }
+        if constexpr (kUTmma) {
+            // u^T: lane = value column 32 q + lane, columns = chunk rows 16 cg ..: four
+            // float4 of 4 rows each, a warp's 32 columns contiguous ([64/4][dv][4])
+            float x[16];
+            ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + reg + 64 + 16 * cg, x);
+            ptx::tmem_ld_wait();
+            float4* const dst = reinterpret_cast<float4*>(u_dst) + 4 * cg * DV + 32 * q + lane;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+                dst[k4 * DV] = make_float4(x[4 * k4], x[4 * k4 + 1], x[4 * k4 + 2], x[4 * k4 + 3]);
+            return;
         }
         // u: lanes 0-15 of each quarter = chunk rows 16 q .., columns DV/4 per warp
         {
@@ -967,7 +983,16 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
         if (okv && !*abort && kBf16In) {
             const uint64_t xd[2] = {ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXop), 1024, 128),
                                     ptx::smem_desc(ptx::smem_u32(sm.ring + kOffXlo), 1024, 128)};
-            if (tid == 0) {  // u = (X Diag(beta)) v, hi then lo
+            if (tid == 0 && kUTmma) {  // u^T = v^T (X Diag(beta))^T (M = dv, v as an M-major A), hi then lo
+                constexpr uint32_t id_u = ptx::idesc_bf16(DV, kChunk) | kAMajorMN;
+                const uint64_t vb = ptx::smem_desc(ptx::smem_u32(sm.vs), 128, 1024);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 16; ++kk)
+                        ptx::mma_bf16(tmem + reg + 64, vb + (uint64_t)(kk * 16), xd[part] + (uint64_t)(kk * 128),
+                                      id_u, part > 0 || kk > 0);
+            } else if (tid == 0) {  // u = (X Diag(beta)) v, hi then lo
                 constexpr uint32_t id_u = ptx::idesc_bf16(kChunk, DV) | kBMajorMN;
                 const uint64_t vb = ptx::smem_desc(ptx::smem_u32(sm.vs), 128, 1024);
 #pragma unroll
@@ -1006,16 +1031,19 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
         *reinterpret_cast<uint4*>(&gP[op_index(i, 8 * jb, kChunk)]) = pack8(x);
     }
 
+    // with ready flags, a CTA's first item leaves at once (its consumers start on it)
+    const bool first_now = plan.ready != nullptr && !have_prev;
     if (have_prev) epilogue(prev_reg, prev_wq, prev_u);
     if (!ptx::mbar_wait_or_abort(&sm.wu_bar, par, abort)) raise_timeout(ws, abort);
     ptx::tc_fence_after();
+    if (first_now) epilogue(reg, gWQ, gU);
     if (tid == 0 && next.h < H && !*abort) {  // v (and, for fp32 inputs, everything) of the next item
         if (kBf16In) issue_v(next, rows_next);
         else issue_qkg(next, rows_next);
     }
     const bool publish_prev = have_prev;  // the previous item's last parts left above
     const Item published = prev_item;
-    have_prev = true;
+    have_prev = !first_now;
     prev_reg = reg;
     prev_wq = gWQ;
     prev_u = gU;
@@ -1023,8 +1051,10 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
     ptx::tc_fence_before();
     __syncthreads();
     if (*abort) break;
-    if (plan.ready && publish_prev && tid == 0)
-        ptx::flag_publish(plan.ready + (size_t)published.c * H + published.h);
+    if (plan.ready && tid == 0) {
+        if (publish_prev) ptx::flag_publish(plan.ready + (size_t)published.c * H + published.h);
+        if (first_now) ptx::flag_publish(plan.ready + (size_t)item.c * H + item.h);
+    }
     par ^= 1u;
     item = next;
     rows_cur = rows_next;

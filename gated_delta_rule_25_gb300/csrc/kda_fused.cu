@@ -33,8 +33,9 @@ constexpr int kCDK = 128, kCDV = 128;  // the fused pipeline's head dimensions
 
 // Tensor-memory columns of a chain CTA (512 allocated; lane = value column n).
 constexpr uint32_t kTS = 0;     // S^T in bf16 (GEMM1's A): channel c at column c / 2
-constexpr uint32_t kTD1 = 64;   // D1^T[b] at 64 + 128 b: columns 0-63 (w S)^T, then U^T in
-                                // tf32 (GEMM2's A); columns 64-127 the output O^T
+constexpr uint32_t kTXa = 64;   // (w S)^T over channels 0-63, then U^T in tf32 (GEMM2's A)
+constexpr uint32_t kTXb = 128;  // (w S)^T over channels 64-127
+constexpr uint32_t kTO = 192;   // O^T[b] at 192 + 64 b: (QG S)^T + U^T P^T (the output)
 constexpr uint32_t kTD2 = 320;  // D2^T = U^T KT^T, column = channel
 constexpr uint32_t kTUB = 448;  // U^T in bf16 (GEMM3's A), 32 columns
 
@@ -62,6 +63,7 @@ __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 // the CTA takes chains first, first + nc, ...; j is the step (chunk) in the chain.
 struct ChainPos {
     int r, s, h, c0, len, j;
+    int tok0, ntok;  // the sequence's first token row and its tokens
 };
 
 template <typename TOut>
@@ -93,11 +95,11 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         ptx::mbar_init(&sm.u_full, 1);
         ptx::mbar_init(&sm.p_full[0], 1);
         ptx::mbar_init(&sm.p_full[1], 1);
-        ptx::mbar_init(&sm.d1, 1);
+        ptx::mbar_init(&sm.d1, 2);  // the two halves of (w S)^T
         ptx::mbar_init(&sm.d2, 1);
         ptx::mbar_init(&sm.d3[0], 1);
         ptx::mbar_init(&sm.d3[1], 1);
-        ptx::mbar_init(&sm.fin, 2);  // both issuing threads
+        ptx::mbar_init(&sm.fin, 3);  // the three issuing threads
         sm.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -111,12 +113,16 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     const uint32_t tmem = sm.tmem;
 
     auto chain_at = [&](int r) {
-        ChainPos p{r, 0, 0, 0, 0, 0};
+        ChainPos p{r, 0, 0, 0, 0, 0, 0, 0};
         if (r < R) {
             p.h = r % H;
             p.s = order[r / H];
             p.c0 = seq_first[p.s];
             p.len = seq_first[p.s + 1] - p.c0;
+            if (p.len > 0) {
+                p.tok0 = chunk_tab[p.c0].y;
+                p.ntok = kChunk * (p.len - 1) + chunk_tab[p.c0 + p.len - 1].z;
+            }
         }
         return p;
     };
@@ -134,8 +140,9 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     };
     auto flag_of = [&](const ChainPos& p) { return ready + (size_t)(p.c0 + p.j) * H + p.h; };
     // The copy thread (lane 0 of warp 2) acquires the ready flags and issues every
-    // bulk copy; thread 0 issues GEMM1 and GEMM2, thread 32 GEMM3.  Copies are
-    // counted so that a CTA that leaves early can wait for those still in flight.
+    // bulk copy; threads 0 and 32 issue the serial part of GEMM1 (thread 0 also
+    // GEMM2), thread 96 its output part and GEMM3.  Copies are counted so that a CTA
+    // that leaves early can wait for those still in flight.
     constexpr int kCopier = 64;
     uint32_t n_wq = 0, n_kt = 0, n_u = 0, n_p0 = 0, n_p1 = 0;
     auto issue_wq = [&](const ChainPos& p) {
@@ -220,7 +227,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     int4 tile_out = make_int4(0, 0, 0, 0);  // {first token row, rows, head, staged?} of the tile
     auto out_stage = [&](uint32_t buf) {    // output of the step in D1^T[buf]: rows 16 g ..
         float acc[16];
-        ptx::tmem_ld16(tmem + lb + kTD1 + 128 * buf + 64 + 16 * g, acc);
+        ptx::tmem_ld16(tmem + lb + kTO + 64 * buf + 16 * g, acc);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) store_out(otile + (16 * g + i) * DV + n, scale * acc[i]);
@@ -243,7 +250,6 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         const ChainPos nxt = next_of(cur);
         const bool nv = nxt.len > 0;
         const uint32_t b = gj & 1u;
-        const int4 chk = chunk_tab[cur.c0 + cur.j];
         // -------- a new chain: its initial state into S^T and the bf16 copy
         if (cur.j == 0) {
             const size_t base = ((size_t)cur.s * H + cur.h) * DK * DV;
@@ -258,17 +264,33 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
             ok = __syncthreads_and(ok && !*abort);
             if (!ok) break;
         }
-        // -------- GEMM1: D1^T[b] = S^T [w; QG]^T
-        if (tid == 0) {
+        // -------- GEMM1, the part on the serial path: (w S)^T = S^T w^T, its two
+        //          halves over the channels issued side by side (threads 0 and 32)
+        if (tid == 0 || tid == 32) {
             if (ptx::mbar_spin_or_abort(&sm.wq_full, b, abort)) {
                 ptx::tc_fence_after();
-                constexpr uint32_t id1 = ptx::idesc_bf16(128, 128) | kBMajorMN;
+                constexpr uint32_t idw = ptx::idesc_bf16(128, kChunk) | kBMajorMN;
                 const uint64_t bd = ptx::smem_desc(ptx::smem_u32(sm.WQ), 128, (DK / 8) * 128);
+                const int k0 = tid == 0 ? 0 : DK / 32;
+#pragma unroll
+                for (int kk = 0; kk < DK / 32; ++kk)
+                    ptx::mma_bf16_ta(tmem + (tid == 0 ? kTXa : kTXb), tmem + kTS + 8 * (k0 + kk),
+                                     bd + (uint64_t)(((k0 + kk) * 256) >> 4), idw, kk > 0);
+                ptx::mma_commit(&sm.d1);
+            } else {
+                chain_raise(ws, abort);
+            }
+        } else if (tid == 96) {
+            // GEMM1, the output part: O^T[b] = S^T QG^T (its B: rows 64-127 of [w; QG]);
+            // issued beside the serial part (the thread would wait for d1 meanwhile)
+            if (ptx::mbar_spin_or_abort(&sm.wq_full, b, abort)) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idq = ptx::idesc_bf16(128, kChunk) | kBMajorMN;
+                const uint64_t bd = ptx::smem_desc(ptx::smem_u32(sm.WQ) + kChunk * DK * 2, 128, (DK / 8) * 128);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk)
-                    ptx::mma_bf16_ta(tmem + kTD1 + 128 * b, tmem + kTS + 8 * kk, bd + (uint64_t)((kk * 256) >> 4),
-                                     id1, kk > 0);
-                ptx::mma_commit(&sm.d1);
+                    ptx::mma_bf16_ta(tmem + kTO + 64 * b, tmem + kTS + 8 * kk, bd + (uint64_t)((kk * 256) >> 4),
+                                     idq, kk > 0);
             } else {
                 chain_raise(ws, abort);
             }
@@ -282,24 +304,29 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         okl = __all_sync(0xffffffffu, okl);
         if (okl) {
             ptx::tc_fence_after();
-            float acc[16];
-            ptx::tmem_ld16(tmem + lb + kTD1 + 128 * b + 16 * g, acc);
             float4 un[4];  // u: value column n, rows 16 g .. 16 g + 15
             const float4* u0 = reinterpret_cast<const float4*>(sm.U0) + 4 * g * DV + n;
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) un[k2] = u0[k2 * DV];
-            ptx::tmem_ld_wait();
-            uint32_t ut[16], ub[8];
+            float uu[16];
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
-                ut[4 * k2] = __float_as_uint(un[k2].x - acc[4 * k2]);
-                ut[4 * k2 + 1] = __float_as_uint(un[k2].y - acc[4 * k2 + 1]);
-                ut[4 * k2 + 2] = __float_as_uint(un[k2].z - acc[4 * k2 + 2]);
-                ut[4 * k2 + 3] = __float_as_uint(un[k2].w - acc[4 * k2 + 3]);
+                uu[4 * k2] = un[k2].x; uu[4 * k2 + 1] = un[k2].y; uu[4 * k2 + 2] = un[k2].z; uu[4 * k2 + 3] = un[k2].w;
             }
 #pragma unroll
+            for (int half = 0; half < 2; ++half) {  // minus both halves of (w S)^T
+                float acc[16];
+                ptx::tmem_ld16(tmem + lb + (half ? kTXb : kTXa) + 16 * g, acc);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) uu[e] -= acc[e];
+            }
+            uint32_t ut[16], ub[8];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ut[e] = __float_as_uint(uu[e]);
+#pragma unroll
             for (int i = 0; i < 8; ++i) ub[i] = pack_bf16(__uint_as_float(ut[2 * i]), __uint_as_float(ut[2 * i + 1]));
-            ptx::tmem_st16(tmem + lb + kTD1 + 128 * b + 16 * g, ut);
+            ptx::tmem_st16(tmem + lb + kTXa + 16 * g, ut);
             ptx::tmem_st8(tmem + lb + kTUB + 8 * g, ub);
             ptx::tmem_st_wait();
         }
@@ -327,20 +354,20 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
                 const uint64_t bd = ptx::smem_desc(ptx::smem_u32(sm.KT), (DK / 8) * 128, 128);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 8; ++kk)
-                    ptx::mma_tf32_ta(tmem + kTD2, tmem + kTD1 + 128 * b + 8 * kk,
+                    ptx::mma_tf32_ta(tmem + kTD2, tmem + kTXa + 8 * kk,
                                      bd + (uint64_t)((kk * 2 * (DK / 8) * 128) >> 4), id2, kk > 0);
                 ptx::mma_commit(&sm.d2);
             } else {
                 chain_raise(ws, abort);
             }
-        } else if (tid == 32) {
+        } else if (tid == 96) {
             if (ptx::mbar_spin_or_abort(&sm.p_full[b], (gj >> 1) & 1u, abort)) {
                 ptx::tc_fence_after();
                 constexpr uint32_t id3 = ptx::idesc_bf16(128, kChunk);
                 const uint64_t bd = ptx::smem_desc(ptx::smem_u32(sm.P[b]), 1024, 128);
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk)
-                    ptx::mma_bf16_ta(tmem + kTD1 + 128 * b + 64, tmem + kTUB + 8 * kk,
+                    ptx::mma_bf16_ta(tmem + kTO + 64 * b, tmem + kTUB + 8 * kk,
                                      bd + (uint64_t)((kk * 2048) >> 4), id3, true);
                 ptx::mma_commit(&sm.d3[b]);
             } else {
@@ -384,7 +411,10 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         }
         ptx::tc_fence_before();
         ok = __syncthreads_and(ok && okd);
-        prev_out = make_int4(chk.y, chk.z, cur.h, 0);
+        {
+            const int rows = cur.ntok - kChunk * cur.j;
+            prev_out = make_int4(cur.tok0 + kChunk * cur.j, rows < kChunk ? rows : kChunk, cur.h, 0);
+        }
         have_prev = true;
         ++gj;
         cur = nxt;
@@ -426,7 +456,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
             if (n_p0) ptx::mbar_wait_or_abort(&sm.p_full[0], (n_p0 - 1) & 1u, &never);
             if (n_p1) ptx::mbar_wait_or_abort(&sm.p_full[1], (n_p1 - 1) & 1u, &never);
         }
-        if (tid == 0 || tid == 32) ptx::mma_commit(&sm.fin);
+        if (tid == 0 || tid == 32 || tid == 96) ptx::mma_commit(&sm.fin);
         if (tid == 0) ptx::mbar_wait_or_abort(&sm.fin, 0, &never);
     }
     ptx::tc_fence_before();

@@ -5,8 +5,6 @@
 //   seq_first       int32[N + 1]: index of the first chunk of each sequence
 //   order           int32[N]:     sequences by decreasing chunk count (longest first)
 //   chunks          int4[Cmax]:   {sequence, first token row, valid rows L, 0}
-//   rank_first      int32[N + 1]: chunks of the sequences ranked before each rank
-//                                 (prefix sum in longest-first order)
 //   plist           int32[Cmax*H]: the order in which the fused pipeline produces
 //                                 (chunk, head) items, each as chunk * H + head
 //   ready           u32[Cmax*H]:  per (chunk, head): 1 once its factors are published
@@ -86,7 +84,7 @@ struct FactorLayout {
 };
 
 struct WsLayout {
-    size_t header, seq_first, order, chunks, rank_first, plist, ready, factors, total;
+    size_t header, seq_first, order, chunks, plist, ready, factors, total;
     long long cmax;
     size_t factor_bytes;
     __host__ __device__ explicit WsLayout(const Dims& d) {
@@ -98,7 +96,6 @@ struct WsLayout {
         seq_first = off; off += align256(size_t(d.N + 1) * 4);
         order = off;     off += align256(size_t(d.N) * 4);
         chunks = off;    off += align256(size_t(cmax) * 16);
-        rank_first = off; off += align256(size_t(d.N + 1) * 4);
         plist = off;     off += align256(size_t(cmax) * d.H * 4);
         ready = off;     off += align256(size_t(cmax) * d.H * 4);
         factors = off;   off += size_t(cmax) * d.H * f.bytes;
@@ -149,15 +146,13 @@ cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, bool g_bf16, const void
 cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                          float* hT, uint8_t* ws, cudaStream_t stream);
 
-// Fused pipeline.  The schedule kernel, given fused_grid > 0, also ranks chain
-// lengths into rank_first and picks how many of the fused kernel's fused_grid CTAs
-// run state chains (production_ratio: the time to produce one item's factors over
-// the time of one chain step); the plan kernel lays out the production order and
-// clears the ready flags; the fused kernel produces factors on the other CTAs while
-// the chain CTAs consume them as they are published.
+// Fused pipeline.  The schedule kernel, given fused_grid > 0, also picks how many of
+// the fused kernel's fused_grid CTAs run state chains (production_ratio: the time to
+// produce one item's factors over the time of one chain step), lays out the
+// production order and clears the ready flags; the fused kernel produces factors on
+// the other CTAs while the chain CTAs consume them as they are published.
 cudaError_t launch_schedule_fused(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
                                   int fused_grid, float production_ratio, cudaStream_t stream);
-cudaError_t launch_plan(const Dims& d, uint8_t* ws, cudaStream_t stream);
 cudaError_t launch_fused(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,
                          const void* v, const void* g, const float* beta, const float* h0,
                          float scale, void* o, float* hT, uint8_t* ws, cudaStream_t stream);

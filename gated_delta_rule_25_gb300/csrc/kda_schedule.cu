@@ -12,7 +12,6 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kPlanThreads = 256;
 
 __device__ inline void seq_span(const Dims& d, const int32_t* cu, int s, long long& row0,
                                 int& len) {
@@ -54,9 +53,9 @@ __device__ int block_scan(int x, int* warp_sums, int* carry) {
     return excl;
 }
 
-// fused_grid > 0: also rank_first and Header::n_chain for a fused kernel of
-// fused_grid CTAs (needs d.N <= kRankMax).  ratio: the time to produce one item's
-// factors over the time of one chain step.
+// fused_grid > 0: also Header::n_chain, the production order and cleared ready
+// flags for a fused kernel of fused_grid CTAs (needs d.N <= kRankMax).  ratio: the
+// time to produce one item's factors over the time of one chain step.
 __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_t* cu,
                                                             uint8_t* ws, int fused_grid,
                                                             float ratio) {
@@ -67,6 +66,11 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     __shared__ int bad;
     __shared__ int warp_sums[kThreads / 32];
     __shared__ int carry;
+    // Up to kRankMax sequences the tables are built in shared memory (and copied
+    // out), so that no step reads back global memory this kernel has just written.
+    __shared__ int s_first[kRankMax + 1], s_order[kRankMax], s_rf[kRankMax + 1];
+    const bool small = d.N <= kRankMax;
+    int* const sf = small ? s_first : seq_first;  // first chunk of each sequence
     const int tid = threadIdx.x;
     if (tid == 0) {
         bad = 0;
@@ -121,136 +125,139 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         __syncthreads();
         int excl = carry + x - n + ((tid >> 5) ? warp_sums[(tid >> 5) - 1] : 0);
         if (s < d.N) {
-            seq_first[s] = excl;
-            long long r0;
-            int len;
-            seq_span(d, cu, s, r0, len);
-            for (int j = 0; j < n; ++j) {
-                int rows = len - j * kChunk;
-                chunks[excl + j] = make_int4(s, (int)(r0 + (long long)j * kChunk),
-                                             rows < kChunk ? rows : kChunk, j);
-            }
+            sf[s] = excl;
+            if (small) seq_first[s] = excl;
         }
         __syncthreads();
         if (tid == 0) carry += warp_sums[kThreads / 32 - 1];
         __syncthreads();
     }
     if (tid == 0) {
-        seq_first[d.N] = carry;
+        sf[d.N] = carry;
+        if (small) seq_first[d.N] = carry;
         hdr->error = 0;
         hdr->total_chunks = carry;
         hdr->next_item = 0;
         hdr->n_chain = 0;
+    }
+    __syncthreads();
+    // the chunk table, one thread per chunk: its sequence is the last one whose first
+    // chunk is <= c
+    for (int c = tid; c < carry; c += kThreads) {
+        int lo = 0, hi = d.N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sf[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        long long r0;
+        int len;
+        seq_span(d, cu, lo, r0, len);
+        const int j = c - sf[lo];
+        const int rows = len - j * kChunk;
+        chunks[c] = make_int4(lo, (int)(r0 + (long long)j * kChunk), rows < kChunk ? rows : kChunk, j);
     }
     // Longest chains first: the state kernel maps its CTAs through this order so
     // that a dominant sequence starts at once instead of after the short ones.
     // Stable rank by chunk count for up to kRankMax sequences, identity beyond.
     int32_t* order = reinterpret_cast<int32_t*>(ws + L.order);
     __syncthreads();
-    if (d.N <= kRankMax) {
+    if (small) {
         for (int s = tid; s < d.N; s += kThreads) {
-            const int ns = seq_first[s + 1] - seq_first[s];
+            const int ns = sf[s + 1] - sf[s];
             int rank = 0;
             for (int t = 0; t < d.N; ++t) {
-                const int nt = seq_first[t + 1] - seq_first[t];
+                const int nt = sf[t + 1] - sf[t];
                 rank += (nt > ns) || (nt == ns && t < s);
             }
             order[rank] = s;
+            s_order[rank] = s;
         }
     } else {
         for (int s = tid; s < d.N; s += kThreads) order[s] = s;
     }
-    if (fused_grid <= 0 || d.N > kRankMax) return;
+    if (fused_grid <= 0 || !small) return;
 
     // ---- fused pipeline.  Chain r = rank * H + head (one chain per sequence and
     // head); chain CTA x takes chains x, x + n_chain, ... (round k = r / n_chain), so
-    // CTA 0 runs the longest chain of every round.  rank_first: chunks before each
-    // rank in longest-first order.
-    int32_t* rank_first = reinterpret_cast<int32_t*>(ws + L.rank_first);
-    __syncthreads();  // order complete
+    // CTA 0 runs the longest chain of every round.  rf: chunks before each rank.
+    __syncthreads();  // s_order complete
+    auto rc0 = [&](int rk) { return s_first[s_order[rk]]; };
+    auto rcntf = [&](int rk) { const int sq = s_order[rk]; return s_first[sq + 1] - s_first[sq]; };
+    int* const rf = s_rf;
     if (tid == 0) carry = 0;
     __syncthreads();
     for (int base = 0; base < d.N; base += kThreads) {
         const int rk = base + tid;
-        const int n = rk < d.N ? seq_first[order[rk] + 1] - seq_first[order[rk]] : 0;
-        const int e = block_scan(n, warp_sums, &carry);
-        if (rk < d.N) rank_first[rk] = e;
+        const int e = block_scan(rk < d.N ? rcntf(rk) : 0, warp_sums, &carry);
+        if (rk < d.N) rf[rk] = e;
     }
-    if (tid == 0) rank_first[d.N] = carry;
+    if (tid == 0) rf[d.N] = carry;
     __syncthreads();
     // n_chain c minimises max(chain steps of CTA 0, ratio * items / (grid - c)):
     // the chain CTAs' critical path against the factor CTAs' share of the items.
     __shared__ unsigned long long best;
     if (tid == 0) best = ~0ull;
     __syncthreads();
-    const long long R = (long long)d.N * d.H, items = (long long)carry * d.H;
+    const int H = d.H;
+    const long long R = (long long)d.N * H, items = (long long)carry * H;
     const long long cmax = R < fused_grid - 1 ? R : fused_grid - 1;
     for (long long c = tid + 1; c <= cmax; c += kThreads) {
         const long long rounds = (R + c - 1) / c;
         if (rounds > 1024) continue;
         long long steps = 0;
-        for (long long k = 0; k < rounds; ++k) {
-            const int rk = (int)(k * c / d.H);
-            steps += rank_first[rk + 1] - rank_first[rk];
-        }
+        for (long long k = 0; k < rounds; ++k) steps += rcntf((int)(k * c / H));
         const float cost = fmaxf((float)steps, ratio * (float)items / (float)(fused_grid - c));
         atomicMin(&best, ((unsigned long long)__float_as_uint(cost) << 32) | (unsigned long long)c);
     }
     __syncthreads();
-    if (tid == 0) hdr->n_chain = best == ~0ull ? (int)cmax : (int)(best & 0xffffffffull);
-}
+    const long long nc = best == ~0ull ? cmax : (long long)(best & 0xffffffffull);
+    if (tid == 0) hdr->n_chain = (int)nc;
 
-// Production order of the fused pipeline: the items of round k (its chains' chunks)
-// come before those of round k + 1, and inside a round step j of every chain comes
-// before step j + 1 (chains in the round's order), so that the chain CTAs find
-// their next chunk published early.  One thread per item, taken in chain order;
-// also clears the item's ready flag.
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Dims d, uint8_t* ws) {
-    const WsLayout L(d);
-    const Header* hdr = reinterpret_cast<const Header*>(ws + L.header);
-    const int nc = hdr->n_chain;
-    if (nc <= 0 || hdr->error) return;
-    const int H = d.H;
-    const int32_t* rf = reinterpret_cast<const int32_t*>(ws + L.rank_first);
-    const int32_t* seq_first = reinterpret_cast<const int32_t*>(ws + L.seq_first);
-    const int32_t* order = reinterpret_cast<const int32_t*>(ws + L.order);
+    // Production order: the items of round k (its chains' chunks) come before those
+    // of round k + 1, and inside a round step j of every chain comes before step
+    // j + 1 (chains in the round's order), so that the chain CTAs find their next
+    // chunk published early.  Items are taken in chain order (t = the item's index
+    // there); each also clears its ready flag.  32-bit arithmetic throughout (items
+    // and chains stay far below 2^31); the searches run over ranks, whose counts do
+    // not increase.
     int32_t* plist = reinterpret_cast<int32_t*>(ws + L.plist);
     uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
-    const long long items = (long long)hdr->total_chunks * H;
-    const long long t = (long long)blockIdx.x * kPlanThreads + threadIdx.x;
-    if (t >= items) return;
-    // the rank holding item t: the last rank with H * rf[rank] <= t (its length > 0)
-    int lo = 0, hi = d.N;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((long long)H * rf[mid] <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    const int rank = lo, len = rf[rank + 1] - rf[rank];
-    const long long within = t - (long long)H * rf[rank];
-    const int h = (int)(within / len), j = (int)(within % len);
-    const long long R = (long long)d.N * H, r = (long long)rank * H + h;
-    auto len_of = [&](long long x) { const int rk = (int)(x / H); return rf[rk + 1] - rf[rk]; };
-    // items of the chains before chain x (chain order)
-    auto before = [&](long long x) -> long long {
-        if (x >= R) return items;
-        const int rk = (int)(x / H);
-        return (long long)H * rf[rk] + (x % H) * (long long)(rf[rk + 1] - rf[rk]);
+    const int R32 = (int)R, items32 = (int)items, nc32 = (int)nc, N = d.N;
+    auto before = [&](int x) -> int {  // items of the chains before chain x
+        if (x >= R32) return items32;
+        const int rk = x / H;
+        return H * rf[rk] + (x - rk * H) * rcntf(rk);
     };
-    const long long a = (r / nc) * nc, b = a + nc < R ? a + nc : R;
-    // cnt: chains of the round longer than j (a prefix: lengths do not increase)
-    long long l2 = a, h2 = b;
-    while (l2 < h2) {
-        const long long mid = (l2 + h2) >> 1;
-        if (len_of(mid) <= j) h2 = mid;
-        else l2 = mid + 1;
+    for (int t = tid; t < items32; t += kThreads) {
+        // the rank holding item t: the last rank with H * rf[rank] <= t (its count > 0)
+        int lo = 0, hi = N;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (H * rf[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        const int rank = lo, len = rcntf(rank);
+        const int within = t - H * rf[rank];
+        const int h = within / len, j = within - h * len;
+        const int r = rank * H + h;
+        const int a = r - r % nc32, b = a + nc32 < R32 ? a + nc32 : R32;
+        // cnt: chains of the round longer than j, a prefix of the round: the first
+        // rank (from a's) whose count is <= j bounds it
+        int l2 = a / H, h2 = N;
+        while (l2 < h2) {
+            const int mid = (l2 + h2) >> 1;
+            if (rcntf(mid) <= j) h2 = mid;
+            else l2 = mid + 1;
+        }
+        const int x1 = l2 * H;
+        const int cnt = (x1 < a ? a : (x1 > b ? b : x1)) - a;
+        // rounds before + steps < j of this round's chains + chains before r at step j
+        const int pos = before(a) + j * cnt + (before(b) - before(a + cnt)) + (r - a);
+        const int c = rc0(rank) + j;
+        plist[pos] = c * H + h;
+        ready[(size_t)c * H + h] = 0u;
     }
-    const long long cnt = l2 - a;
-    // rounds before + steps < j of this round's chains + chains before r at step j
-    const long long pos = before(a) + (long long)j * cnt + (before(b) - before(a + cnt)) + (r - a);
-    const int c = seq_first[order[rank]] + j;
-    plist[pos] = c * H + h;
-    ready[(size_t)c * H + h] = 0u;
 }
 
 }  // namespace
@@ -264,15 +271,6 @@ cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* w
 cudaError_t launch_schedule_fused(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
                                   int fused_grid, float production_ratio, cudaStream_t stream) {
     schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, fused_grid, production_ratio);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_plan(const Dims& d, uint8_t* ws, cudaStream_t stream) {
-    const WsLayout L(d);
-    const long long items = L.cmax * d.H;
-    if (items == 0) return cudaSuccess;
-    const long long blocks = (items + kPlanThreads - 1) / kPlanThreads;
-    plan_kernel<<<(unsigned)blocks, kPlanThreads, 0, stream>>>(d, ws);
     return cudaGetLastError();
 }
 

@@ -103,8 +103,9 @@ kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* d
 /* Static, human-readable name of a status. */
 const char* kda_status_string(kda_status status);
 
-/* Number of kernel launches kda_fwd enqueues for these sizes (for launch counts):
- * 3 in either pipeline (schedule, plan, fused; or schedule, factors, state). */
+/* Number of kernel launches kda_fwd enqueues for these sizes under the current
+ * pipeline setting (for launch counts): 2 with the fused pipeline (schedule, fused),
+ * 3 with the split one (schedule, factors, state). */
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /*
@@ -141,12 +142,12 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
 /*
  * Pipelines of the forward (both compute the same operation; their kernels differ,
  * so results may differ in the last bits):
- *   KDA_PIPELINE_FUSED (default): a schedule kernel, a plan kernel, then one
- *     persistent cooperative kernel in which some CTAs produce the per-chunk
- *     factors and the others run the state recurrence over whole (sequence, head)
- *     chains, consuming each chunk's factors as soon as they are published.  Taken
- *     for batches of at most 2048 sequences and 65536 (sequence, head) pairs on a
- *     device with at least 2 SMs; other sizes take the split pipeline.
+ *   KDA_PIPELINE_FUSED (default): a schedule kernel, then one persistent
+ *     cooperative kernel in which some CTAs produce the per-chunk factors and the
+ *     others run the state recurrence over whole (sequence, head) chains,
+ *     consuming each chunk's factors as soon as they are published.  Taken for
+ *     dk = dv = 128, batches of at most 2048 sequences and 65536 (sequence, head)
+ *     pairs, on a device with at least 2 SMs; other sizes take the split pipeline.
  *   KDA_PIPELINE_SPLIT: a schedule kernel, a factor kernel over every chunk, then
  *     a state kernel over (sequence, head, value-column tile) chains.
  * The setting is process-wide (an atomic; calls already enqueued keep theirs); it

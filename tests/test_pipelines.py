@@ -1,0 +1,99 @@
+"""The two pipelines of the forward: which one a call takes, and parity of each.
+
+The fused pipeline (default for dk = dv = 128) runs factor production and the state
+chains in one cooperative kernel; the split one (a factor kernel, then a state
+kernel) serves the other head sizes and stays selectable.  Both are checked against
+the fp64 oracle with the gates of test_gpu_parity.py.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from tests import gen
+from tests.test_gpu_parity import SALT, _assert_parity, _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_delta_rule_25_gb300 as m
+    return m
+
+
+@pytest.fixture
+def split(kda):
+    kda.set_pipeline("split")
+    try:
+        yield kda
+    finally:
+        kda.set_pipeline("fused")
+
+
+def test_pipeline_selection(kda):
+    assert kda.get_pipeline() == "fused"
+    assert kda.uses_fused(1, 8192, 32, 128, 128, 1)
+    assert kda.uses_fused(1, 8192, 32, 128, 128, 2048)          # varlen, 2048 sequences
+    assert not kda.uses_fused(1, 8192, 32, 128, 128, 2049)      # beyond the ranking
+    assert not kda.uses_fused(1, 256, 2, 64, 64, 1)             # dk = dv = 64
+    assert not kda.uses_fused(1, 256, 2, 128, 64, 1)
+    assert kda.launch_count(1, 8192, 32, 128, 128, 1) == 2
+    kda.set_pipeline("split")
+    try:
+        assert not kda.uses_fused(1, 8192, 32, 128, 128, 1)
+        assert kda.launch_count(1, 8192, 32, 128, 128, 1) == 3
+    finally:
+        kda.set_pipeline("fused")
+    with pytest.raises(ValueError):
+        kda.set_pipeline("other")
+
+
+@pytest.mark.parametrize("name", ["cfg2", "cfg3", "cfg4"])
+def test_split_pipeline_parity(split, name):
+    x = getattr(gen, f"make_{name}")(seed=3, salt=SALT)
+    heads = [0, x.H // 2, x.H - 1]
+    _assert_parity(x, *_gpu(split, x), heads=heads)
+
+
+def test_split_pipeline_head_dims_128(split):
+    x = gen.make_lengths([70, 1, 129, 64, 0, 33] * 4, seed=8, salt=SALT, H=4, d=128)
+    _assert_parity(x, *_gpu(split, x))
+
+
+def test_fused_many_rounds_and_empty_chains(kda):
+    """More chains than chain CTAs (several rounds), chains of one step, empty ones,
+    and one long chain that sets the critical path."""
+    lens = [0, 1, 64, 65, 3000, 0, 17, 128] * 9 + [0, 0]
+    x = gen.make_lengths(lens, seed=12, salt=SALT, H=6, d=128)
+    assert kda.uses_fused(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs)
+    _assert_parity(x, *_gpu(kda, x))
+
+
+def test_fused_single_step_chains(kda):
+    """Hundreds of one-chunk chains per chain CTA: every step starts a new chain."""
+    lens = [64, 1, 37, 64, 50] * 40
+    x = gen.make_lengths(lens, seed=13, salt=SALT, H=8, d=128)
+    _assert_parity(x, *_gpu(kda, x))
+
+
+def test_fused_all_sequences_empty(kda):
+    """No token at all: the states pass through (h_T = h0) and nothing else runs."""
+    x = gen.make_lengths([0, 0, 0], seed=14, salt=SALT, H=3, d=128)
+    o, hT = _gpu(kda, x)
+    assert o.numel() == 0
+    assert torch.equal(hT, x.h0)
+
+
+def test_fused_and_split_agree(kda, split):
+    """Both pipelines on the same varlen batch stay within the gates of each other's
+    reference (each is checked against the oracle; here only that they agree)."""
+    x = gen.make_cfg3(seed=15, salt=SALT)
+    o_s, h_s = _gpu(split, x)
+    split.set_pipeline("fused")
+    o_f, h_f = _gpu(kda, x)
+    from tests.metrics import rel_rmse
+    assert rel_rmse(o_f, o_s.double()) <= 1e-2
+    assert rel_rmse(h_f, h_s.double()) <= 5e-3
