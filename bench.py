@@ -364,9 +364,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pipeline", default="fused", choices=["fused", "split"],
-                    help="fused: factor production and state chains in one kernel (default); "
-                         "split: a factor kernel, then a state kernel")
+    ap.add_argument("--pipeline", default="auto", choices=["auto", "fused", "split"],
+                    help="auto (default): the library's choice for the sizes; fused: factor "
+                         "production and state chains in one kernel; split: a factor kernel, "
+                         "then a state kernel")
     ap.add_argument("--workload", default="cfg2",
                     help="cfg2 (the headline workload), cfg2-gbf16 (bf16 gate), cfg3, cfg4, "
                          "cfg5-{fixed|varlen}-H{16|32|64}-{total}, "

@@ -44,7 +44,23 @@ int num_sms() {
 
 namespace {
 
-std::atomic<int> g_pipeline{KDA_PIPELINE_FUSED};
+std::atomic<int> g_pipeline{KDA_PIPELINE_AUTO};
+
+// The fused pipeline's grid for these sizes under the current setting, or 0 for the
+// split pipeline.  Automatic choice: where the fused pipeline was measured faster on
+// GB300 (the throughput sweep of 22 shapes: fixed-length batches with B * H from 32
+// to 256 gain 6-15 %; varlen batches, where the chains of a round differ in length,
+// B * H = 16, whose few chains bound it, and B * H >= 512, where the factor CTAs it
+// gives up cost more than the chains gain, run faster split).
+int pipeline_grid(const kda::Dims& d) {
+    const int p = g_pipeline.load();
+    if (p == KDA_PIPELINE_SPLIT) return 0;
+    const int grid = kda::fused_grid(d);
+    if (grid == 0 || p == KDA_PIPELINE_FUSED) return grid;
+    const long long pairs = (long long)d.N * d.H;
+    const bool uniform = !d.varlen || d.N == 1;
+    return uniform && pairs >= 32 && pairs <= 256 ? grid : 0;
+}
 
 bool valid_head_dim(int x) { return x == 64 || x == 128; }
 
@@ -84,7 +100,9 @@ int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
 }
 
 void kda_set_pipeline(kda_pipeline pipeline) {
-    g_pipeline.store(pipeline == KDA_PIPELINE_SPLIT ? KDA_PIPELINE_SPLIT : KDA_PIPELINE_FUSED);
+    g_pipeline.store(pipeline == KDA_PIPELINE_SPLIT ? KDA_PIPELINE_SPLIT
+                     : pipeline == KDA_PIPELINE_FUSED ? KDA_PIPELINE_FUSED
+                                                      : KDA_PIPELINE_AUTO);
 }
 
 kda_pipeline kda_get_pipeline(void) { return static_cast<kda_pipeline>(g_pipeline.load()); }
@@ -92,7 +110,7 @@ kda_pipeline kda_get_pipeline(void) { return static_cast<kda_pipeline>(g_pipelin
 int kda_fwd_uses_fused(int B, int T, int H, int dk, int dv, int num_seqs) {
     kda::Dims d;
     if (make_dims(B, T, H, dk, dv, num_seqs, B == 1 && num_seqs != B, d) != KDA_OK) return 0;
-    return g_pipeline.load() == KDA_PIPELINE_FUSED && kda::fused_grid(d) > 0 ? 1 : 0;
+    return pipeline_grid(d) > 0 ? 1 : 0;
 }
 
 }  // extern "C"
@@ -133,7 +151,7 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         return cudaEventRecord(static_cast<cudaEvent_t>(events[ev++]), s) == cudaSuccess;
     };
     const bool gbf = g_dtype == KDA_BF16;
-    const int grid = g_pipeline.load() == KDA_PIPELINE_FUSED ? kda::fused_grid(d) : 0;
+    const int grid = pipeline_grid(d);
     if (grid > 0) {
         if (!mark() || kda::launch_schedule_fused(d, cu_seqlens, ws, grid, kda::fused_ratio(d, bf16), s) !=
                            cudaSuccess)

@@ -218,6 +218,14 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     for (int e = 0; e < 32; ++e) S[e] = 0.f;
     bool have_prev = false;
     int4 prev_out = make_int4(0, 0, 0, 0);  // {first token row, rows, head, 0} of the previous step
+    ChainPos prev_pos = cur;                // the previous step
+    // The previous step's factor block: every part of it has been read (its GEMM3,
+    // the last reader, is done) and nothing else reads it, so its lines leave L2
+    // without being written back.
+    auto drop_prev_block = [&]() {
+        const uint8_t* blk = block_of(prev_pos);
+        for (int i = tid; i < (int)(W.factor_bytes / 128); i += kThreads) ptx::discard_l2_line(blk + 128 * i);
+    };
     uint32_t gj = 0;                        // steps of this CTA so far
     // The output leaves in two moves: each thread puts its 16 rows of column n from
     // tensor memory into a row-major staging tile; after the next barrier, lane 0 of
@@ -374,10 +382,13 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
                 chain_raise(ws, abort);
             }
         }
-        // -------- output of the previous step into the staging tile, while GEMM2 runs
+        // -------- output of the previous step into the staging tile, and its factor
+        //          block out of L2 (its GEMM3 was waited for before the barrier), while
+        //          GEMM2 runs
         if (have_prev) {
             ptx::tc_fence_after();
             out_stage(b ^ 1u);
+            drop_prev_block();
         }
         // -------- S^T <- S^T Diag(GL) + D2^T  ->  bf16 S^T (GEMM1, its reader, is done)
         bool okd = ptx::mbar_spin_or_abort(&sm.d2, b, abort);
@@ -416,6 +427,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
             prev_out = make_int4(cur.tok0 + kChunk * cur.j, rows < kChunk ? rows : kChunk, cur.h, 0);
         }
         have_prev = true;
+        prev_pos = cur;
         ++gj;
         cur = nxt;
         have = nv;
@@ -430,6 +442,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         if (ok) {
             ptx::tc_fence_after();
             out_stage((gj - 1) & 1u);
+            drop_prev_block();
         } else {
             chain_raise(ws, abort);
         }
@@ -536,7 +549,8 @@ cudaError_t launch_fused_t(const Dims& d, const void* q, const void* k, const vo
 
 int fused_grid(const Dims& d) {
     const int sms = num_sms();
-    if (d.dk != kCDK || d.dv != kCDV || sms < 2 || d.N > kRankMax || (long long)d.N * d.H > 65536) return 0;
+    if (d.dk != kCDK || d.dv != kCDV || sms < 2 || sms > 1025 || d.N > kRankMax || (long long)d.N * d.H > 65536)
+        return 0;
     return sms;
 }
 

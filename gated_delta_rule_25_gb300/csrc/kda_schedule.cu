@@ -12,6 +12,7 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kMaxGrid = 1024;  // fused grids of up to this many CTAs
 
 __device__ inline void seq_span(const Dims& d, const int32_t* cu, int s, long long& row0,
                                 int& len) {
@@ -182,8 +183,15 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     // head); chain CTA x takes chains x, x + n_chain, ... (round k = r / n_chain), so
     // CTA 0 runs the longest chain of every round.  rf: chunks before each rank.
     __syncthreads();  // s_order complete
-    auto rc0 = [&](int rk) { return s_first[s_order[rk]]; };
-    auto rcntf = [&](int rk) { const int sq = s_order[rk]; return s_first[sq + 1] - s_first[sq]; };
+    __shared__ int s_rc0[kRankMax], s_rcnt[kRankMax];  // first chunk and chunks of each rank
+    for (int rk = tid; rk < d.N; rk += kThreads) {
+        const int sq = s_order[rk];
+        s_rc0[rk] = s_first[sq];
+        s_rcnt[rk] = s_first[sq + 1] - s_first[sq];
+    }
+    __syncthreads();
+    auto rc0 = [&](int rk) { return s_rc0[rk]; };
+    auto rcntf = [&](int rk) { return s_rcnt[rk]; };
     int* const rf = s_rf;
     if (tid == 0) carry = 0;
     __syncthreads();
@@ -194,42 +202,65 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     }
     if (tid == 0) rf[d.N] = carry;
     __syncthreads();
-    // n_chain c minimises max(chain steps of CTA 0, ratio * items / (grid - c)):
-    // the chain CTAs' critical path against the factor CTAs' share of the items.
+    // n_chain c minimises max(chain steps of CTA 0, ratio * items / (grid - c)): the
+    // chain CTAs' critical path against the factor CTAs' share of the items.  CTA 0
+    // runs chains 0, c, 2c, ...: steps(c) = sum over rounds k of the count of rank
+    // (k c) / H, summed by several threads per candidate (ranks tracked without
+    // division).
+    __shared__ int steps_s[kMaxGrid + 1];
     __shared__ unsigned long long best;
+    const int H = d.H, N = d.N;
+    const int R = N * H, items = carry * H;
+    const int cmax = R < fused_grid - 1 ? R : fused_grid - 1;
+    for (int c = tid; c <= cmax; c += kThreads) steps_s[c] = 0;
     if (tid == 0) best = ~0ull;
     __syncthreads();
-    const int H = d.H;
-    const long long R = (long long)d.N * H, items = (long long)carry * H;
-    const long long cmax = R < fused_grid - 1 ? R : fused_grid - 1;
-    for (long long c = tid + 1; c <= cmax; c += kThreads) {
-        const long long rounds = (R + c - 1) / c;
-        if (rounds > 1024) continue;
-        long long steps = 0;
-        for (long long k = 0; k < rounds; ++k) steps += rcntf((int)(k * c / H));
-        const float cost = fmaxf((float)steps, ratio * (float)items / (float)(fused_grid - c));
+    {
+        const int split = cmax > 0 ? (kThreads / cmax > 0 ? kThreads / cmax : 1) : 1;
+        for (int w = tid; w < cmax * split; w += kThreads) {
+            const int c = w % cmax + 1, part = w / cmax;
+            const int stride = split * c;  // chains between this thread's rounds
+            const int dq = stride / H, dr = stride - dq * H;
+            int rk = (part * c) / H, rem = part * c - rk * H, sum = 0;
+            for (int r = part * c; r < R; r += stride) {
+                sum += rcntf(rk);
+                rk += dq;
+                rem += dr;
+                if (rem >= H) {
+                    rem -= H;
+                    ++rk;
+                }
+            }
+            atomicAdd(&steps_s[c], sum);
+        }
+    }
+    __syncthreads();
+    for (int c = tid + 1; c <= cmax; c += kThreads) {
+        const float cost = fmaxf((float)steps_s[c], ratio * (float)items / (float)(fused_grid - c));
         atomicMin(&best, ((unsigned long long)__float_as_uint(cost) << 32) | (unsigned long long)c);
     }
     __syncthreads();
-    const long long nc = best == ~0ull ? cmax : (long long)(best & 0xffffffffull);
-    if (tid == 0) hdr->n_chain = (int)nc;
+    const int nc = best == ~0ull ? cmax : (int)(best & 0xffffffffull);
+    if (tid == 0) hdr->n_chain = nc;
 
     // Production order: the items of round k (its chains' chunks) come before those
     // of round k + 1, and inside a round step j of every chain comes before step
     // j + 1 (chains in the round's order), so that the chain CTAs find their next
-    // chunk published early.  Items are taken in chain order (t = the item's index
-    // there); each also clears its ready flag.  32-bit arithmetic throughout (items
-    // and chains stay far below 2^31); the searches run over ranks, whose counts do
-    // not increase.
+    // chunk published early.  Items are taken in chain order (t, the index there),
+    // each thread a run of consecutive ones, walking (rank, head, step) forward;
+    // each also clears its ready flag.  32-bit arithmetic throughout (items and
+    // chains stay far below 2^31); counts do not increase with the rank.
     int32_t* plist = reinterpret_cast<int32_t*>(ws + L.plist);
     uint32_t* ready = reinterpret_cast<uint32_t*>(ws + L.ready);
-    const int R32 = (int)R, items32 = (int)items, nc32 = (int)nc, N = d.N;
     auto before = [&](int x) -> int {  // items of the chains before chain x
-        if (x >= R32) return items32;
+        if (x >= R) return items;
         const int rk = x / H;
         return H * rf[rk] + (x - rk * H) * rcntf(rk);
     };
-    for (int t = tid; t < items32; t += kThreads) {
+    const int per = (items + kThreads - 1) / kThreads;
+    int t = tid * per;
+    const int t_end = t + per < items ? t + per : items;
+    if (t < t_end) {
         // the rank holding item t: the last rank with H * rf[rank] <= t (its count > 0)
         int lo = 0, hi = N;
         while (lo < hi) {
@@ -237,26 +268,55 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
             if (H * rf[mid] <= t) lo = mid;
             else hi = mid - 1;
         }
-        const int rank = lo, len = rcntf(rank);
+        int rank = lo, len = rcntf(rank);
         const int within = t - H * rf[rank];
-        const int h = within / len, j = within - h * len;
-        const int r = rank * H + h;
-        const int a = r - r % nc32, b = a + nc32 < R32 ? a + nc32 : R32;
-        // cnt: chains of the round longer than j, a prefix of the round: the first
-        // rank (from a's) whose count is <= j bounds it
-        int l2 = a / H, h2 = N;
-        while (l2 < h2) {
-            const int mid = (l2 + h2) >> 1;
-            if (rcntf(mid) <= j) h2 = mid;
-            else l2 = mid + 1;
+        int h = within / len, j = within - h * len;
+        int r = rank * H + h;
+        int a = r - r % nc, b = a + nc < R ? a + nc : R;
+        int a_rank = a / H, Ba = before(a), Bb = before(b);
+        for (; t < t_end; ++t) {
+            // chains of the round longer than j: a prefix, bounded by the first rank
+            // (from a's) whose count is <= j
+            int l2 = a_rank, h2 = N;
+            while (l2 < h2) {
+                const int mid = (l2 + h2) >> 1;
+                if (rcntf(mid) <= j) h2 = mid;
+                else l2 = mid + 1;
+            }
+            const int x1 = l2 * H;
+            int cnt, Bc;
+            if (x1 <= a) {
+                cnt = 0;
+                Bc = Ba;
+            } else if (x1 >= b) {
+                cnt = b - a;
+                Bc = Bb;
+            } else {
+                cnt = x1 - a;
+                Bc = H * rf[l2];
+            }
+            // rounds before + steps < j of this round's chains + chains before r at step j
+            const int pos = Ba + j * cnt + (Bb - Bc) + (r - a);
+            const int c = rc0(rank) + j;
+            plist[pos] = c * H + h;
+            ready[(size_t)c * H + h] = 0u;
+            if (++j == len) {  // the next chain
+                j = 0;
+                ++r;
+                if (++h == H) {
+                    h = 0;
+                    ++rank;
+                    len = rank < N ? rcntf(rank) : 0;
+                }
+                if (r >= b) {  // the next round
+                    a = b;
+                    b = a + nc < R ? a + nc : R;
+                    a_rank = a / H;
+                    Ba = Bb;
+                    Bb = before(b);
+                }
+            }
         }
-        const int x1 = l2 * H;
-        const int cnt = (x1 < a ? a : (x1 > b ? b : x1)) - a;
-        // rounds before + steps < j of this round's chains + chains before r at step j
-        const int pos = before(a) + j * cnt + (before(b) - before(a + cnt)) + (r - a);
-        const int c = rc0(rank) + j;
-        plist[pos] = c * H + h;
-        ready[(size_t)c * H + h] = 0u;
     }
 }
 

@@ -346,6 +346,12 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Drops one 128-byte line (128-byte aligned global address) from L2 without writing
+// it back: for data that nothing reads again.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ---------------------------------------------------------------- flags between CTAs
 // Publishes what this CTA wrote to global memory (the other threads' stores are
 // ordered before this call by a CTA barrier): a proxy fence, so that bulk copies in

@@ -142,23 +142,26 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
 /*
  * Pipelines of the forward (both compute the same operation; their kernels differ,
  * so results may differ in the last bits):
- *   KDA_PIPELINE_FUSED (default): a schedule kernel, then one persistent
- *     cooperative kernel in which some CTAs produce the per-chunk factors and the
- *     others run the state recurrence over whole (sequence, head) chains,
- *     consuming each chunk's factors as soon as they are published.  Taken for
- *     dk = dv = 128, batches of at most 2048 sequences and 65536 (sequence, head)
- *     pairs, on a device with at least 2 SMs; other sizes take the split pipeline.
- *   KDA_PIPELINE_SPLIT: a schedule kernel, a factor kernel over every chunk, then
- *     a state kernel over (sequence, head, value-column tile) chains.
- * The setting is process-wide (an atomic; calls already enqueued keep theirs); it
- * exists for measurement and testing.
+ *   fused: a schedule kernel, then one persistent cooperative kernel in which some
+ *     CTAs produce the per-chunk factors and the others run the state recurrence
+ *     over whole (sequence, head) chains, consuming each chunk's factors as soon as
+ *     they are published.  Applies to dk = dv = 128, batches of at most 2048
+ *     sequences and 65536 (sequence, head) pairs, on a device with 2 to 1025 SMs.
+ *   split: a schedule kernel, a factor kernel over every chunk, then a state kernel
+ *     over (sequence, head, value-column tile) chains.  Applies to every size.
+ * KDA_PIPELINE_AUTO (default) takes the fused pipeline where it applies and was
+ * measured faster on GB300: fixed-length batches (or a single sequence) with
+ * 32 <= B * H <= 256; every other size takes the split one.  KDA_PIPELINE_FUSED
+ * takes it wherever it applies, KDA_PIPELINE_SPLIT never.  The setting is
+ * process-wide (an atomic; calls already enqueued keep theirs); it exists for
+ * measurement and testing.
  */
-typedef enum { KDA_PIPELINE_FUSED = 0, KDA_PIPELINE_SPLIT = 1 } kda_pipeline;
+typedef enum { KDA_PIPELINE_AUTO = 0, KDA_PIPELINE_FUSED = 1, KDA_PIPELINE_SPLIT = 2 } kda_pipeline;
 void kda_set_pipeline(kda_pipeline pipeline);
 kda_pipeline kda_get_pipeline(void);
 
 /* 1 if kda_fwd takes the fused pipeline for these sizes under the current setting
- * (on the current device), else 0. */
+ * (on the current device), else 0.  B == 1 with num_seqs != 1 is a varlen batch. */
 int kda_fwd_uses_fused(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /* Size of the device scratch array built into the library for kda_fwd_noalloc. */
