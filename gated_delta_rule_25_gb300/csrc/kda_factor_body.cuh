@@ -525,6 +525,8 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
     bool have_prev = false;
     uint32_t prev_reg = 0;
     Item prev_item{0, H, 0};
+    bool pub_pending = false;  // with ready flags: an item complete but not yet published
+    Item pub_item{0, H, 0};
     uint8_t* prev_wq = nullptr;
     float* prev_u = nullptr;
     while (item.h < H) {
@@ -881,9 +883,14 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
             }
             named_sync(2, 256);      // warps 0-7: the two 32-blocks
             inv_join64(X, A, T, warp, lane);
-        } else if (kBf16In && next.h < H) {
-            p1(rows_next.y, par ^ 1u, tid - kThreads / 2, HalfThreads{}, sm.bs[par ^ 1u]);
-            if (tid == kThreads / 2 + 64) warm_l2(y, rows_y);
+        } else {
+            if (kBf16In && next.h < H) {
+                p1(rows_next.y, par ^ 1u, tid - kThreads / 2, HalfThreads{}, sm.bs[par ^ 1u]);
+                if (tid == kThreads / 2 + 64) warm_l2(y, rows_y);
+            }
+            // the item whose last parts left before the previous item's end barrier:
+            // published here, where warps 8-15 have slack and its stores have drained
+            if (tid == kThreads / 2 && pub_pending) ptx::flag_publish(plan.ready + (size_t)pub_item.c * H + pub_item.h);
         }
         __syncthreads();
         if (kBf16In && next.h < H) {
@@ -1051,10 +1058,9 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
     ptx::tc_fence_before();
     __syncthreads();
     if (*abort) break;
-    if (plan.ready && tid == 0) {
-        if (publish_prev) ptx::flag_publish(plan.ready + (size_t)published.c * H + published.h);
-        if (first_now) ptx::flag_publish(plan.ready + (size_t)item.c * H + item.h);
-    }
+    pub_pending = plan.ready != nullptr && publish_prev;  // (published during the next item)
+    pub_item = published;
+    if (first_now && tid == 0) ptx::flag_publish(plan.ready + (size_t)item.c * H + item.h);
     par ^= 1u;
     item = next;
     rows_cur = rows_next;
@@ -1081,8 +1087,10 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (plan.ready && have_prev && tid == 0 && !*abort)  // the last item's parts all left
-        ptx::flag_publish(plan.ready + (size_t)prev_item.c * H + prev_item.h);
+    if (plan.ready && tid == 0 && !*abort) {  // the last items' parts all left
+        if (pub_pending) ptx::flag_publish(plan.ready + (size_t)pub_item.c * H + pub_item.h);
+        if (have_prev) ptx::flag_publish(plan.ready + (size_t)prev_item.c * H + prev_item.h);
+    }
     if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
