@@ -143,6 +143,27 @@ def test_fused_all_sequences_empty(fused):
     assert torch.equal(hT, x.h0)
 
 
+def test_fused_pipeline_bf16_gate(fused):
+    """A bf16 gate through the fused pipeline: parity, and bit-identical to the fp32
+    gate fed the same values."""
+    x = gen.make_cfg2(seed=16, salt=SALT, T=300, H=16, B=2)
+    x.g = x.g.to(torch.bfloat16)
+    o16, h16 = _gpu(fused, x)
+    _assert_parity(x, o16, h16)
+    x32 = gen.make_cfg2(seed=16, salt=SALT, T=300, H=16, B=2)
+    x32.g = x.g.float()
+    o32, h32 = _gpu(fused, x32)
+    assert torch.equal(o16, o32) and torch.equal(h16, h32)
+
+
+def test_fused_pipeline_fp32_inputs(fused):
+    """fp32 q, k, v at d = 128 through the fused pipeline (u on tf32 operands, the
+    [64/4][dv][4] layout written by scalar stores)."""
+    x = gen.make_cfg1(seed=17, salt=SALT, T=300, H=4, d=128)
+    assert fused.uses_fused(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs)
+    _assert_parity(x, *_gpu(fused, x))
+
+
 def test_fused_and_split_agree(kda):
     """Both pipelines on the same varlen batch stay within the gates of each other's
     reference (each is checked against the oracle; here only that they agree)."""

@@ -65,7 +65,9 @@ def test_noalloc_matches_fwd_on_two_calls_in_a_row(kda):
     """Both entry points run the same kernels on the same inputs, so the results are
     bit-identical; a stale or shared-scratch bug would show as any differing element."""
     cases = [gen.make_lengths([200, 1, 67, 0, 150], seed=21, salt=gen.fresh_salt(), H=4, d=128),
-             gen.make_cfg2(seed=22, salt=gen.fresh_salt(), T=384, H=6, B=2)]
+             gen.make_cfg2(seed=22, salt=gen.fresh_salt(), T=384, H=6, B=2),
+             gen.make_cfg2(seed=26, salt=gen.fresh_salt(), T=384, H=16, B=2)]  # B*H = 32: fused
+    assert kda.uses_fused(2, 384, 16, 128, 128, 2) and not kda.uses_fused(2, 384, 6, 128, 128, 2)
     for x in cases:  # two calls in a row share the built-in scratch
         xd = x.to("cuda")
         o_ref, h_ref = kda.fwd(**xd.tensors(), check=True)
