@@ -43,7 +43,7 @@ WORKLOADS = {
     "cfg4": "varlen skewed 8192 tokens in 32 sequences (one ~5000), H=32, d=128, extreme-value probes",
 }
 KERNEL_NAMES = {"fused": ["schedule", "fused"],
-                "split": ["schedule", "factors", "state_recurrence"]}
+                "split": ["schedule", "factors", "state_recurrence", "state_recurrence_128"]}
 
 
 def make_workload(name: str, seed: int, salt: int):
@@ -85,7 +85,7 @@ def _algorithmic_bytes(kernel: str, tokens: int, heads: int, dk: int, dv: int, n
     th = tokens * heads
     if kernel == "factors":       # reads q, k, v, g, beta
         return th * (2 * dk * 2 + dv * 2 + dk * g_bytes + 4)
-    if kernel == "state_recurrence":  # writes o; reads h0, writes hT
+    if kernel in ("state_recurrence", "state_recurrence_128"):  # writes o; reads h0, writes hT
         return th * dv * 2 + 2 * nseq * heads * dk * dv * 4
     if kernel == "fused":         # the whole path: both of the above
         return _path_bytes(tokens, heads, dk, dv, nseq, g_bytes)

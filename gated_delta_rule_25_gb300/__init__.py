@@ -205,9 +205,9 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     ws_bytes = int(lib.kda_fwd_workspace_size(B, T, H, dk, dv, N))
     if ws_bytes == 0:
         raise KdaError(2, "kda_fwd_workspace_size")
-    if workspace is None or workspace.numel() < ws_bytes:
+    if workspace is None or workspace.numel() - (-workspace.data_ptr()) % 256 < ws_bytes:
         workspace = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
-    ws_ptr = (workspace.data_ptr() + 255) & ~255
+    ws_ptr = (workspace.data_ptr() + 255) & ~255  # the library wants 256-byte alignment
     avail = workspace.numel() - (ws_ptr - workspace.data_ptr())
     stream = torch.cuda.current_stream(dev).cuda_stream
     dt = KDA_BF16 if q.dtype == torch.bfloat16 else KDA_FP32

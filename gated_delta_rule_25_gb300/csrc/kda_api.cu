@@ -64,6 +64,16 @@ int pipeline_grid(const kda::Dims& d) {
 
 bool valid_head_dim(int x) { return x == 64 || x == 128; }
 
+// The split pipeline's state kernel: 0 tiled, 1 the 128-column chains, 2 decided on
+// the device from the chain lengths (varlen batches of at least 512 chains; the
+// 128-column kernel was never picked below that on the sweep's shapes, and the
+// decision costs a launch of the kernel not chosen).
+int c128_mode(const kda::Dims& d) {
+    if (!kda::chain128_applies(d)) return 0;
+    if (d.varlen && d.N > 1) return (long long)d.N * d.H >= 512 ? 2 : 0;
+    return kda::chain128_pick_uniform(d) ? 1 : 0;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks sizes; fills Dims.  Returns KDA_OK or the status to report.
@@ -95,8 +105,12 @@ size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs)
 }
 
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
-    // schedule, fused; or schedule, factors, state recurrence
-    return kda_fwd_uses_fused(B, T, H, dk, dv, num_seqs) ? 2 : 3;
+    // schedule, fused; or schedule, factors, a state kernel (varlen batches with
+    // dk = dv = 128: both state kernels, one of them leaving at once)
+    if (kda_fwd_uses_fused(B, T, H, dk, dv, num_seqs)) return 2;
+    kda::Dims d;
+    if (make_dims(B, T, H, dk, dv, num_seqs, B == 1 && num_seqs != B, d) != KDA_OK) return 3;
+    return c128_mode(d) == 2 ? 4 : 3;
 }
 
 void kda_set_pipeline(kda_pipeline pipeline) {
@@ -161,12 +175,27 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         if (ce != cudaSuccess || !mark()) return KDA_ERR_CUDA;
         return KDA_OK;
     }
-    if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+    // split: the state recurrence on value tiles or, dk = dv = 128, on 128-column
+    // chains where that is predicted faster (decided here for equal-length chains,
+    // by the schedule kernel from the lengths for varlen batches, in which case both
+    // kernels are launched and the one not chosen leaves at once)
+    const int mode = c128_mode(d);
+    if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, kda::split_nv_for(d), mode, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
     if (!mark() || kda::launch_prep_tc(d, bf16, gbf, q, k, v, g, beta, ws, s) != cudaSuccess)
         return KDA_ERR_CUDA;
+    cudaError_t ce;
+    if (mode != 1) {
+        if (!mark()) return KDA_ERR_CUDA;
+        ce = kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
+        if (ce != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    if (mode != 0) {
+        if (!mark()) return KDA_ERR_CUDA;
+        ce = kda::launch_chain128(d, bf16, h0, scale, o, hT, ws, s);
+        if (ce != cudaSuccess) return KDA_ERR_CUDA;
+    }
     if (!mark()) return KDA_ERR_CUDA;
-    const cudaError_t ce = kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
-    if (ce != cudaSuccess || !mark()) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

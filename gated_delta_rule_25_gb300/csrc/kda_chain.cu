@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int4* chunks = reinterpret_cast<const int4*>(ws + W.chunks);
     const int n_items = d.N * d.H * NVT;
     volatile int* abort = &sm.abort;
+    if (hdr->chain128) return;  // the 128-column chain kernel runs the recurrence instead
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -485,13 +486,20 @@ cudaError_t launch_t(const Dims& d, const float* h0, float scale, void* o, float
 template <int DK, int DV, typename TOut>
 cudaError_t launch_nv(const Dims& d, const float* h0, float scale, void* o, float* hT, uint8_t* ws,
                       cudaStream_t stream) {
-    const long long chains32 = (long long)d.N * d.H * (DV / 32);
-    if (chains32 > num_sms()) return launch_t<DK, DV, 64, TOut>(d, h0, scale, o, hT, ws, stream);
-    if (2 * chains32 <= num_sms()) return launch_t<DK, DV, 16, TOut>(d, h0, scale, o, hT, ws, stream);
+    const int nv = split_nv_for(d);
+    if (nv == 64) return launch_t<DK, DV, 64, TOut>(d, h0, scale, o, hT, ws, stream);
+    if (nv == 16) return launch_t<DK, DV, 16, TOut>(d, h0, scale, o, hT, ws, stream);
     return launch_t<DK, DV, 32, TOut>(d, h0, scale, o, hT, ws, stream);
 }
 
 }  // namespace
+
+int split_nv_for(const Dims& d) {
+    const long long chains32 = (long long)d.N * d.H * (d.dv / 32);
+    if (chains32 > num_sms()) return 64;
+    if (2 * chains32 <= num_sms()) return 16;
+    return 32;
+}
 
 cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                          float* hT, uint8_t* ws, cudaStream_t stream) {

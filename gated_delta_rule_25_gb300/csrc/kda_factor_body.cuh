@@ -59,6 +59,7 @@ struct ItemPlan {
     const int32_t* list;
     int first, stride;
     uint32_t* ready;
+    bool ut;  // u leaves as [64/4][dv][4] (the 128-column chains' layout), else slabbed
 };
 
 namespace {
@@ -258,12 +259,13 @@ __device__ __forceinline__ void issue_level_pair(uint32_t tmem, const uint8_t* b
 
 // tmq .. tmg: addresses of __grid_constant__ kernel parameters.  smem_raw: the
 // kernel's dynamic shared memory (1024-byte aligned, sizeof(FactorSmem) bytes).
-// UT: u leaves as [64/4][dv][4] fp32 (a float4 of 4 consecutive rows per value
+// plan.ut: u leaves as [64/4][dv][4] fp32 (a float4 of 4 consecutive rows per value
 // column, columns fastest: a warp of consecutive columns reads 4 rows of each with
 // one contiguous 512-byte load) instead of the slabbed U0 layout; with bf16 inputs
 // and dv = 128 the product itself is transposed (u^T, M = dv), so that every
-// thread leaves with four 16-byte stores.
-template <int DK, int DV, typename TIn, typename TG, bool UT>
+// thread leaves with four 16-byte stores.  (A runtime choice, uniform over the CTA:
+// one copy of the body serves both layouts.)
+template <int DK, int DV, typename TIn, typename TG>
 __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tmq, const CUtensorMap* tmk,
                                             const CUtensorMap* tmv, const CUtensorMap* tmg,
                                             const float* __restrict__ beta, uint8_t* __restrict__ ws,
@@ -273,7 +275,8 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
     using Cf = FactorCfg<DK, DV, TIn>;
     constexpr bool kBf16In = sizeof(TIn) == 2;
     // u^T straight from the tensor cores (bf16 inputs, dv = 128: the M = dv product)
-    constexpr bool kUTmma = UT && kBf16In && DV == 128;
+    const bool UT = plan.ut;
+    const bool kUTmma = UT && kBf16In && DV == 128;
     constexpr int CPT = DK / 64;  // channels per thread in the level phase
     Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
 
@@ -386,7 +389,7 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
                 *reinterpret_cast<uint4*>(wq_dst + mn_off<DK>(16 * cg + 8, cc)) = pack8(y1);
             }
         }
-        if constexpr (kUTmma) {
+        if (kUTmma) {
             // u^T: lane = value column 32 q + lane, columns = chunk rows 16 cg ..: four
             // float4 of 4 rows each, a warp's 32 columns contiguous ([64/4][dv][4])
             float x[16];
@@ -408,7 +411,7 @@ __device__ __forceinline__ void factor_body(const Dims& d, const CUtensorMap* tm
                 ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + reg + 64 + cg * NC + 16 * i, x);
                 ptx::tmem_ld_wait();
                 if (lane < 16) {
-                    if constexpr (UT) {  // [64/4][dv][4]: a float4 of 4 consecutive rows per column
+                    if (UT) {  // [64/4][dv][4]: a float4 of 4 consecutive rows per column
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             u_dst[((row >> 2) * DV + cg * NC + 16 * i + e) * 4 + (row & 3)] = x[e];

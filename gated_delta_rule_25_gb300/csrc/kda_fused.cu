@@ -1,5 +1,5 @@
 // Fused pipeline: one persistent launch in which some CTAs produce the per-chunk
-// factor blocks (the factor body, items in the plan kernel's production order) and
+// factor blocks (the factor body, items in the schedule kernel's production order) and
 // the others run the state recurrence, each over whole (sequence, head) chains
 // with all dv value columns at once, consuming every block as soon as its producer
 // has published it (a per-item ready flag, release/acquire at GPU scope).  A block
@@ -15,11 +15,13 @@
 // in tensor memory (the A operand of an MMA may be read from there) instead of
 // passing through shared memory: lane n of tensor memory is value column n.  For
 // chunk j of a chain (fp32 state S^T, dv x dk, in registers: warp w holds lanes
-// 32 (w % 4) .. and channels 32 (w / 4) ..):
-//   [(w S)^T | (QG S)^T] = S^T [w; QG]^T          GEMM1  M=dv, N=128, K=dk  (bf16, A = S^T in TMEM)
-//   U^T = u^T - (w S)^T                             (fp32 into TMEM, and bf16 for GEMM3)
-//   S^T <- S^T Diag(GL) + U^T KT^T                  GEMM2  M=dv, N=dk,  K=64  (tf32, A = U^T in TMEM)
-//   O^T = scale ((QG S)^T + U^T P^T)                GEMM3  M=dv, N=64,  K=64  (bf16, A = U^T in TMEM)
+// 32 (w % 4) .. and channels 32 (w / 4) ..), all products with M = dv:
+//   (w S)^T  = S^T w^T         GEMM1a/b  N=64, K=dk, its two channel halves into two
+//                                        accumulators (bf16, A = S^T in TMEM)
+//   (QG S)^T = S^T QG^T        GEMM1c    N=64, K=dk (the output part)
+//   U^T = u^T - (w S)^T                  fp32 into TMEM, and bf16 for GEMM3
+//   S^T <- S^T Diag(GL) + U^T KT^T       GEMM2  N=dk, K=64 (tf32, A = U^T in TMEM)
+//   O^T = scale ((QG S)^T + U^T P^T)     GEMM3  N=64, K=64 (bf16, A = U^T in TMEM)
 // [w; QG], u, KT (with GL) and P arrive by bulk copies into shared memory, each
 // part as soon as its slot frees; the output of step j is staged in shared memory
 // while GEMM2 of step j + 1 runs and leaves by bulk copies during step j + 2.
@@ -66,10 +68,14 @@ struct ChainPos {
     int tok0, ntok;  // the sequence's first token row and its tokens
 };
 
+// nc: the chain CTAs (this one is blockIdx.x among them).  use_flags: the factor
+// blocks are published as the pipeline runs (fused kernel); false when they were all
+// written before this kernel started (the split pipeline's 128-column chain kernel).
 template <typename TOut>
 __device__ __forceinline__ void chain_role(const Dims& d, const float* __restrict__ h0, float scale,
                                            TOut* __restrict__ o, float* __restrict__ hT,
-                                           uint8_t* __restrict__ ws, uint8_t* smem_raw, int nc) {
+                                           uint8_t* __restrict__ ws, uint8_t* smem_raw, int nc,
+                                           bool use_flags) {
     constexpr int DK = kCDK, DV = kCDV;
     ChainRoleSmem& sm = *reinterpret_cast<ChainRoleSmem*>(smem_raw);
     constexpr uint32_t WQB = 2 * kChunk * DK * 2, KTB = DK * kChunk * 4, PB = kChunk * kChunk * 2,
@@ -172,7 +178,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     constexpr int kLook = 8;
     uint32_t ready_to = 0;  // (copy thread) steps below this one are acquired
     auto acquire = [&](uint32_t step, const ChainPos& p0) -> bool {  // p0: the position of `step`
-        if (step < ready_to) return true;
+        if (step < ready_to || !use_flags) return true;
         ChainPos p = p0;
         uint32_t v[kLook];
         int nl = 0;
@@ -494,12 +500,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nc = reinterpret_cast<const Header*>(ws + W.header)->n_chain;
     if (nc <= 0) return;  // malformed cu_seqlens (reported in the error word): nothing to do
     if ((int)blockIdx.x < nc) {
-        chain_role<TIn>(d, h0, scale, o, hT, ws, smem_raw, nc);
+        chain_role<TIn>(d, h0, scale, o, hT, ws, smem_raw, nc, true);
     } else {
         const ItemPlan plan{reinterpret_cast<const int32_t*>(ws + W.plist), (int)blockIdx.x - nc,
-                            (int)gridDim.x - nc, reinterpret_cast<uint32_t*>(ws + W.ready)};
-        factor_body<kCDK, kCDV, TIn, TG, true>(d, &tm_q, &tm_k, &tm_v, &tm_g, beta, ws, smem_raw, plan);
+                            (int)gridDim.x - nc, reinterpret_cast<uint32_t*>(ws + W.ready), true};
+        factor_body<kCDK, kCDV, TIn, TG>(d, &tm_q, &tm_k, &tm_v, &tm_g, beta, ws, smem_raw, plan);
     }
+}
+
+// The split pipeline's 128-column chain kernel: the fused kernel's chain role over
+// factor blocks that the factor kernel has finished; runs only when the schedule
+// kernel chose it for these chain lengths.
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads, 1)
+    chain128_kernel(Dims d, const float* __restrict__ h0, float scale, TIn* __restrict__ o,
+                    float* __restrict__ hT, uint8_t* __restrict__ ws) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const WsLayout W(d);
+    if (!reinterpret_cast<const Header*>(ws + W.header)->chain128) return;
+    chain_role<TIn>(d, h0, scale, o, hT, ws, smem_raw, (int)gridDim.x, false);
+}
+
+template <typename TIn>
+cudaError_t launch_chain128_t(const Dims& d, const float* h0, float scale, void* o, float* hT, uint8_t* ws,
+                              cudaStream_t stream) {
+    auto kern = chain128_kernel<TIn>;
+    const size_t smem = sizeof(ChainRoleSmem);
+    cudaError_t e = ensure_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    const long long chains = (long long)d.N * d.H;
+    if (chains == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)(chains < num_sms() ? chains : num_sms());
+    kern<<<grid, kThreads, smem, stream>>>(d, h0, scale, static_cast<TIn*>(o), hT, ws);
+    return cudaGetLastError();
 }
 
 template <typename TIn>
@@ -559,6 +592,15 @@ int fused_grid(const Dims& d) {
 float fused_ratio(const Dims& d, bool qkv_bf16) {
     (void)d;
     return qkv_bf16 ? 4.f : 5.f;
+}
+
+bool chain128_applies(const Dims& d) { return d.dk == kCDK && d.dv == kCDV && d.N <= kRankMax; }
+
+cudaError_t launch_chain128(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
+                            float* hT, uint8_t* ws, cudaStream_t stream) {
+    if (!chain128_applies(d)) return cudaErrorInvalidValue;
+    return qkv_bf16 ? launch_chain128_t<__nv_bfloat16>(d, h0, scale, o, hT, ws, stream)
+                    : launch_chain128_t<float>(d, h0, scale, o, hT, ws, stream);
 }
 
 cudaError_t launch_fused(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,

@@ -118,6 +118,8 @@ struct Header {
     int32_t total_chunks;
     int32_t next_item;  // work counter of the persistent state kernel (reset per call)
     int32_t n_chain;    // fused pipeline: CTAs that run state chains (0: none)
+    int32_t chain128;   // split pipeline: 1 when the 128-column chain kernel runs the
+                        // state recurrence (and the factors' u is in its layout)
 };
 
 // Longest-first ranking covers up to this many sequences (identity order beyond);
@@ -138,13 +140,27 @@ cudaError_t ensure_smem(Kernel kern, size_t bytes) {
 }
 
 // Launchers (each enqueues on `stream`; return cudaGetLastError()).
-cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
-                            cudaStream_t stream);
+// Split pipeline.  c128_mode: 0, the tiled state kernel runs (value tiles of
+// split_nv_for columns); 1, the 128-column chain kernel runs; 2 (varlen, dk = dv =
+// 128), the schedule kernel picks one of the two from the chain lengths and the
+// other leaves at once.
+cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws, int split_nv,
+                            int c128_mode, cudaStream_t stream);
+// For equal-length chains (a fixed-length batch or one sequence): whether the
+// 128-column chain kernel is predicted faster.
+bool chain128_pick_uniform(const Dims& d);
 cudaError_t launch_prep_tc(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,
                            const void* v, const void* g, const float* beta, uint8_t* ws,
                            cudaStream_t stream);
 cudaError_t launch_chain(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                          float* hT, uint8_t* ws, cudaStream_t stream);
+// Value-tile width of the split state kernel for these sizes (16, 32 or 64).
+int split_nv_for(const Dims& d);
+// The split pipeline's 128-column chain kernel (dk = dv = 128), which runs only when
+// the schedule kernel chose it (Header::chain128); and whether it applies at all.
+cudaError_t launch_chain128(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
+                            float* hT, uint8_t* ws, cudaStream_t stream);
+bool chain128_applies(const Dims& d);
 
 // Fused pipeline.  The schedule kernel, given fused_grid > 0, also picks how many of
 // the fused kernel's fused_grid CTAs run state chains (production_ratio: the time to

@@ -57,9 +57,13 @@ __device__ int block_scan(int x, int* warp_sums, int* carry) {
 // fused_grid > 0: also Header::n_chain, the production order and cleared ready
 // flags for a fused kernel of fused_grid CTAs (needs d.N <= kRankMax).  ratio: the
 // time to produce one item's factors over the time of one chain step.
+// Header::chain128 (split pipeline): c128_mode 0 or 1 sets it as given; 2 (varlen,
+// dk = dv = 128) decides between the state kernel with split_nv-column tiles and the
+// 128-column chain kernel from their predicted times on these chain lengths.
 __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_t* cu,
                                                             uint8_t* ws, int fused_grid,
-                                                            float ratio) {
+                                                            float ratio, int split_nv, int c128_mode,
+                                                            int sms) {
     WsLayout L(d);
     Header* hdr = reinterpret_cast<Header*>(ws + L.header);
     int32_t* seq_first = reinterpret_cast<int32_t*>(ws + L.seq_first);
@@ -93,6 +97,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
             hdr->total_chunks = 0;
             hdr->next_item = 0;
             hdr->n_chain = 0;
+            hdr->chain128 = 0;
         }
         return;
     }
@@ -140,6 +145,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         hdr->total_chunks = carry;
         hdr->next_item = 0;
         hdr->n_chain = 0;
+        hdr->chain128 = c128_mode == 1 ? 1 : 0;
     }
     __syncthreads();
     // the chunk table, one thread per chunk: its sequence is the last one whose first
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     } else {
         for (int s = tid; s < d.N; s += kThreads) order[s] = s;
     }
-    if (fused_grid <= 0 || !small) return;
+    if ((fused_grid <= 0 && c128_mode != 2) || !small) return;
 
     // ---- fused pipeline.  Chain r = rank * H + head (one chain per sequence and
     // head); chain CTA x takes chains x, x + n_chain, ... (round k = r / n_chain), so
@@ -192,6 +198,36 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     __syncthreads();
     auto rc0 = [&](int rk) { return s_rc0[rk]; };
     auto rcntf = [&](int rk) { return s_rcnt[rk]; };
+    if (fused_grid <= 0) {
+        // ---- split pipeline: which state kernel.  Per-step times measured on GB300:
+        // 2.5 us for a 128-column chain step, 2.0 / 1.55 / 1.42 us for a 64 / 32 / 16
+        // column one.  The 128-column kernel gives CTA x chains x, x + G, ... (G CTAs;
+        // CTA 0, with the longest of each round, finishes last); the tiled kernel takes
+        // its (chain, tile) items longest first from a counter, bounded by the longest
+        // chain or by its share of all the steps.
+        __shared__ int steps128;
+        const int H = d.H, R = d.N * d.H;
+        const int G = R < sms ? R : sms;
+        if (tid == 0) steps128 = 0;
+        __syncthreads();
+        if (tid < 32 && G > 0) {
+            int sum = 0;
+            for (int k = tid; k * G < R; k += 32) sum += rcntf((k * G) / H);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (tid == 0) steps128 = sum;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const float t128 = 2.5f * (float)steps128;
+            const float per = split_nv == 64 ? 2.0f : (split_nv == 32 ? 1.55f : 1.42f);
+            const float share = (float)carry * H * (float)(d.dv / split_nv) / (float)sms;
+            const float longest = d.N > 0 ? (float)rcntf(0) : 0.f;
+            const float tnv = per * (longest > share ? longest : share);
+            hdr->chain128 = t128 < 0.9f * tnv ? 1 : 0;
+        }
+        return;
+    }
     int* const rf = s_rf;
     if (tid == 0) carry = 0;
     __syncthreads();
@@ -322,15 +358,30 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
 
 }  // namespace
 
-cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
-                            cudaStream_t stream) {
-    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, 0, 0.f);
+cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws, int split_nv,
+                            int c128_mode, cudaStream_t stream) {
+    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, 0, 0.f, split_nv, c128_mode, num_sms());
     return cudaGetLastError();
+}
+
+// The same prediction as the schedule kernel's, for chains of equal length.
+bool chain128_pick_uniform(const Dims& d) {
+    const long long nch = ((long long)d.T + kChunk - 1) / kChunk;  // chunks per chain
+    const long long R = (long long)d.N * d.H;
+    const int sms = num_sms();
+    if (R == 0 || nch == 0) return false;
+    const long long G = R < sms ? R : sms;
+    const float t128 = 2.5f * (float)(((R + G - 1) / G) * nch);
+    const int nv = split_nv_for(d);
+    const float per = nv == 64 ? 2.0f : (nv == 32 ? 1.55f : 1.42f);
+    const float share = (float)(R * nch) * (float)(d.dv / nv) / (float)sms;
+    const float tnv = per * ((float)nch > share ? (float)nch : share);
+    return t128 < 0.9f * tnv;
 }
 
 cudaError_t launch_schedule_fused(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
                                   int fused_grid, float production_ratio, cudaStream_t stream) {
-    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, fused_grid, production_ratio);
+    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, fused_grid, production_ratio, 0, 0, 0);
     return cudaGetLastError();
 }
 

@@ -105,7 +105,8 @@ const char* kda_status_string(kda_status status);
 
 /* Number of kernel launches kda_fwd enqueues for these sizes under the current
  * pipeline setting (for launch counts): 2 with the fused pipeline (schedule, fused),
- * 3 with the split one (schedule, factors, state). */
+ * 3 with the split one (schedule, factors, state), 4 when the split pipeline leaves
+ * the choice of state kernel to the device (both launched). */
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /*
@@ -147,8 +148,13 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
  *     over whole (sequence, head) chains, consuming each chunk's factors as soon as
  *     they are published.  Applies to dk = dv = 128, batches of at most 2048
  *     sequences and 65536 (sequence, head) pairs, on a device with 2 to 1025 SMs.
- *   split: a schedule kernel, a factor kernel over every chunk, then a state kernel
- *     over (sequence, head, value-column tile) chains.  Applies to every size.
+ *   split: a schedule kernel, a factor kernel over every chunk, then a state kernel:
+ *     over (sequence, head, value-column tile) chains, or, with dk = dv = 128 where
+ *     that is predicted faster, over whole (sequence, head) chains of 128 columns.
+ *     The state kernel is chosen on the host for equal-length chains and by the
+ *     schedule kernel from the chain lengths for varlen batches of at least 512
+ *     (sequence, head) pairs (both are then launched; the one not chosen leaves at
+ *     once).  Applies to every size.
  * KDA_PIPELINE_AUTO (default) takes the fused pipeline where it applies and was
  * measured faster on GB300: fixed-length batches (or a single sequence) with
  * 32 <= B * H <= 256; every other size takes the split one.  KDA_PIPELINE_FUSED

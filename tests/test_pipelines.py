@@ -52,8 +52,10 @@ def test_pipeline_selection(kda):
     assert not kda.uses_fused(16, 8192, 32, 128, 128, 16)       # B * H = 512
     assert not kda.uses_fused(1, 8192, 32, 128, 128, 8)         # varlen
     assert not kda.uses_fused(1, 256, 32, 64, 64, 1)            # dk = dv = 64
-    assert kda.launch_count(1, 8192, 32, 128, 128, 1) == 2
-    assert kda.launch_count(1, 8192, 32, 128, 128, 8) == 3
+    assert kda.launch_count(1, 8192, 32, 128, 128, 1) == 2           # schedule, fused
+    assert kda.launch_count(1, 8192, 32, 128, 128, 8) == 3           # varlen, 256 chains
+    assert kda.launch_count(1, 8192, 32, 128, 128, 16) == 4          # varlen, 512: both state kernels
+    assert kda.launch_count(1, 256, 32, 64, 64, 1) == 3
     kda.set_pipeline("fused")
     try:
         assert kda.get_pipeline() == "fused"
@@ -67,7 +69,7 @@ def test_pipeline_selection(kda):
     kda.set_pipeline("split")
     try:
         assert not kda.uses_fused(1, 8192, 32, 128, 128, 1)
-        assert kda.launch_count(1, 8192, 32, 128, 128, 1) == 3
+        assert kda.launch_count(1, 8192, 32, 128, 128, 1) == 3           # one state kernel
     finally:
         kda.set_pipeline("auto")
     with pytest.raises(ValueError):
@@ -162,6 +164,49 @@ def test_fused_pipeline_fp32_inputs(fused):
     x = gen.make_cfg1(seed=17, salt=SALT, T=300, H=4, d=128)
     assert fused.uses_fused(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs)
     _assert_parity(x, *_gpu(fused, x))
+
+
+def _chain128_chosen(kda, x):
+    """Runs the forward with an explicit workspace and reads the schedule kernel's
+    choice of state kernel (the header's fifth word)."""
+    xd = x.to("cuda")
+    ws = torch.empty(kda.workspace_size(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs) + 256,
+                     dtype=torch.uint8, device="cuda")
+    o, hT = kda.fwd(**xd.tensors(), workspace=ws, check=True)
+    torch.cuda.synchronize()
+    base = (-ws.data_ptr()) % 256
+    word = int(ws[base + 16:base + 20].cpu().numpy().view("int32")[0])
+    return o.cpu(), hT.cpu(), word
+
+
+def test_split_pipeline_chain128_fixed(kda):
+    """B * H = 512 chains of 8 chunks: the split pipeline with the 128-column chain
+    kernel alone (predicted 80 us against 108 us for 64-column tiles)."""
+    x = gen.make_cfg2(seed=18, salt=SALT, T=512, H=64, B=8)
+    assert not kda.uses_fused(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs)
+    assert kda.launch_count(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs) == 3
+    o, hT, chosen = _chain128_chosen(kda, x)
+    assert chosen == 1
+    _assert_parity(x, o, hT, heads=[0, 31, 63])
+
+
+def test_split_pipeline_chain128_varlen(kda):
+    """Many varlen chains, empty sequences included, through the 128-column chain
+    kernel when the schedule picks it; parity either way."""
+    lens = [150, 0, 77, 300, 1, 64, 129, 200] * 24
+    x = gen.make_lengths(lens, seed=19, salt=SALT, H=8, d=128)
+    assert x.num_seqs * x.H >= 512
+    o, hT, chosen = _chain128_chosen(kda, x)
+    assert chosen == 1
+    _assert_parity(x, o, hT)
+
+
+def test_split_pipeline_tiled_state_kernel_when_few_chains(kda):
+    """Few long chains: the schedule keeps the tiled state kernel."""
+    x = gen.make_cfg2(seed=20, salt=SALT, T=2048, H=16, B=1)
+    o, hT, chosen = _chain128_chosen(kda, x)
+    assert chosen == 0
+    _assert_parity(x, o, hT, heads=[0, 15])
 
 
 def test_fused_and_split_agree(kda):
