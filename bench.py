@@ -43,11 +43,18 @@ WORKLOADS = {
     "cfg4": "varlen skewed 8192 tokens in 32 sequences (one ~5000), H=32, d=128, extreme-value probes",
 }
 KERNEL_NAMES = {"fused": ["schedule", "fused"],
-                "split": ["schedule", "factors", "state_recurrence", "state_recurrence_128"]}
+                "split": ["schedule", "factors", "state_recurrence", "state_recurrence_128"],
+                # few long chains: the segmented recurrence (pass A, scan, pass C), with
+                # the tiled state kernel before it when the schedule decides on the device
+                "split-seg": ["schedule", "factors", "segments_a", "segments_scan", "segments_c"],
+                "split-seg-decide": ["schedule", "factors", "state_recurrence", "segments_a",
+                                     "segments_scan", "segments_c"]}
+STATE_KERNELS = ("state_recurrence", "state_recurrence_128", "segments_a", "segments_c")
 
 
 def make_workload(name: str, seed: int, salt: int):
-    """cfg2 (default), cfg3, cfg4, or a throughput-sweep row cfg5-{fixed|varlen}-H{H}-{total}."""
+    """cfg2 (default), cfg3, cfg4, a throughput-sweep row cfg5-{fixed|varlen}-H{H}-{total},
+    or long-B{B}-H{H}-{T} (fixed length, few long chains)."""
     if name == "cfg2":
         return gen.make_cfg2(seed=seed, salt=salt), WORKLOADS[name]
     if name == "cfg2-gbf16":
@@ -66,6 +73,12 @@ def make_workload(name: str, seed: int, salt: int):
                 f"({'B=' + str(total_ // 8192) + ' x 8192' if kind == 'fixed' else str(x.num_seqs) + ' sequences'}; "
                 "heads 0-1 drawn from the recipe, the others token-rolled copies of them)")
         return x, desc
+    if name.startswith("long-"):
+        _, bs, hs, ts = name.split("-")
+        B_, H_, T_ = int(bs[1:]), int(hs[1:]), int(ts)
+        desc = (f"few long chains: fixed-length B={B_} T={T_} H={H_} dk=dv=128 bf16 q/k/v, "
+                "fp32 g/beta/h0 (the cfg2 recipe)")
+        return gen.make_cfg2(seed=seed, salt=salt, T=T_, H=H_, B=B_), desc
     raise ValueError(f"unknown workload {name}")
 
 
@@ -85,7 +98,7 @@ def _algorithmic_bytes(kernel: str, tokens: int, heads: int, dk: int, dv: int, n
     th = tokens * heads
     if kernel == "factors":       # reads q, k, v, g, beta
         return th * (2 * dk * 2 + dv * 2 + dk * g_bytes + 4)
-    if kernel in ("state_recurrence", "state_recurrence_128"):  # writes o; reads h0, writes hT
+    if kernel in STATE_KERNELS:   # writes o; reads h0, writes hT (a segment pass: charged the whole)
         return th * dv * 2 + 2 * nseq * heads * dk * dv * 4
     if kernel == "fused":         # the whole path: both of the above
         return _path_bytes(tokens, heads, dk, dv, nseq, g_bytes)
@@ -364,13 +377,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pipeline", default="auto", choices=["auto", "fused", "split"],
+    ap.add_argument("--pipeline", default="auto", choices=["auto", "fused", "split", "split-whole"],
                     help="auto (default): the library's choice for the sizes; fused: factor "
                          "production and state chains in one kernel; split: a factor kernel, "
-                         "then a state kernel")
+                         "then the state kernels (few long chains cut into segments where "
+                         "predicted faster); split-whole: split, chains never cut")
     ap.add_argument("--workload", default="cfg2",
                     help="cfg2 (the headline workload), cfg2-gbf16 (bf16 gate), cfg3, cfg4, "
-                         "cfg5-{fixed|varlen}-H{16|32|64}-{total}, "
+                         "cfg5-{fixed|varlen}-H{16|32|64}-{total}, long-B{B}-H{H}-{T} "
+                         "(few long fixed-length chains), "
                          "decode-N{sequences}-H{heads}")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -409,8 +424,10 @@ def main():
     hT = torch.empty_like(xd.h0)
     ws = torch.empty(kda.workspace_size(B, T, H, D, D, nseq) + 256, dtype=torch.uint8, device=dev)
     nl = kda.launch_count(B, T, H, D, D, nseq)
-    pipeline = "fused" if kda.uses_fused(B, T, H, D, D, nseq) else "split"
-    names = KERNEL_NAMES[pipeline]
+    fused = kda.uses_fused(B, T, H, D, D, nseq)
+    pipeline = "fused" if fused else ("split-whole" if args.pipeline == "split-whole" else "split")
+    names = KERNEL_NAMES["fused" if fused else "split" if nl < 5 else
+                         ("split-seg" if nl == 5 else "split-seg-decide")]
     stream = torch.cuda.current_stream(dev)
 
     def step(events=None):
@@ -467,7 +484,7 @@ def main():
     if rank == 0:
         import oracle
         from tests.metrics import rel_rmse
-        hs = [0, x2.H // 2 + 1]
+        hs = sorted({0, min(x2.H - 1, x2.H // 2 + 1)})
         t = x2.tensors()
         for key in ("q", "k", "v", "g", "beta"):
             t[key] = t[key][:, :, hs].contiguous()

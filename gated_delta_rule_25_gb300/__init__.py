@@ -96,14 +96,16 @@ def launch_count(B: int, T: int, H: int, dk: int, dv: int, num_seqs: int) -> int
     return int(load_library().kda_fwd_launch_count(B, T, H, dk, dv, num_seqs))
 
 
-PIPELINES = {"auto": 0, "fused": 1, "split": 2}
+PIPELINES = {"auto": 0, "fused": 1, "split": 2, "split-whole": 3}
 
 
 def set_pipeline(name: str) -> None:
     """Selects the forward's pipeline, process-wide: "auto" (default: the fused one
     where it applies and was measured faster, else split), "fused" (one cooperative
     kernel producing factors and running the state chains at once, wherever the
-    sizes allow) or "split" (a factor kernel, then a state kernel)."""
+    sizes allow), "split" (a factor kernel, then the state kernels; few long chains
+    cut into segments where predicted faster) or "split-whole" (split, chains never
+    cut)."""
     if name not in PIPELINES:
         raise ValueError(f"pipeline must be one of {sorted(PIPELINES)}, got {name!r}")
     load_library().kda_set_pipeline(PIPELINES[name])

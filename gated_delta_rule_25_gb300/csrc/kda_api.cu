@@ -54,7 +54,7 @@ std::atomic<int> g_pipeline{KDA_PIPELINE_AUTO};
 // gives up cost more than the chains gain, run faster split).
 int pipeline_grid(const kda::Dims& d) {
     const int p = g_pipeline.load();
-    if (p == KDA_PIPELINE_SPLIT) return 0;
+    if (p == KDA_PIPELINE_SPLIT || p == KDA_PIPELINE_SPLIT_WHOLE) return 0;
     const int grid = kda::fused_grid(d);
     if (grid == 0 || p == KDA_PIPELINE_FUSED) return grid;
     const long long pairs = (long long)d.N * d.H;
@@ -72,6 +72,19 @@ int c128_mode(const kda::Dims& d) {
     if (!kda::chain128_applies(d)) return 0;
     if (d.varlen && d.N > 1) return (long long)d.N * d.H >= 512 ? 2 : 0;
     return kda::chain128_pick_uniform(d) ? 1 : 0;
+}
+
+// Segmented chains (split pipeline, few long chains, a workspace with the segment
+// region): the segment length for equal-length chains (0: none), or -1 for varlen
+// batches long enough that segments may pay, decided on the device from the lengths
+// (the tiled state kernel and the segment kernels are then all launched; those not
+// chosen leave at once).
+int seg_mode(const kda::Dims& d, size_t workspace_bytes) {
+    if (g_pipeline.load() == KDA_PIPELINE_SPLIT_WHOLE) return 0;
+    if (!kda::seg_layout_applies(d) || d.N > kda::kRankMax) return 0;
+    if (workspace_bytes < kda::WsLayout(d).total_seg) return 0;
+    if (!d.varlen || d.N == 1) return kda::seg_pick_uniform(d);
+    return (long long)d.T >= 32LL * kda::kChunk ? -1 : 0;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -101,22 +114,25 @@ size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs)
     // B == 1 may be either layout; the varlen bound (T/64 + N chunks) covers both.
     kda::Dims d;
     if (make_dims(B, T, H, dk, dv, num_seqs, B == 1, d) != KDA_OK) return 0;
-    return kda::WsLayout(d).total;
+    return kda::WsLayout(d).total_seg;
 }
 
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs) {
-    // schedule, fused; or schedule, factors, a state kernel (varlen batches with
-    // dk = dv = 128: both state kernels, one of them leaving at once)
+    // schedule, fused; or schedule, factors, then the state kernels (see fwd_impl)
     if (kda_fwd_uses_fused(B, T, H, dk, dv, num_seqs)) return 2;
     kda::Dims d;
     if (make_dims(B, T, H, dk, dv, num_seqs, B == 1 && num_seqs != B, d) != KDA_OK) return 3;
+    const int seg = seg_mode(d, kda::WsLayout(d).total_seg);
+    if (seg > 0) return 5;   // schedule, factors, pass A, scan, pass C
+    if (seg < 0) return 6;   // ... and the tiled state kernel before the passes
     return c128_mode(d) == 2 ? 4 : 3;
 }
 
 void kda_set_pipeline(kda_pipeline pipeline) {
-    g_pipeline.store(pipeline == KDA_PIPELINE_SPLIT ? KDA_PIPELINE_SPLIT
-                     : pipeline == KDA_PIPELINE_FUSED ? KDA_PIPELINE_FUSED
-                                                      : KDA_PIPELINE_AUTO);
+    g_pipeline.store(pipeline == KDA_PIPELINE_SPLIT          ? KDA_PIPELINE_SPLIT
+                     : pipeline == KDA_PIPELINE_SPLIT_WHOLE ? KDA_PIPELINE_SPLIT_WHOLE
+                     : pipeline == KDA_PIPELINE_FUSED       ? KDA_PIPELINE_FUSED
+                                                            : KDA_PIPELINE_AUTO);
 }
 
 kda_pipeline kda_get_pipeline(void) { return static_cast<kda_pipeline>(g_pipeline.load()); }
@@ -179,12 +195,21 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
     // chains where that is predicted faster (decided here for equal-length chains,
     // by the schedule kernel from the lengths for varlen batches, in which case both
     // kernels are launched and the one not chosen leaves at once)
+    // (or, for few long chains, on segments: seg_mode)
     const int mode = c128_mode(d);
-    if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, kda::split_nv_for(d), mode, s) != cudaSuccess)
+    const int seg = seg_mode(d, workspace_bytes);
+    if (!mark() || kda::launch_schedule(d, cu_seqlens, ws, kda::split_nv_for(d), mode, seg, s) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (!mark() || kda::launch_prep_tc(d, bf16, gbf, q, k, v, g, beta, ws, s) != cudaSuccess)
         return KDA_ERR_CUDA;
     cudaError_t ce;
+    if (seg > 0) {
+        if (!mark() || kda::launch_seg_pass(d, bf16, 0, h0, scale, o, hT, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark() || kda::launch_seg_scan(d, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark() || kda::launch_seg_pass(d, bf16, 1, h0, scale, o, hT, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark()) return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
     if (mode != 1) {
         if (!mark()) return KDA_ERR_CUDA;
         ce = kda::launch_chain(d, bf16, h0, scale, o, hT, ws, s);
@@ -194,6 +219,11 @@ kda_status fwd_impl(const void* q, const void* k, const void* v, kda_dtype qkv_d
         if (!mark()) return KDA_ERR_CUDA;
         ce = kda::launch_chain128(d, bf16, h0, scale, o, hT, ws, s);
         if (ce != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    if (seg < 0) {
+        if (!mark() || kda::launch_seg_pass(d, bf16, 0, h0, scale, o, hT, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark() || kda::launch_seg_scan(d, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark() || kda::launch_seg_pass(d, bf16, 1, h0, scale, o, hT, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (!mark()) return KDA_ERR_CUDA;
     return KDA_OK;

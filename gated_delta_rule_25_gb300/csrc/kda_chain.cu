@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int4* chunks = reinterpret_cast<const int4*>(ws + W.chunks);
     const int n_items = d.N * d.H * NVT;
     volatile int* abort = &sm.abort;
-    if (hdr->chain128) return;  // the 128-column chain kernel runs the recurrence instead
+    if (hdr->chain128 || hdr->seg) return;  // the 128-column or segmented chains run it instead
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {

@@ -63,8 +63,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const float* __restrict__ beta, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // the 128-column chain kernel, when it runs, reads u in its own layout
-    const bool ut = DK == 128 && DV == 128 && reinterpret_cast<const Header*>(ws + WsLayout(d).header)->chain128;
+    // the 128-column chain kernel and the segment passes, when they run, read u in
+    // their own layout
+    const Header* hdr = reinterpret_cast<const Header*>(ws + WsLayout(d).header);
+    const bool ut = DK == 128 && DV == 128 && (hdr->chain128 || hdr->seg);
     factor_body<DK, DV, TIn, TG>(d, &tm_q, &tm_k, &tm_v, &tm_g, beta, ws, smem_raw,
                                  ItemPlan{nullptr, (int)blockIdx.x, (int)gridDim.x, nullptr, ut});
 }

@@ -61,21 +61,35 @@ __device__ __forceinline__ void chain_raise(uint8_t* ws, volatile int* abort) {
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16(x); }
 __device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
 
-// A position in this CTA's chains: chain r = rank * H + head (ranks longest first);
-// the CTA takes chains first, first + nc, ...; j is the step (chunk) in the chain.
+// A position in this CTA's chains: chain r = rank * H + head (ranks longest first),
+// or task r of a segment pass; the CTA takes chains first, first + nc, ...; j is the
+// step (chunk) in the chain.
 struct ChainPos {
     int r, s, h, c0, len, j;
-    int tok0, ntok;  // the sequence's first token row and its tokens
+    int tok0, ntok;  // the chain's first token row and its tokens
+    int w;           // segment task: kind | last << 3 | slot << 4 (kTaskWhole otherwise)
 };
+
+// A segment pass: its tasks and the segment buffers (dk x dv fp32 each).
+struct SegRun {
+    const int4* tasks;
+    int ntasks;
+    float* E;  // segment start states, row-major (and, before the scan, the middle segments' Z)
+    float* F;  // the middle segments' maps, transposed: F^T[m][r] = F[r][m]
+};
+
+// Where a task's chain starts and where its final state goes.
+__device__ __forceinline__ bool task_outputs(int w) { return (w & 7) != kTaskMapF && (w & 7) != kTaskMapZ; }
 
 // nc: the chain CTAs (this one is blockIdx.x among them).  use_flags: the factor
 // blocks are published as the pipeline runs (fused kernel); false when they were all
 // written before this kernel started (the split pipeline's 128-column chain kernel).
-template <typename TOut>
+// kSeg: the chains are the tasks of a segment pass (seg).
+template <typename TOut, bool kSeg = false>
 __device__ __forceinline__ void chain_role(const Dims& d, const float* __restrict__ h0, float scale,
                                            TOut* __restrict__ o, float* __restrict__ hT,
                                            uint8_t* __restrict__ ws, uint8_t* smem_raw, int nc,
-                                           bool use_flags) {
+                                           bool use_flags, const SegRun* seg = nullptr) {
     constexpr int DK = kCDK, DV = kCDV;
     ChainRoleSmem& sm = *reinterpret_cast<ChainRoleSmem*>(smem_raw);
     constexpr uint32_t WQB = 2 * kChunk * DK * 2, KTB = DK * kChunk * 4, PB = kChunk * kChunk * 2,
@@ -92,7 +106,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     const int32_t* order = reinterpret_cast<const int32_t*>(ws + W.order);
     const int4* chunk_tab = reinterpret_cast<const int4*>(ws + W.chunks);
     const uint32_t* ready = reinterpret_cast<const uint32_t*>(ws + W.ready);
-    const int H = d.H, R = d.N * d.H;
+    const int H = d.H, R = kSeg ? seg->ntasks : d.N * d.H;
     volatile int* abort = &sm.abort;
 
     if (tid == 0) {
@@ -119,7 +133,22 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     const uint32_t tmem = sm.tmem;
 
     auto chain_at = [&](int r) {
-        ChainPos p{r, 0, 0, 0, 0, 0, 0, 0};
+        ChainPos p{r, 0, 0, 0, 0, 0, 0, 0, kTaskWhole};
+        if (kSeg) {
+            if (r < R) {
+                const int4 t = seg->tasks[r];
+                p.c0 = t.x;
+                p.len = t.y;
+                p.s = t.z / H;
+                p.h = t.z - p.s * H;
+                p.w = t.w;
+                if (p.len > 0) {
+                    p.tok0 = chunk_tab[p.c0].y;
+                    p.ntok = kChunk * (p.len - 1) + chunk_tab[p.c0 + p.len - 1].z;
+                }
+            }
+            return p;
+        }
         if (r < R) {
             p.h = r % H;
             p.s = order[r / H];
@@ -229,6 +258,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
     // the last reader, is done) and nothing else reads it, so its lines leave L2
     // without being written back.
     auto drop_prev_block = [&]() {
+        if (kSeg && !task_outputs(prev_pos.w)) return;  // a map task: the tail task reads it again
         const uint8_t* blk = block_of(prev_pos);
         for (int i = tid; i < (int)(W.factor_bytes / 128); i += kThreads) ptx::discard_l2_line(blk + 128 * i);
     };
@@ -267,8 +297,17 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         // -------- a new chain: its initial state into S^T and the bf16 copy
         if (cur.j == 0) {
             const size_t base = ((size_t)cur.s * H + cur.h) * DK * DV;
+            const float* src = h0 ? h0 + base : nullptr;
+            bool ident = false;
+            if (kSeg) {
+                const int kind = cur.w & 7;
+                if (kind == kTaskMapF || kind == kTaskMapZ) src = nullptr;
+                if (kind == kTaskMapF) ident = true;
+                if (kind == kTaskTail) src = seg->E + (size_t)(cur.w >> 4) * DK * DV;
+            }
 #pragma unroll
-            for (int e = 0; e < 32; ++e) S[e] = h0 ? h0[base + (size_t)(32 * g + e) * DV + n] : 0.f;
+            for (int e = 0; e < 32; ++e)
+                S[e] = ident ? (32 * g + e == n ? 1.f : 0.f) : src ? src[(size_t)(32 * g + e) * DV + n] : 0.f;
             uint32_t sb[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) sb[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
@@ -326,6 +365,10 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
                 uu[4 * k2] = un[k2].x; uu[4 * k2 + 1] = un[k2].y; uu[4 * k2 + 2] = un[k2].z; uu[4 * k2 + 3] = un[k2].w;
+            }
+            if (kSeg && (cur.w & 7) == kTaskMapF) {  // the map: the step without its u
+#pragma unroll
+                for (int e = 0; e < 16; ++e) uu[e] = 0.f;
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {  // minus both halves of (w S)^T
@@ -391,7 +434,7 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         // -------- output of the previous step into the staging tile, and its factor
         //          block out of L2 (its GEMM3 was waited for before the barrier), while
         //          GEMM2 runs
-        if (have_prev) {
+        if (have_prev && (!kSeg || task_outputs(prev_pos.w))) {
             ptx::tc_fence_after();
             out_stage(b ^ 1u);
             drop_prev_block();
@@ -420,10 +463,25 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
             for (int i = 0; i < 16; ++i) sb[i] = pack_bf16(S[2 * i], S[2 * i + 1]);
             ptx::tmem_st16(tmem + lb + kTS + 16 * g, sb);
             ptx::tmem_st_wait();
-            if (hT && cur.j == cur.len - 1) {  // the chain's last chunk: its final state
-                const size_t base = ((size_t)cur.s * H + cur.h) * DK * DV;
+            if (cur.j == cur.len - 1) {  // the chain's last chunk: its final state
+                float* dst = hT ? hT + ((size_t)cur.s * H + cur.h) * DK * DV : nullptr;
+                if (kSeg) {
+                    const int kind = cur.w & 7;
+                    const size_t slot = (size_t)(cur.w >> 4) * DK * DV;
+                    if (kind == kTaskHead || kind == kTaskMapZ) dst = seg->E + slot;
+                    if (kind == kTaskTail && !((cur.w >> 3) & 1)) dst = nullptr;  // the scan made it
+                    if (kind == kTaskMapF) {  // the map, transposed: F^T[n][c], 32 floats per thread
+                        float4* ft = reinterpret_cast<float4*>(seg->F + slot + (size_t)n * DK + 32 * g);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) hT[base + (size_t)(32 * g + e) * DV + n] = S[e];
+                        for (int e = 0; e < 8; ++e)
+                            ft[e] = make_float4(S[4 * e], S[4 * e + 1], S[4 * e + 2], S[4 * e + 3]);
+                        dst = nullptr;
+                    }
+                }
+                if (dst) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dst[(size_t)(32 * g + e) * DV + n] = S[e];
+                }
             }
         }
         ptx::tc_fence_before();
@@ -447,8 +505,10 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
         ok = __syncthreads_and(okl);  // the tile is free again
         if (ok) {
             ptx::tc_fence_after();
-            out_stage((gj - 1) & 1u);
-            drop_prev_block();
+            if (!kSeg || task_outputs(prev_pos.w)) {
+                out_stage((gj - 1) & 1u);
+                drop_prev_block();
+            }
         } else {
             chain_raise(ws, abort);
         }
@@ -535,6 +595,145 @@ cudaError_t launch_chain128_t(const Dims& d, const float* h0, float scale, void*
     return cudaGetLastError();
 }
 
+// A pass of segmented chains (the split pipeline for few long chains): pass 0 runs
+// the first segments from h0 and the middle segments' maps F and states from zero Z;
+// pass 1 the segments after the first from the start states the scan made.  Each
+// task is a chain of the chain role; runs only when the schedule kernel chose
+// segments.
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads, 1)
+    seg_chain_kernel(Dims d, const float* __restrict__ h0, float scale, TIn* __restrict__ o,
+                     float* __restrict__ hT, uint8_t* __restrict__ ws, int pass) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const WsLayout W(d);
+    const Header* hdr = reinterpret_cast<const Header*>(ws + W.header);
+    if (!hdr->seg) return;
+    const SegRun run{reinterpret_cast<const int4*>(ws + (pass ? W.seg_c : W.seg_a)),
+                     pass ? hdr->seg_nc : hdr->seg_na, reinterpret_cast<float*>(ws + W.seg_e),
+                     reinterpret_cast<float*>(ws + W.seg_f)};
+    chain_role<TIn, true>(d, h0, scale, o, hT, ws, smem_raw, (int)gridDim.x, false, &run);
+}
+
+// The scan between the passes: for every chain with three or more segments, the
+// start state of segment k + 1 is F_k E_k + Z_k (k = 1 .. segments - 2), E_1 being
+// the first segment's final state; Z_k is overwritten by the result.  The value
+// columns are independent, so each CTA takes one 16-column tile of one chain and
+// walks its segments in order, in fp32: F_k^T arrives in shared memory by one bulk
+// copy (two buffers: the maps do not depend on the scan, so the next one loads
+// while a step computes) and the tile stays in shared memory.  The sum over m is
+// split in four quarters over the CTA's 16 warps (enough warps to hide the shared
+// memory latency); in each quarter a thread accumulates a 4 x 4 block (per m, a
+// float4 of F^T's row m and one of the tile's row m: conflict-free and broadcast),
+// and the four partial blocks are added with Z_k through shared memory.
+constexpr int kScanCols = 16, kScanThreads = 512, kScanK = 4;
+struct __align__(16) ScanSmem {
+    float FT[2][kCDK * kCDK];
+    float prev[kCDK][kScanCols];
+    float part[kScanK][kCDK][kScanCols];
+    uint64_t full[2];
+    int abort;
+};
+
+__global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t* __restrict__ ws) {
+    constexpr int DK = kCDK, DV = kCDV, kTiles = DV / kScanCols, kM = DK / kScanK;
+    constexpr uint32_t FB = DK * DK * 4;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    ScanSmem& sm = *reinterpret_cast<ScanSmem*>(smem_raw);
+    const WsLayout W(d);
+    Header* hdr = reinterpret_cast<Header*>(ws + W.header);
+    if (!hdr->seg) return;
+    const int i = (int)blockIdx.x / kTiles, col0 = kScanCols * ((int)blockIdx.x % kTiles);
+    if (i >= hdr->seg_ns) return;
+    const int4 e = reinterpret_cast<const int4*>(ws + W.seg_scan)[i];  // {pair, E slot, F slot, segments}
+    const int steps = e.w - 2;
+    float* E = reinterpret_cast<float*>(ws + W.seg_e);
+    const float* FT = reinterpret_cast<const float*>(ws + W.seg_f);
+    const int tid = threadIdx.x;
+    const int kq = tid >> 7, rg = tid & 31, cg = (tid >> 5) & 3;  // m quarter; rows 4 rg .., columns 4 cg ..
+    const int orow = tid >> 2, ocol = 4 * (tid & 3);                // the output float4 of this thread
+    uint32_t issued[2] = {0, 0};
+    if (tid == 0) {
+        ptx::mbar_init(&sm.full[0], 1);
+        ptx::mbar_init(&sm.full[1], 1);
+        sm.abort = 0;
+        ptx::fence_mbar_init();
+        // The maps and Z of the later steps into L2 now (pass A's factor reads may have
+        // pushed them out), each by one of the chain's tile CTAs.
+        const int tile = (int)blockIdx.x % kTiles;
+        for (int k = 3 + tile; k <= steps; k += kTiles) {
+            ptx::bulk_prefetch_l2(FT + (size_t)(e.z + k - 1) * DK * DK, FB);
+            ptx::bulk_prefetch_l2(E + (size_t)(e.y + k) * DK * DV, FB);
+        }
+        for (int k = 1; k <= 2 && k <= steps; ++k) {
+            ptx::mbar_arrive_expect_tx(&sm.full[k - 1], FB);
+            ptx::bulk_g2s(sm.FT[k - 1], FT + (size_t)(e.z + k - 1) * DK * DK, FB, &sm.full[k - 1]);
+            ++issued[k - 1];
+        }
+    }
+    *reinterpret_cast<float4*>(&sm.prev[orow][ocol]) =
+        *reinterpret_cast<const float4*>(E + (size_t)e.y * DK * DV + (size_t)orow * DV + col0 + ocol);
+    __syncthreads();
+    bool ok = true;
+    for (int k = 1; k <= steps; ++k) {
+        const int b = (k - 1) & 1;
+        float* Ek = E + (size_t)(e.y + k) * DK * DV + (size_t)orow * DV + col0 + ocol;
+        const float4 z = *reinterpret_cast<const float4*>(Ek);
+        ok = __syncthreads_and(ptx::mbar_wait_or_abort(&sm.full[b], ((k - 1) >> 1) & 1u, &sm.abort));
+        if (!ok) break;
+        float acc[4][4] = {};
+        const float* ft = sm.FT[b] + kq * kM * DK + 4 * rg;
+#pragma unroll 8
+        for (int m = 0; m < kM; ++m) {
+            const float4 f = *reinterpret_cast<const float4*>(ft + m * DK);
+            const float4 p = *reinterpret_cast<const float4*>(&sm.prev[kq * kM + m][4 * cg]);
+            const float fr[4] = {f.x, f.y, f.z, f.w}, pc[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(fr[r], pc[c], acc[r][c]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(&sm.part[kq][4 * rg + r][4 * cg]) =
+                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        __syncthreads();  // every partial block written; the previous start state and F buffer b read
+        float4 v = z;
+#pragma unroll
+        for (int q = 0; q < kScanK; ++q) {
+            const float4 p = *reinterpret_cast<const float4*>(&sm.part[q][orow][ocol]);
+            v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+        }
+        *reinterpret_cast<float4*>(&sm.prev[orow][ocol]) = v;
+        *reinterpret_cast<float4*>(Ek) = v;
+        if (tid == 0 && k + 2 <= steps) {  // the map after next into the buffer just read
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive_expect_tx(&sm.full[b], FB);
+            ptx::bulk_g2s(sm.FT[b], FT + (size_t)(e.z + k + 1) * DK * DK, FB, &sm.full[b]);
+            ++issued[b];
+        }
+        __syncthreads();  // the new start state complete; the partial blocks read
+    }
+    if (!ok && tid == 0) {  // a copy did not land in time: report, and let those in flight land
+        atomicOr(&hdr->error, kDevErrTimeout);
+        volatile int never = 0;
+        for (int b = 0; b < 2; ++b)
+            if (issued[b]) ptx::mbar_wait_or_abort(&sm.full[b], (issued[b] - 1) & 1u, &never);
+    }
+}
+
+template <typename TIn>
+cudaError_t launch_seg_pass_t(const Dims& d, int pass, const float* h0, float scale, void* o, float* hT,
+                              uint8_t* ws, cudaStream_t stream) {
+    auto kern = seg_chain_kernel<TIn>;
+    const size_t smem = sizeof(ChainRoleSmem);
+    cudaError_t e = ensure_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    const int sms = num_sms();
+    const unsigned grid = (unsigned)(sms < kSegTasks ? sms : kSegTasks);
+    kern<<<grid, kThreads, smem, stream>>>(d, h0, scale, static_cast<TIn*>(o), hT, ws, pass);
+    return cudaGetLastError();
+}
+
 template <typename TIn>
 constexpr size_t fused_smem() {
     return sizeof(FactorSmem<kCDK, kCDV, TIn>) > sizeof(ChainRoleSmem) ? sizeof(FactorSmem<kCDK, kCDV, TIn>)
@@ -601,6 +800,24 @@ cudaError_t launch_chain128(const Dims& d, bool qkv_bf16, const float* h0, float
     if (!chain128_applies(d)) return cudaErrorInvalidValue;
     return qkv_bf16 ? launch_chain128_t<__nv_bfloat16>(d, h0, scale, o, hT, ws, stream)
                     : launch_chain128_t<float>(d, h0, scale, o, hT, ws, stream);
+}
+
+cudaError_t launch_seg_pass(const Dims& d, bool qkv_bf16, int pass, const float* h0, float scale,
+                            void* o, float* hT, uint8_t* ws, cudaStream_t stream) {
+    if (!seg_layout_applies(d)) return cudaErrorInvalidValue;
+    return qkv_bf16 ? launch_seg_pass_t<__nv_bfloat16>(d, pass, h0, scale, o, hT, ws, stream)
+                    : launch_seg_pass_t<float>(d, pass, h0, scale, o, hT, ws, stream);
+}
+
+cudaError_t launch_seg_scan(const Dims& d, uint8_t* ws, cudaStream_t stream) {
+    if (!seg_layout_applies(d)) return cudaErrorInvalidValue;
+    const long long pairs = (long long)d.N * d.H;
+    if (pairs == 0) return cudaSuccess;
+    const size_t smem = sizeof(ScanSmem);
+    cudaError_t e = ensure_smem(seg_scan_kernel, smem);
+    if (e != cudaSuccess) return e;
+    seg_scan_kernel<<<(unsigned)(pairs * (kCDV / kScanCols)), kScanThreads, smem, stream>>>(d, ws);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_fused(const Dims& d, bool qkv_bf16, bool g_bf16, const void* q, const void* k,

@@ -9,6 +9,10 @@
 //                                 (chunk, head) items, each as chunk * H + head
 //   ready           u32[Cmax*H]:  per (chunk, head): 1 once its factors are published
 //   factors         per (chunk, head): the factors of the chunkwise form
+//   (segments, when they may apply: dk = dv = 128 and N * H <= kSegPairs)
+//   seg_a, seg_c    int4[kSegTasks] each: the two chain passes' task lists
+//   seg_scan        int4[kSegPairs]: the scan's (pair, E slot, F slot, segments)
+//   seg_e, seg_f    fp32[slots][dk * dv] each: segment start states and maps
 //
 // Per (chunk, head) factor block, every part a multiple of 256 bytes:
 //   WQ  [128 x dk] bf16, M-major operand layout: rows 0-63
@@ -48,6 +52,7 @@ constexpr int kNV = 32;  // value columns per state-recurrence chain
 // Device error word bits (mirrors of the KDA_DEVERR_* values of kda.h).
 constexpr unsigned kDevErrCuSeqlens = 0x1u;
 constexpr unsigned kDevErrTimeout = 0x2u;
+constexpr unsigned kDevErrPlan = 0x4u;
 
 // Element index of (row r, value column n) in the slabbed U0 block (fp32): one
 // slab of kChunk x kNV per value tile, inside it groups of 4 columns, each a
@@ -83,9 +88,32 @@ struct FactorLayout {
     }
 };
 
+// Exact inter-chunk split ("segments") of few long chains, in the split pipeline
+// (dk = dv = 128, at most kSegPairs (sequence, head) pairs): each chain is cut into
+// segments of L chunks; the chunk step S <- M_c S + D_c is affine, so a middle
+// segment k is the map S -> F_k S + Z_k (F_k the product of its M_c, Z_k its state
+// from zero).  Pass A runs segment 0 from h0 and F_k, Z_k of the middle segments,
+// all at once; a scan then gives every segment's start state; pass C reruns
+// segments 1.. from those, writing the outputs and h_T.
+constexpr int kSegPairs = 64;    // (sequence, head) pairs, at most
+constexpr int kSegTasks = 1024;  // tasks of one pass, at most
+constexpr int kSegSlots = 160;   // segment start states (and maps), at most
+// Task kinds (int4 {first chunk, chunks, sequence * H + head, kind | last << 3 | slot << 4}).
+constexpr int kTaskWhole = 0;  // a whole chain: h0 -> outputs, h_T
+constexpr int kTaskHead = 1;   // segment 0: h0 -> outputs, end state to E[slot]
+constexpr int kTaskMapF = 2;   // a middle segment's map: identity, u = 0 -> F[slot]
+constexpr int kTaskMapZ = 3;   // a middle segment from zero -> E[slot]
+constexpr int kTaskTail = 4;   // segment k >= 1: E[slot] -> outputs (h_T when last)
+
+__host__ __device__ inline bool seg_layout_applies(const Dims& d) {
+    return d.dk == 128 && d.dv == 128 && (long long)d.N * d.H <= kSegPairs;
+}
+
 struct WsLayout {
     size_t header, seq_first, order, chunks, plist, ready, factors, total;
+    size_t seg_a, seg_c, seg_scan, seg_e, seg_f, total_seg;
     long long cmax;
+    int seg_slots;  // capacity of seg_e and seg_f (0: no segment region)
     size_t factor_bytes;
     __host__ __device__ explicit WsLayout(const Dims& d) {
         cmax = max_chunks(d);
@@ -100,6 +128,15 @@ struct WsLayout {
         ready = off;     off += align256(size_t(cmax) * d.H * 4);
         factors = off;   off += size_t(cmax) * d.H * f.bytes;
         total = off;
+        const long long pairs_chunks = cmax * d.H;
+        seg_slots = seg_layout_applies(d) ? (int)(pairs_chunks < kSegSlots ? pairs_chunks : kSegSlots) : 0;
+        off = align256(off);
+        seg_a = off;     off += seg_slots ? size_t(kSegTasks) * 16 : 0;
+        seg_c = off;     off += seg_slots ? size_t(kSegTasks) * 16 : 0;
+        seg_scan = off;  off += seg_slots ? size_t(kSegPairs) * 16 : 0;
+        seg_e = off;     off += size_t(seg_slots) * d.dk * d.dv * 4;
+        seg_f = off;     off += size_t(seg_slots) * d.dk * d.dv * 4;
+        total_seg = seg_slots ? off : total;
     }
 };
 
@@ -120,6 +157,10 @@ struct Header {
     int32_t n_chain;    // fused pipeline: CTAs that run state chains (0: none)
     int32_t chain128;   // split pipeline: 1 when the 128-column chain kernel runs the
                         // state recurrence (and the factors' u is in its layout)
+    int32_t seg;        // split pipeline: 1 when segmented chains run the recurrence
+                        // (the factors' u then in the 128-column layout too)
+    int32_t seg_na, seg_nc, seg_ns;  // tasks of pass A and C, pairs of the scan
+    int32_t seg_len;    // chunks per segment
 };
 
 // Longest-first ranking covers up to this many sequences (identity order beyond);
@@ -145,7 +186,7 @@ cudaError_t ensure_smem(Kernel kern, size_t bytes) {
 // 128), the schedule kernel picks one of the two from the chain lengths and the
 // other leaves at once.
 cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws, int split_nv,
-                            int c128_mode, cudaStream_t stream);
+                            int c128_mode, int seg_len, cudaStream_t stream);
 // For equal-length chains (a fixed-length batch or one sequence): whether the
 // 128-column chain kernel is predicted faster.
 bool chain128_pick_uniform(const Dims& d);
@@ -161,6 +202,17 @@ int split_nv_for(const Dims& d);
 cudaError_t launch_chain128(const Dims& d, bool qkv_bf16, const float* h0, float scale, void* o,
                             float* hT, uint8_t* ws, cudaStream_t stream);
 bool chain128_applies(const Dims& d);
+
+// Segmented chains (split pipeline, seg_layout_applies and a workspace of
+// WsLayout::total_seg bytes).  seg_pick_uniform: for chains of equal length, the
+// segment length predicted fastest, or 0 where the unsegmented state kernel is
+// predicted faster.  The schedule kernel's seg_len: > 0 use it, 0 none, -1 decide
+// from the chain lengths.  launch_seg_pass(pass 0 = A, 1 = C) and launch_seg_scan
+// run only when the schedule kernel set Header::seg (they leave at once otherwise).
+int seg_pick_uniform(const Dims& d);
+cudaError_t launch_seg_pass(const Dims& d, bool qkv_bf16, int pass, const float* h0, float scale,
+                            void* o, float* hT, uint8_t* ws, cudaStream_t stream);
+cudaError_t launch_seg_scan(const Dims& d, uint8_t* ws, cudaStream_t stream);
 
 // Fused pipeline.  The schedule kernel, given fused_grid > 0, also picks how many of
 // the fused kernel's fused_grid CTAs run state chains (production_ratio: the time to

@@ -14,6 +14,43 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kMaxGrid = 1024;  // fused grids of up to this many CTAs
 
+// Per-step times of the state kernels, measured on GB300 (us): a 128-column chain
+// step (the segment passes' tasks too), and a 64 / 32 / 16-column tile step.
+constexpr float kStep128 = 2.5f;
+__host__ __device__ inline float tile_step(int nv) { return nv == 64 ? 2.0f : (nv == 32 ? 1.55f : 1.42f); }
+// Predicted time of the tiled state kernel: its items are taken longest first, so
+// it is bound by the longest chain or by its share of all the steps.
+__host__ __device__ inline float tiled_time(int longest, long long steps, int H, int dv, int nv, int sms) {
+    const float share = (float)steps * H * (float)(dv / nv) / (float)sms;
+    return tile_step(nv) * ((float)longest > share ? (float)longest : share);
+}
+
+// Segments of L chunks: a chain of n chunks has ceil(n / L) segments.  Pass A holds
+// per (sequence, head) the first segment and two map tasks per middle segment (or
+// the whole chain when it has one segment), pass C the segments after the first.
+// Both passes must fit one round of CTAs, and the start states the slots.  Time
+// (measured on GB300): 2.5 us per step of the longest task of each pass plus about
+// 10 us per pass (a task's start and end: tensor memory, barriers, its first
+// copies, its final state), and for the scan about 5 us plus 3.6 us per serial step.
+struct SegCount {
+    int tasks_a, slots, nseg_max, tail_max;
+    __host__ __device__ void add(int n, int L, int H) {  // one sequence of n > 0 chunks
+        const int ns = (n + L - 1) / L;
+        tasks_a += H * (ns >= 2 ? 2 * ns - 3 : 1);
+        slots += H * (ns - 1);
+        if (ns > nseg_max) nseg_max = ns;
+        const int tail = ns >= 3 ? L : (ns == 2 ? n - L : 0);
+        if (tail > tail_max) tail_max = tail;
+    }
+    // predicted time (us), or a negative value where L does not apply
+    __host__ __device__ float time(int L, int longest, int empty_tasks, int sms, int slot_cap) const {
+        const int cap = sms < kSegTasks - empty_tasks ? sms : kSegTasks - empty_tasks;
+        if (nseg_max < 3 || tasks_a > cap || slots > slot_cap) return -1.f;
+        const int head = L < longest ? L : longest;
+        return kStep128 * (float)(head + tail_max) + 2.f * 10.f + 5.f + 3.6f * (float)(nseg_max - 2);
+    }
+};
+
 __device__ inline void seq_span(const Dims& d, const int32_t* cu, int s, long long& row0,
                                 int& len) {
     if (d.varlen) {
@@ -60,10 +97,13 @@ __device__ int block_scan(int x, int* warp_sums, int* carry) {
 // Header::chain128 (split pipeline): c128_mode 0 or 1 sets it as given; 2 (varlen,
 // dk = dv = 128) decides between the state kernel with split_nv-column tiles and the
 // 128-column chain kernel from their predicted times on these chain lengths.
+// seg_len (split pipeline, seg_layout_applies): > 0, segments of that many chunks;
+// 0, none; -1, segments where predicted faster than the tiled state kernel (the
+// length then chosen here), with the task lists and the scan's list.
 __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_t* cu,
                                                             uint8_t* ws, int fused_grid,
                                                             float ratio, int split_nv, int c128_mode,
-                                                            int sms) {
+                                                            int seg_len, int sms) {
     WsLayout L(d);
     Header* hdr = reinterpret_cast<Header*>(ws + L.header);
     int32_t* seq_first = reinterpret_cast<int32_t*>(ws + L.seq_first);
@@ -98,6 +138,8 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
             hdr->next_item = 0;
             hdr->n_chain = 0;
             hdr->chain128 = 0;
+            hdr->seg = 0;
+            hdr->seg_na = hdr->seg_nc = hdr->seg_ns = hdr->seg_len = 0;
         }
         return;
     }
@@ -146,6 +188,8 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         hdr->next_item = 0;
         hdr->n_chain = 0;
         hdr->chain128 = c128_mode == 1 ? 1 : 0;
+        hdr->seg = 0;
+        hdr->seg_na = hdr->seg_nc = hdr->seg_ns = hdr->seg_len = 0;
     }
     __syncthreads();
     // the chunk table, one thread per chunk: its sequence is the last one whose first
@@ -183,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
     } else {
         for (int s = tid; s < d.N; s += kThreads) order[s] = s;
     }
-    if ((fused_grid <= 0 && c128_mode != 2) || !small) return;
+    if ((fused_grid <= 0 && c128_mode != 2 && seg_len == 0) || !small) return;
 
     // ---- fused pipeline.  Chain r = rank * H + head (one chain per sequence and
     // head); chain CTA x takes chains x, x + n_chain, ... (round k = r / n_chain), so
@@ -205,27 +249,115 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
         // CTA 0, with the longest of each round, finishes last); the tiled kernel takes
         // its (chain, tile) items longest first from a counter, bounded by the longest
         // chain or by its share of all the steps.
-        __shared__ int steps128;
         const int H = d.H, R = d.N * d.H;
-        const int G = R < sms ? R : sms;
-        if (tid == 0) steps128 = 0;
-        __syncthreads();
-        if (tid < 32 && G > 0) {
-            int sum = 0;
-            for (int k = tid; k * G < R; k += 32) sum += rcntf((k * G) / H);
+        const int longest = d.N > 0 ? rcntf(0) : 0;
+        const float tnv = tiled_time(longest, carry, H, d.dv, split_nv, sms);
+        if (c128_mode == 2) {
+            __shared__ int steps128;
+            const int G = R < sms ? R : sms;
+            if (tid == 0) steps128 = 0;
+            __syncthreads();
+            if (tid < 32 && G > 0) {
+                int sum = 0;
+                for (int k = tid; k * G < R; k += 32) sum += rcntf((k * G) / H);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            if (tid == 0) steps128 = sum;
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                if (tid == 0) steps128 = sum;
+            }
+            __syncthreads();
+            if (tid == 0) hdr->chain128 = kStep128 * (float)steps128 < 0.9f * tnv ? 1 : 0;
+        }
+        if (seg_len == 0 || !seg_layout_applies(d) || L.seg_slots == 0) return;
+        // ---- segments (few chains, at most kSegPairs): the length, then the lists
+        __shared__ unsigned long long seg_best;
+        __shared__ int s_empty;
+        if (tid == 0) {
+            seg_best = ~0ull;
+            int empty = 0;
+            for (int rk = 0; rk < d.N; ++rk) empty += rcntf(rk) == 0;
+            s_empty = empty * H;
         }
         __syncthreads();
-        if (tid == 0) {
-            const float t128 = 2.5f * (float)steps128;
-            const float per = split_nv == 64 ? 2.0f : (split_nv == 32 ? 1.55f : 1.42f);
-            const float share = (float)carry * H * (float)(d.dv / split_nv) / (float)sms;
-            const float longest = d.N > 0 ? (float)rcntf(0) : 0.f;
-            const float tnv = per * (longest > share ? longest : share);
-            hdr->chain128 = t128 < 0.9f * tnv ? 1 : 0;
+        int Lp = seg_len;
+        if (seg_len < 0) {
+            for (int Lc = tid + 1; Lc < longest; Lc += kThreads) {
+                SegCount sc{0, 0, 0, 0};
+                for (int rk = 0; rk < d.N; ++rk)
+                    if (rcntf(rk) > 0) sc.add(rcntf(rk), Lc, H);
+                const float t = sc.time(Lc, longest, s_empty, sms, L.seg_slots);
+                if (t >= 0.f)
+                    atomicMin(&seg_best, ((unsigned long long)__float_as_uint(t) << 32) | (unsigned long long)Lc);
+            }
+            __syncthreads();
+            Lp = 0;
+            if (seg_best != ~0ull && __uint_as_float((unsigned)(seg_best >> 32)) < 0.85f * tnv)
+                Lp = (int)(seg_best & 0xffffffffull);
         }
+        if (Lp <= 0) return;
+        // The lists, one thread per (rank, head) pair in rank order: its task counts,
+        // their exclusive prefixes (thread 0, at most kSegPairs pairs), then its tasks.
+        __shared__ int s_pa[kSegPairs + 1], s_pc[kSegPairs + 1], s_pe[kSegPairs + 1], s_pf[kSegPairs + 1],
+            s_ps[kSegPairs + 1], s_pz[kSegPairs + 1];
+        __shared__ int s_plan_ok;
+        const int P = d.N * H;
+        if (tid == 0) {
+            SegCount sc{0, 0, 0, 0};  // a length given by the host was checked there with the same counts
+            for (int rk = 0; rk < d.N; ++rk)
+                if (rcntf(rk) > 0) sc.add(rcntf(rk), Lp, H);
+            s_plan_ok = sc.time(Lp, longest, s_empty, sms, L.seg_slots) >= 0.f;
+            if (!s_plan_ok) hdr->error |= kDevErrPlan;
+            int a = 0, c = 0, e = 0, f = 0, sn = 0, z = 0;
+            for (int p = 0; p < P; ++p) {
+                s_pa[p] = a; s_pc[p] = c; s_pe[p] = e; s_pf[p] = f; s_ps[p] = sn; s_pz[p] = z;
+                const int n = rcntf(p / H), nseg = (n + Lp - 1) / Lp;
+                if (n == 0) {
+                    ++z;
+                    continue;
+                }
+                a += nseg >= 2 ? 2 * nseg - 3 : 1;
+                c += nseg - 1;
+                e += nseg - 1;
+                f += nseg >= 2 ? nseg - 2 : 0;
+                sn += nseg >= 3;
+            }
+            s_pa[P] = a; s_pc[P] = c; s_pe[P] = e; s_pf[P] = f; s_ps[P] = sn; s_pz[P] = z;
+        }
+        __syncthreads();
+        if (!s_plan_ok) return;
+        int4* ta = reinterpret_cast<int4*>(ws + L.seg_a);
+        int4* tc = reinterpret_cast<int4*>(ws + L.seg_c);
+        int4* tscan = reinterpret_cast<int4*>(ws + L.seg_scan);
+        for (int p = tid; p < P; p += kThreads) {
+            const int rk = p / H, h = p - rk * H, sq = s_order[rk], n = rcntf(rk), c0 = rc0(rk);
+            const int pair = sq * H + h;
+            if (n == 0) {  // empty sequences last: h_T = h0
+                ta[s_pa[P] + s_pz[p]] = make_int4(0, 0, pair, kTaskWhole);
+                continue;
+            }
+            const int nseg = (n + Lp - 1) / Lp, eb = s_pe[p], fb = s_pf[p];
+            int na = s_pa[p], nct = s_pc[p];
+            if (nseg == 1) {
+                ta[na] = make_int4(c0, n, pair, kTaskWhole);
+                continue;
+            }
+            ta[na++] = make_int4(c0, Lp, pair, kTaskHead | (eb << 4));
+            for (int k = 1; k + 1 < nseg; ++k) {
+                ta[na++] = make_int4(c0 + k * Lp, Lp, pair, kTaskMapF | ((fb + k - 1) << 4));
+                ta[na++] = make_int4(c0 + k * Lp, Lp, pair, kTaskMapZ | ((eb + k) << 4));
+            }
+            for (int k = 1; k < nseg; ++k) {
+                const int len = n - k * Lp < Lp ? n - k * Lp : Lp;
+                tc[nct++] = make_int4(c0 + k * Lp, len, pair, kTaskTail | ((k == nseg - 1) << 3) | ((eb + k - 1) << 4));
+            }
+            if (nseg >= 3) tscan[s_ps[p]] = make_int4(pair, eb, fb, nseg);
+        }
+        if (tid != 0) return;
+        const int na = s_pa[P] + s_pz[P], nct = s_pc[P], ns = s_ps[P];
+        hdr->seg = 1;
+        hdr->seg_na = na;
+        hdr->seg_nc = nct;
+        hdr->seg_ns = ns;
+        hdr->seg_len = Lp;
         return;
     }
     int* const rf = s_rf;
@@ -359,9 +491,32 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Dims d, const int32_
 }  // namespace
 
 cudaError_t launch_schedule(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws, int split_nv,
-                            int c128_mode, cudaStream_t stream) {
-    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, 0, 0.f, split_nv, c128_mode, num_sms());
+                            int c128_mode, int seg_len, cudaStream_t stream) {
+    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, 0, 0.f, split_nv, c128_mode, seg_len,
+                                                num_sms());
     return cudaGetLastError();
+}
+
+// The same prediction as the schedule kernel's, for chains of equal length.
+int seg_pick_uniform(const Dims& d) {
+    const WsLayout W(d);
+    if (!seg_layout_applies(d) || W.seg_slots == 0 || d.N > kRankMax) return 0;
+    const int n = (int)(((long long)d.T + kChunk - 1) / kChunk);
+    if (n == 0 || d.N == 0) return 0;
+    const int sms = num_sms();
+    const float tnv = tiled_time(n, (long long)n * d.N, d.H, d.dv, split_nv_for(d), sms);
+    float best = -1.f;
+    int bestL = 0;
+    for (int L = 1; L < n; ++L) {
+        SegCount sc{0, 0, 0, 0};
+        for (int s = 0; s < d.N; ++s) sc.add(n, L, d.H);
+        const float t = sc.time(L, n, 0, sms, W.seg_slots);
+        if (t >= 0.f && (best < 0.f || t < best)) {
+            best = t;
+            bestL = L;
+        }
+    }
+    return best >= 0.f && best < 0.85f * tnv ? bestL : 0;
 }
 
 // The same prediction as the schedule kernel's, for chains of equal length.
@@ -371,17 +526,13 @@ bool chain128_pick_uniform(const Dims& d) {
     const int sms = num_sms();
     if (R == 0 || nch == 0) return false;
     const long long G = R < sms ? R : sms;
-    const float t128 = 2.5f * (float)(((R + G - 1) / G) * nch);
-    const int nv = split_nv_for(d);
-    const float per = nv == 64 ? 2.0f : (nv == 32 ? 1.55f : 1.42f);
-    const float share = (float)(R * nch) * (float)(d.dv / nv) / (float)sms;
-    const float tnv = per * ((float)nch > share ? (float)nch : share);
-    return t128 < 0.9f * tnv;
+    const float t128 = kStep128 * (float)(((R + G - 1) / G) * nch);
+    return t128 < 0.9f * tiled_time((int)nch, nch * d.N, d.H, d.dv, split_nv_for(d), sms);
 }
 
 cudaError_t launch_schedule_fused(const Dims& d, const int32_t* cu_seqlens, uint8_t* ws,
                                   int fused_grid, float production_ratio, cudaStream_t stream) {
-    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, fused_grid, production_ratio, 0, 0, 0);
+    schedule_kernel<<<1, kThreads, 0, stream>>>(d, cu_seqlens, ws, fused_grid, production_ratio, 0, 0, 0, 0);
     return cudaGetLastError();
 }
 

@@ -107,6 +107,11 @@ __device__ __forceinline__ bool mbar_spin_or_abort(uint64_t* bar, uint32_t parit
 }
 
 // ---------------------------------------------------------------- bulk copies
+// Prefetch of a global range into L2 (bytes: multiple of 16, address 16-byte aligned).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
 // Global -> shared bulk copy completing on `bar` (bytes: multiple of 16, both
 // addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,

@@ -69,6 +69,8 @@ typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
 /* Device error word bits (kda_fwd_check). */
 #define KDA_DEVERR_CU_SEQLENS 0x1u   /* cu_seqlens not 0-based, decreasing, or != T */
 #define KDA_DEVERR_TIMEOUT 0x2u      /* a kernel's bounded wait ran out (it left early) */
+#define KDA_DEVERR_PLAN 0x4u         /* the schedule did not fit its workspace (a library
+                                        fault: the state recurrence did not run) */
 
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (0 on bad sizes).
@@ -154,15 +156,30 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
  *     The state kernel is chosen on the host for equal-length chains and by the
  *     schedule kernel from the chain lengths for varlen batches of at least 512
  *     (sequence, head) pairs (both are then launched; the one not chosen leaves at
- *     once).  Applies to every size.
+ *     once).  Few long chains (dk = dv = 128, at most 64 (sequence, head) pairs, a
+ *     workspace of kda_fwd_workspace_size bytes) are cut into segments where that is
+ *     predicted faster: a first pass runs each chain's first segment and, for every
+ *     middle segment, its state map and its state from zero; a scan kernel gives
+ *     each segment's start state; a second pass reruns the later segments from
+ *     those (exact up to rounding: the chunk step is affine in the state).  The
+ *     segment length is chosen on the host for equal-length chains, by the schedule
+ *     kernel for varlen batches of at least 2048 tokens (the tiled state kernel is
+ *     then launched too, and the kernels not chosen leave at once).  Applies to
+ *     every size.
  * KDA_PIPELINE_AUTO (default) takes the fused pipeline where it applies and was
  * measured faster on GB300: fixed-length batches (or a single sequence) with
  * 32 <= B * H <= 256; every other size takes the split one.  KDA_PIPELINE_FUSED
- * takes it wherever it applies, KDA_PIPELINE_SPLIT never.  The setting is
- * process-wide (an atomic; calls already enqueued keep theirs); it exists for
- * measurement and testing.
+ * takes it wherever it applies, KDA_PIPELINE_SPLIT never, KDA_PIPELINE_SPLIT_WHOLE
+ * never and never cuts chains into segments.  The setting is process-wide (an
+ * atomic; calls already enqueued keep theirs); it exists for measurement and
+ * testing.
  */
-typedef enum { KDA_PIPELINE_AUTO = 0, KDA_PIPELINE_FUSED = 1, KDA_PIPELINE_SPLIT = 2 } kda_pipeline;
+typedef enum {
+    KDA_PIPELINE_AUTO = 0,
+    KDA_PIPELINE_FUSED = 1,
+    KDA_PIPELINE_SPLIT = 2,
+    KDA_PIPELINE_SPLIT_WHOLE = 3
+} kda_pipeline;
 void kda_set_pipeline(kda_pipeline pipeline);
 kda_pipeline kda_get_pipeline(void);
 

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 from oracle import brute
-from oracle.chunked import kda_chunked_fp64
+from oracle.chunked import kda_chunked_fp64, kda_segmented_fp64
 from tests import gen
 from tests.metrics import rel_rmse
 from tests.oracle_pins import PINS, brute_case, expected_reciprocal_norm
@@ -81,6 +81,26 @@ def test_chunked_equals_recurrence_probes(kind):
     oc, hc = kda_chunked_fp64(**x.tensors(), chunk=64)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(h))
     assert rel_rmse(oc, o) < 1e-10 and rel_rmse(hc, h) < 1e-10
+
+
+@pytest.mark.parametrize("seg_chunks,chunk", [(1, 4), (2, 4), (3, 8), (5, 4), (4, 64)])
+def test_segmented_equals_recurrence(seg_chunks, chunk):
+    """The exact inter-chunk split (segment maps, a scan of start states, the later
+    segments rerun) equals the token recurrence: chains of 0 to 10 segments, ragged
+    last chunks and segments, an empty sequence."""
+    x = gen.make_lengths([70, 1, 0, 129, 64, 300], seed=5, H=2, d=8)
+    o, h = oracle.kda_recurrence_fp64(**x.tensors())
+    os_, hs = kda_segmented_fp64(**x.tensors(), seg_chunks=seg_chunks, chunk=chunk)
+    assert rel_rmse(os_, o) < 1e-11 and rel_rmse(hs, h) < 1e-11
+
+
+@pytest.mark.parametrize("kind", ["deep", "abyss", "saturated", "repeated_keys", "beta01"])
+def test_segmented_equals_recurrence_probes(kind):
+    x = gen.make_probe(kind, seed=2, T=200, H=2, d=8)
+    o, h = oracle.kda_recurrence_fp64(**x.tensors())
+    os_, hs = kda_segmented_fp64(**x.tensors(), seg_chunks=2, chunk=16)
+    assert np.all(np.isfinite(os_)) and np.all(np.isfinite(hs))
+    assert rel_rmse(os_, o) < 1e-10 and rel_rmse(hs, h) < 1e-10
 
 
 def test_zero_length_sequence_returns_h0():
