@@ -150,3 +150,13 @@ def test_segments_agree_with_fused(kda):
     assert rel_rmse(o_s, o_f.double()) <= 1e-2
     assert rel_rmse(h_s, h_f.double()) <= 5e-3
     _assert_parity(x, o_s, h_s, heads=[0, 7, 15])
+
+
+def test_segments_one_long_sequence(kda):
+    """A single 131,072-token sequence at H = 1: a 2,048-step chain cut into dozens of
+    segments (the whole sequence against the oracle)."""
+    x = gen.make_cfg2(seed=40, salt=SALT, T=131072, H=1, B=1)
+    assert kda.launch_count(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs) == 5
+    o, hT, hdr = _run_with_header(kda, x)
+    assert hdr["seg"] == 1 and hdr["seg_ns"] == 1
+    _assert_parity(x, o, hT)
