@@ -370,6 +370,71 @@ def run_decode(args):
     print(json.dumps(line), flush=True)
 
 
+def run_backward(args):
+    """--backward: times kda_bwd (the gradients of sum(o do) + sum(h_T dh_T)) on the
+    workload's inputs with random do and dh_T (CUDA events, inputs resident), then
+    checks two heads' gradients against the fp64 autograd oracle."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_delta_rule_25_gb300 as kda
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    salt = gen.fresh_salt()
+    x, desc = make_workload(args.workload, 0, salt)
+    xd = x.to(dev)
+    rng = np.random.default_rng(salt)
+    do = torch.from_numpy(rng.standard_normal(tuple(x.v.shape)).astype(np.float32)).to(x.v.dtype)
+    dhT = torch.from_numpy(rng.standard_normal((x.num_seqs, x.H, x.dk, x.dv)).astype(np.float32))
+    do_d, dhT_d = do.to(dev), dhT.to(dev)
+    ws = torch.empty(int(kda.load_library().kda_bwd_workspace_size(x.B, x.T, x.H, x.dk, x.dv, x.num_seqs))
+                     + 256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return kda.bwd(**xd.tensors(), do=do_d, dhT=dhT_d, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        out = step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    parity = None
+    if not args.no_parity:
+        from oracle.backward import kda_backward_fp64
+        from tests.metrics import rel_rmse
+        hs = sorted({0, min(1, x.H - 1)})
+        t = x.tensors()
+        for key in ("q", "k", "v", "g", "beta"):
+            t[key] = t[key][:, :, hs].contiguous()
+        if t["h0"] is not None:
+            t["h0"] = t["h0"][:, hs].contiguous()
+        ref = kda_backward_fp64(**t, do=do[:, :, hs].double(), dhT=dhT[:, hs].double())
+        names = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+        parity = {"heads": hs}
+        for name, a, r in zip(names, out, ref):
+            a = a.cpu()
+            a = a[:, hs] if name == "dh0" else a[:, :, hs]
+            parity[name + "_rel_rmse"] = rel_rmse(a, r)
+    line = {
+        "metric": "KDA backward tokens/s (gradients of o and h_T for q, k, v, g, beta, h0)",
+        "value": x.tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": desc, "name": args.workload, "tokens_per_step": x.tokens,
+                                        "heads": x.H, "dk": x.dk, "dv": x.dv, "salt": salt},
+        "gpu_launches": 2 * args.steps, "clocks": clk, "parity": parity,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,6 +442,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (kda_bwd) on the workload instead of the forward")
+    ap.add_argument("--no-parity", action="store_true", help="--backward: skip the oracle check")
     ap.add_argument("--pipeline", default="auto", choices=["auto", "fused", "split", "split-whole"],
                     help="auto (default): the library's choice for the sizes; fused: factor "
                          "production and state chains in one kernel; split: a factor kernel, "
@@ -393,6 +461,8 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
+    if args.backward:
+        return run_backward(args)
     if args.workload.startswith("decode-"):
         run_decode(args)
         return

@@ -84,6 +84,11 @@ def load_library():
         lib.kda_get_pipeline.restype = i32
         lib.kda_fwd_uses_fused.argtypes = [i32] * 6
         lib.kda_fwd_uses_fused.restype = i32
+        lib.kda_bwd_workspace_size.argtypes = [i32] * 6
+        lib.kda_bwd_workspace_size.restype = sz
+        lib.kda_bwd.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
+                                vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_bwd.restype = i32
         _lib = lib
         return lib
 
@@ -274,7 +279,55 @@ def fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     return o, hT
 
 
-__all__ = ["fwd", "fwd_noalloc", "workspace_size", "launch_count", "load_library", "KdaError",
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+        beta: torch.Tensor, h0: Optional[torch.Tensor] = None,
+        cu_seqlens: Optional[torch.Tensor] = None, scale: Optional[float] = None, *,
+        do: torch.Tensor, dhT: Optional[torch.Tensor] = None, want_dh0: bool = True,
+        workspace: Optional[torch.Tensor] = None, check: bool = False):
+    """Backward pass through ``kda_bwd``: the gradients of sum(o * do) + sum(h_T * dhT)
+    of the forward on the same inputs, with respect to q, k, v, g, beta and h0.
+
+    Returns (dq, dk, dv, dg, dbeta, dh0), fp32 tensors shaped like the inputs (dh0
+    [N, H, dk, dv], or None when ``want_dh0`` is False).  ``do`` has v's dtype and
+    shape; ``dhT`` (fp32 [N, H, dk, dv]) may be None.  The gate must be fp32."""
+    B, T, H, dk, dv, N, dev = _validate(q, k, v, g, beta, h0, cu_seqlens, None, None, False)
+    _check(do, "do", q.dtype, (B, T, H, dv), dev)
+    if dhT is not None:
+        _check(dhT, "dhT", torch.float32, (N, H, dk, dv), dev)
+    lib = load_library()
+    if scale is None:
+        scale = dk ** -0.5
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq = torch.empty((B, T, H, dk), **f32)
+    dk_ = torch.empty((B, T, H, dk), **f32)
+    dv_ = torch.empty((B, T, H, dv), **f32)
+    dg = torch.empty((B, T, H, dk), **f32)
+    dbeta = torch.empty((B, T, H), **f32)
+    dh0 = torch.empty((N, H, dk, dv), **f32) if want_dh0 else None
+    ws_bytes = int(lib.kda_bwd_workspace_size(B, T, H, dk, dv, N))
+    if ws_bytes == 0:
+        raise KdaError(2, "kda_bwd_workspace_size")
+    if workspace is None or workspace.numel() - (-workspace.data_ptr()) % 256 < ws_bytes:
+        workspace = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    ws_ptr = (workspace.data_ptr() + 255) & ~255
+    avail = workspace.numel() - (ws_ptr - workspace.data_ptr())
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    dt = KDA_BF16 if q.dtype == torch.bfloat16 else KDA_FP32
+    st = lib.kda_bwd(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(g), _ptr(beta), _ptr(h0), _ptr(cu_seqlens),
+                     N, B, T, H, dk, dv, float(scale), _ptr(do), _ptr(dhT), _ptr(dq), _ptr(dk_),
+                     _ptr(dv_), _ptr(dg), _ptr(dbeta), _ptr(dh0), ctypes.c_void_p(ws_ptr), avail,
+                     ctypes.c_void_p(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_bwd")
+    if check:
+        err = ctypes.c_uint32(0)
+        st = lib.kda_fwd_check(ctypes.c_void_p(ws_ptr), ctypes.c_void_p(stream), ctypes.byref(err))
+        if st != KDA_OK:
+            raise KdaError(st, f"kda_bwd (device error bits {err.value:#x})")
+    return dq, dk_, dv_, dg, dbeta, dh0
+
+
+__all__ = ["fwd", "bwd", "fwd_noalloc", "workspace_size", "launch_count", "load_library", "KdaError",
            "LIB_PATH", "set_pipeline", "get_pipeline", "uses_fused"]
 
 

@@ -48,10 +48,12 @@ std::atomic<int> g_pipeline{KDA_PIPELINE_AUTO};
 
 // The fused pipeline's grid for these sizes under the current setting, or 0 for the
 // split pipeline.  Automatic choice: where the fused pipeline was measured faster on
-// GB300 (the throughput sweep of 22 shapes: fixed-length batches with B * H from 32
-// to 256 gain 6-15 %; varlen batches, where the chains of a round differ in length,
-// B * H = 16, whose few chains bound it, and B * H >= 512, where the factor CTAs it
-// gives up cost more than the chains gain, run faster split).
+// GB300 (the throughput sweep of 22 shapes): fixed-length batches with B * H from 32
+// to 256 whose split pipeline would run the tiled state kernel (B * H = 32 and 64:
+// 6-16 %).  Where the split pipeline takes the 128-column chain kernel (B * H = 128
+// and 256 at 128-chunk chains: 2-5 % faster split), for varlen batches (the chains of
+// a round differ in length), B * H = 16 (its few chain CTAs bound it) and B * H >= 512
+// (the factor CTAs it gives up cost more than the chains gain), the split one.
 int pipeline_grid(const kda::Dims& d) {
     const int p = g_pipeline.load();
     if (p == KDA_PIPELINE_SPLIT || p == KDA_PIPELINE_SPLIT_WHOLE) return 0;
@@ -59,7 +61,7 @@ int pipeline_grid(const kda::Dims& d) {
     if (grid == 0 || p == KDA_PIPELINE_FUSED) return grid;
     const long long pairs = (long long)d.N * d.H;
     const bool uniform = !d.varlen || d.N == 1;
-    return uniform && pairs >= 32 && pairs <= 256 ? grid : 0;
+    return uniform && pairs >= 32 && pairs <= 256 && !kda::chain128_pick_uniform(d) ? grid : 0;
 }
 
 bool valid_head_dim(int x) { return x == 64 || x == 128; }
@@ -274,6 +276,44 @@ kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* d
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
     if (device_error) *device_error = hdr.error;
     return hdr.error ? KDA_ERR_DEVICE : KDA_OK;
+}
+
+size_t kda_bwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs) {
+    kda::Dims d;
+    if (make_dims(B, T, H, dk, dv, num_seqs, B == 1, d) != KDA_OK) return 0;
+    return kda::bwd_workspace_bytes(d);
+}
+
+kda_status kda_bwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                   const float* g, const float* beta, const float* h0,
+                   const int32_t* cu_seqlens, int num_seqs,
+                   int B, int T, int H, int dk, int dv, float scale,
+                   const void* dout, const float* dhT,
+                   float* dq, float* dk_out, float* dv_out, float* dg, float* dbeta, float* dh0,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    if (qkv_dtype != KDA_BF16 && qkv_dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    kda::Dims d;
+    kda_status st = make_dims(B, T, H, dk, dv, num_seqs, cu_seqlens != nullptr, d);
+    if (st != KDA_OK) return st;
+    const bool any_tokens = (long long)B * T > 0;
+    if (any_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk_out || !dv_out || !dg || !dbeta))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(h0) || !aligned16(dout) || !aligned16(dhT) || !aligned16(dq) || !aligned16(dk_out) ||
+        !aligned16(dv_out) || !aligned16(dg) || !aligned16(dbeta) || !aligned16(dh0) || !aligned16(cu_seqlens))
+        return KDA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < kda::bwd_workspace_bytes(d) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KDA_ERR_WORKSPACE;
+    if (num_seqs == 0) return KDA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (kda::launch_schedule(d, cu_seqlens, ws, kda::kNV, 0, 0, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_bwd(d, qkv_dtype == KDA_BF16, cu_seqlens, q, k, v, g, beta, h0, dout, dhT, scale, dq,
+                        dk_out, dv_out, dg, dbeta, dh0, ws, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
 }
 
 const char* kda_status_string(kda_status status) {

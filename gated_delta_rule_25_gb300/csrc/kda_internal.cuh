@@ -214,6 +214,14 @@ cudaError_t launch_seg_pass(const Dims& d, bool qkv_bf16, int pass, const float*
                             void* o, float* hT, uint8_t* ws, cudaStream_t stream);
 cudaError_t launch_seg_scan(const Dims& d, uint8_t* ws, cudaStream_t stream);
 
+// Backward pass: workspace bytes for the current device (after the schedule's
+// tables), and the launch (after launch_schedule has filled the tables).
+size_t bwd_workspace_bytes(const Dims& d);
+cudaError_t launch_bwd(const Dims& d, bool qkv_bf16, const int32_t* cu, const void* q, const void* k,
+                       const void* v, const float* g, const float* beta, const float* h0, const void* dout,
+                       const float* dhT, float scale, float* dq, float* dk, float* dv, float* dg,
+                       float* dbeta, float* dh0, uint8_t* ws, cudaStream_t stream);
+
 // Fused pipeline.  The schedule kernel, given fused_grid > 0, also picks how many of
 // the fused kernel's fused_grid CTAs run state chains (production_ratio: the time to
 // produce one item's factors over the time of one chain step), lays out the

@@ -168,7 +168,8 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, kda_dty
  *     every size.
  * KDA_PIPELINE_AUTO (default) takes the fused pipeline where it applies and was
  * measured faster on GB300: fixed-length batches (or a single sequence) with
- * 32 <= B * H <= 256; every other size takes the split one.  KDA_PIPELINE_FUSED
+ * 32 <= B * H <= 256 for which the split pipeline would not take the 128-column
+ * chain kernel; every other size takes the split one.  KDA_PIPELINE_FUSED
  * takes it wherever it applies, KDA_PIPELINE_SPLIT never, KDA_PIPELINE_SPLIT_WHOLE
  * never and never cuts chains into segments.  The setting is process-wide (an
  * atomic; calls already enqueued keep theirs); it exists for measurement and
@@ -257,6 +258,39 @@ kda_status kda_fwd_noalloc_check(kda_stream_t stream, uint32_t* device_error);
 kda_status kda_decode(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
                       const float* g, const float* beta, const float* h_in, float* h_out,
                       int N, int H, int dk, int dv, float scale, void* o, kda_stream_t stream);
+
+/*
+ * Backward pass ("Autoresearch on Kimi Delta Attention", sections THE MECHANISM and
+ * OPTIMIZATION TRACE: the training-side workload, the state's gradient carried
+ * backwards through the chunks): for the forward of kda_fwd on the same inputs,
+ * the gradients of  L = sum(o * dout) + sum(h_T * dhT)  with respect to q, k, v, g,
+ * beta and h0 (through the L2 normalisations of q and k and alpha = exp(g)).
+ *
+ * Layouts as kda_fwd (DEVICE pointers, row-major, contiguous, 16-byte aligned):
+ *     q, k, dout-like : q, k [B, T, H, dk], v and dout [B, T, H, dv] (qkv_dtype)
+ *     g : [B, T, H, dk] fp32      beta : [B, T, H] fp32
+ *     h0 : [N, H, dk, dv] fp32 or NULL (zero initial state)
+ *     dhT : [N, H, dk, dv] fp32 or NULL (no gradient through h_T)
+ * Outputs (fp32, written in full): dq, dk : [B, T, H, dk]; dv : [B, T, H, dv];
+ *     dg : [B, T, H, dk]; dbeta : [B, T, H]; dh0 : [N, H, dk, dv] or NULL (not wanted).
+ * cu_seqlens as kda_fwd.  Workspace: kda_bwd_workspace_size bytes (for the current
+ * device), 256-byte aligned, caller-owned scratch; it holds the state at every
+ * chunk start and, per CTA, the states of one chunk.
+ *
+ * Computation: one CTA per (sequence, head) chain at a time, fp32 state in
+ * registers, fp32 arithmetic on the CUDA cores: the forward recomputed with
+ * checkpoints at chunk starts, then every chunk in reverse (its states recomputed,
+ * then its tokens in reverse).  Two launches (the schedule kernel, the backward).
+ * Statuses as kda_fwd (malformed cu_seqlens: the device error word, kda_fwd_check).
+ */
+size_t kda_bwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs);
+kda_status kda_bwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                   const float* g, const float* beta, const float* h0,
+                   const int32_t* cu_seqlens, int num_seqs,
+                   int B, int T, int H, int dk, int dv, float scale,
+                   const void* dout, const float* dhT,
+                   float* dq, float* dk_out, float* dv_out, float* dg, float* dbeta, float* dh0,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream);
 
 #ifdef __cplusplus
 }

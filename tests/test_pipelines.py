@@ -3,7 +3,8 @@
 The fused pipeline runs factor production and the state chains in one cooperative
 kernel (dk = dv = 128); the split one (a factor kernel, then a state kernel) serves
 every size.  The automatic choice takes the fused one for fixed-length batches with
-32 <= B * H <= 256, so most of test_gpu_parity.py runs split; the cases here force
+32 <= B * H <= 256 whose split pipeline would keep the tiled state kernel, so most of
+test_gpu_parity.py runs split; the cases here force
 the fused pipeline on varlen batches, edge cases and probes, and the split one on
 the configs, all against the fp64 oracle with the gates of test_gpu_parity.py.
 """
@@ -47,7 +48,9 @@ def fused(kda):
 def test_pipeline_selection(kda):
     assert kda.get_pipeline() == "auto"
     assert kda.uses_fused(1, 8192, 32, 128, 128, 1)             # B * H = 32, fixed length
-    assert kda.uses_fused(4, 8192, 64, 128, 128, 4)             # B * H = 256
+    assert kda.uses_fused(4, 8192, 16, 128, 128, 4)             # B * H = 64
+    assert not kda.uses_fused(4, 8192, 64, 128, 128, 4)         # B * H = 256: split takes 128-column chains
+    assert not kda.uses_fused(4, 8192, 32, 128, 128, 4)         # B * H = 128: the same
     assert not kda.uses_fused(1, 8192, 16, 128, 128, 1)         # B * H = 16: split is faster
     assert not kda.uses_fused(16, 8192, 32, 128, 128, 16)       # B * H = 512
     assert not kda.uses_fused(1, 8192, 32, 128, 128, 8)         # varlen
