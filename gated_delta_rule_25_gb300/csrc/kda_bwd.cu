@@ -5,7 +5,8 @@
 //
 // One CTA per (sequence, head) chain at a time (persistent, chains in steps of the
 // grid), 4 * dk threads: thread (c, qd) holds row c of the fp32 state S (dk x dv) and
-// of its gradient dS, value columns qd * dv/4 .. .  Per chain:
+// of its gradient dS, value columns qd, qd + 4, qd + 8, ... (interleaved, so that the
+// four threads of a row read consecutive words of a shared vector).  Per chain:
 //   1. forward over the chain, the state at the start of every 64-token chunk saved
 //      (a checkpoint in the workspace);
 //   2. chunks in reverse: the chunk's states S_{t-1} recomputed from its checkpoint
@@ -79,32 +80,44 @@ __global__ void __launch_bounds__(DK * 4, 1)
     if (hdr->error) return;  // malformed cu_seqlens (reported in the error word)
     const int32_t* seq_first = reinterpret_cast<const int32_t*>(ws + W.seq_first);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = tid >> 2, qd = tid & 3, n0 = qd * NC;
+    const int c = tid >> 2, qd = tid & 3, n0 = qd * NC;  // n0: this thread's slots in a saved state
     const int H = d.H;
     const size_t st = size_t(DK) * DV;
     float* ckpt_all = reinterpret_cast<float*>(ws + L.ckpt);
     float* scr = reinterpret_cast<float*>(ws + L.scratch) + size_t(blockIdx.x) * kChunk * st;
 
-    // Sum over the state's rows of x[i] (column n0 + i), for every column: the result
-    // lands in sm.vec.  Two barriers; callers read sm.vec after it returns.
-    auto col_sum = [&](float (&x)[NC]) {
+    // Sum over the state's rows of x[i] (column 4 i + qd), for every column: the result
+    // lands in sm.vec.  Inside a warp (8 rows) a butterfly: at each of three shuffle
+    // distances a thread keeps half of its remaining slots and hands the other half to
+    // its partner, ending with NC / 8 slots summed over the warp's rows (NC - 4
+    // shuffles in all instead of 3 NC); then one pass through shared memory over the
+    // warps.  Two barriers; callers read sm.vec after it returns.
+    const bool b2 = (lane >> 4) & 1, b1 = (lane >> 3) & 1, b0 = (lane >> 2) & 1;
+    const int slot0 = (b2 ? NC / 2 : 0) + (b1 ? NC / 4 : 0) + (b0 ? NC / 8 : 0);
+    auto col_sum = [&](const float (&x)[NC]) {
+        float y[NC / 2], z[NC / 4], w[NC / 8];
 #pragma unroll
-        for (int i = 0; i < NC; ++i) {
-            float y = x[i];
-            y += __shfl_xor_sync(0xffffffffu, y, 4);
-            y += __shfl_xor_sync(0xffffffffu, y, 8);
-            y += __shfl_xor_sync(0xffffffffu, y, 16);
-            x[i] = y;
+        for (int i = 0; i < NC / 2; ++i) {
+            const float send = b2 ? x[i] : x[i + NC / 2];
+            y[i] = (b2 ? x[i + NC / 2] : x[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
         }
-        if (lane < 4) {
 #pragma unroll
-            for (int i = 0; i < NC; ++i) sm.red[warp][n0 + i] = x[i];
+        for (int i = 0; i < NC / 4; ++i) {
+            const float send = b1 ? y[i] : y[i + NC / 4];
+            z[i] = (b1 ? y[i + NC / 4] : y[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
         }
+#pragma unroll
+        for (int i = 0; i < NC / 8; ++i) {
+            const float send = b0 ? z[i] : z[i + NC / 8];
+            w[i] = (b0 ? z[i + NC / 8] : z[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+#pragma unroll
+        for (int i = 0; i < NC / 8; ++i) sm.red[warp][4 * (slot0 + i) + qd] = w[i];
         __syncthreads();
         if (tid < DV) {
             float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) s += sm.red[w][tid];
+            for (int w2 = 0; w2 < NW; ++w2) s += sm.red[w2][tid];
             sm.vec[tid] = s;
         }
         __syncthreads();
@@ -129,10 +142,10 @@ __global__ void __launch_bounds__(DK * 4, 1)
         }
         const int len = eos - bos, nch = (len + kChunk - 1) / kChunk;
         float* ck = ckpt_all + ((size_t)seq_first[s] * H + h) * st;  // chunk j at + j * H * st
-        const size_t sbase = ((size_t)s * H + h) * st + (size_t)c * DV + n0;
+        const size_t rbase = ((size_t)s * H + h) * st + (size_t)c * DV + qd;  // + 4 i: column 4 i + qd
         float S[NC], dS[NC];
 #pragma unroll
-        for (int i = 0; i < NC; ++i) S[i] = h0 ? h0[sbase + i] : 0.f;
+        for (int i = 0; i < NC; ++i) S[i] = h0 ? h0[rbase + 4 * i] : 0.f;
         // -------- 1. forward, checkpoints at chunk starts
         for (int j = 0; j < nch; ++j) {
             float* cj = ck + (size_t)j * H * st + (size_t)c * DV + n0;
@@ -172,12 +185,12 @@ __global__ void __launch_bounds__(DK * 4, 1)
                 }
                 col_sum(x);
 #pragma unroll
-                for (int i = 0; i < NC; ++i) S[i] = fmaf(be * kc, sm.v[tt][n0 + i] - sm.vec[n0 + i], P[i]);
+                for (int i = 0; i < NC; ++i) S[i] = fmaf(be * kc, sm.v[tt][4 * i + qd] - sm.vec[4 * i + qd], P[i]);
             }
         }
         // -------- 2. chunks in reverse
 #pragma unroll
-        for (int i = 0; i < NC; ++i) dS[i] = dhT ? dhT[sbase + i] : 0.f;
+        for (int i = 0; i < NC; ++i) dS[i] = dhT ? dhT[rbase + 4 * i] : 0.f;
         for (int j = nch - 1; j >= 0; --j) {
             const int t0 = bos + j * kChunk, rows = eos - t0 < kChunk ? eos - t0 : kChunk;
             const float* cj = ck + (size_t)j * H * st + (size_t)c * DV + n0;
@@ -238,24 +251,31 @@ __global__ void __launch_bounds__(DK * 4, 1)
                 col_sum(x);
                 if (tid < DV) sm.r[tt][tid] = sm.v[tt][tid] - sm.vec[tid];
 #pragma unroll
-                for (int i = 0; i < NC; ++i) S[i] = fmaf(be * kc, sm.v[tt][n0 + i] - sm.vec[n0 + i], P[i]);
+                for (int i = 0; i < NC; ++i) S[i] = fmaf(be * kc, sm.v[tt][4 * i + qd] - sm.vec[4 * i + qd], P[i]);
             }
             __syncthreads();  // sm.r complete
-            // tokens in reverse
-            for (int tt = rows - 1; tt >= 0; --tt) {
-                const size_t row = (size_t)b * d.T + t0 + tt;
+            // tokens in reverse; each step's S_{t-1} loads during the step before
+            float nxt[NC];
+            auto load_prev = [&](int tt) {
                 const float* sp = scr + (size_t)tt * st + (size_t)c * DV + n0;
-                float Sp[NC];
 #pragma unroll
                 for (int i = 0; i < NC; i += 4) {
                     const float4 w4 = *reinterpret_cast<const float4*>(sp + i);
-                    Sp[i] = w4.x; Sp[i + 1] = w4.y; Sp[i + 2] = w4.z; Sp[i + 3] = w4.w;
+                    nxt[i] = w4.x; nxt[i + 1] = w4.y; nxt[i + 2] = w4.z; nxt[i + 3] = w4.w;
                 }
+            };
+            if (rows > 0) load_prev(rows - 1);
+            for (int tt = rows - 1; tt >= 0; --tt) {
+                const size_t row = (size_t)b * d.T + t0 + tt;
+                float Sp[NC];
+#pragma unroll
+                for (int i = 0; i < NC; ++i) Sp[i] = nxt[i];
+                if (tt > 0) load_prev(tt - 1);
                 const float a = sm.al[tt][c], kc = sm.kh[tt][c], qc = sm.qh[tt][c], be = sm.beta[tt];
                 float dqh = 0.f, u = 0.f, x[NC];
 #pragma unroll
                 for (int i = 0; i < NC; ++i) {
-                    const float ri = sm.r[tt][n0 + i], di = sm.dout[tt][n0 + i];
+                    const float ri = sm.r[tt][4 * i + qd], di = sm.dout[tt][4 * i + qd];
                     const float St = fmaf(be * kc, ri, a * Sp[i]);
                     dS[i] = fmaf(scale * qc, di, dS[i]);
                     dqh = fmaf(St, di, dqh);
@@ -266,7 +286,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
                 float dkh2 = 0.f, dal = 0.f;
 #pragma unroll
                 for (int i = 0; i < NC; ++i) {
-                    const float dr = be * sm.vec[n0 + i];
+                    const float dr = be * sm.vec[4 * i + qd];
                     const float P = a * Sp[i];
                     const float dP = fmaf(-kc, dr, dS[i]);
                     dkh2 = fmaf(-P, dr, dkh2);
@@ -325,8 +345,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
         // -------- 3. the gradient of the initial state
         if (dh0) {
 #pragma unroll
-            for (int i = 0; i < NC; i += 4)
-                *reinterpret_cast<float4*>(dh0 + sbase + i) = make_float4(dS[i], dS[i + 1], dS[i + 2], dS[i + 3]);
+            for (int i = 0; i < NC; ++i) dh0[rbase + 4 * i] = dS[i];
         }
         __syncthreads();  // the chunk vectors and scratch are free for the next chain
     }
