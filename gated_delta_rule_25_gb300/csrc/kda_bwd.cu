@@ -38,13 +38,21 @@ __device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat
 __device__ __forceinline__ float ld_in(const float* p) { return *p; }
 
 // Shared memory of one CTA: the current chunk's per-token vectors and the
-// reduction scratch.
+// reduction scratch.  Vectors over the value columns are kept permuted and padded:
+// column n at vidx(n) = (n % 4) (dv/4 + 4) + n / 4, so that the dv/4 columns of
+// thread qd (n = 4 i + qd) are contiguous and the four threads of a row read them by
+// 16-byte loads in distinct banks.
+template <int DV>
+__host__ __device__ constexpr int vpad() { return 4 * (DV / 4 + 4); }
+template <int DV>
+__device__ __forceinline__ int vidx(int n) { return (n & 3) * (DV / 4 + 4) + (n >> 2); }
+
 template <int DK, int DV>
-struct BwdSmem {
+struct __align__(16) BwdSmem {
     float kh[kChunk][DK], qh[kChunk][DK], al[kChunk][DK];
-    float v[kChunk][DV], dout[kChunk][DV], r[kChunk][DV];
-    float red[DK / 8][DV];  // per-warp partial column sums
-    float vec[DV];          // a finished column sum
+    float v[kChunk][vpad<DV>()], dout[kChunk][vpad<DV>()], r[kChunk][vpad<DV>()];
+    float red[DK / 8][DV];  // per-warp partial column sums (natural order)
+    float vec[vpad<DV>()];  // a finished column sum
     float bpart[kChunk][DK / 8];
     float rk[kChunk], rq[kChunk], beta[kChunk];
 };
@@ -86,7 +94,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
     float* ckpt_all = reinterpret_cast<float*>(ws + L.ckpt);
     float* scr = reinterpret_cast<float*>(ws + L.scratch) + size_t(blockIdx.x) * kChunk * st;
 
-    // Sum over the state's rows of x[i] (column 4 i + qd), for every column: the result
+    // Sum over the state's rows of f x[i] (column 4 i + qd), for every column: the result
     // lands in sm.vec.  Inside a warp (8 rows) a butterfly: at each of three shuffle
     // distances a thread keeps half of its remaining slots and hands the other half to
     // its partner, ending with NC / 8 slots summed over the warp's rows (NC - 4
@@ -94,12 +102,12 @@ __global__ void __launch_bounds__(DK * 4, 1)
     // warps.  Two barriers; callers read sm.vec after it returns.
     const bool b2 = (lane >> 4) & 1, b1 = (lane >> 3) & 1, b0 = (lane >> 2) & 1;
     const int slot0 = (b2 ? NC / 2 : 0) + (b1 ? NC / 4 : 0) + (b0 ? NC / 8 : 0);
-    auto col_sum = [&](const float (&x)[NC]) {
+    auto col_sum = [&](const float (&x)[NC], float f) {
         float y[NC / 2], z[NC / 4], w[NC / 8];
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
-            const float send = b2 ? x[i] : x[i + NC / 2];
-            y[i] = (b2 ? x[i + NC / 2] : x[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+            const float lo = f * x[i], hi = f * x[i + NC / 2];
+            y[i] = (b2 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b2 ? lo : hi, 16);
         }
 #pragma unroll
         for (int i = 0; i < NC / 4; ++i) {
@@ -118,9 +126,14 @@ __global__ void __launch_bounds__(DK * 4, 1)
             float s = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < NW; ++w2) s += sm.red[w2][tid];
-            sm.vec[tid] = s;
+            sm.vec[vidx<DV>(tid)] = s;
         }
         __syncthreads();
+    };
+    // This thread's NC columns (4 i + qd) of a permuted vector: four of them (i = 4 j
+    // .. 4 j + 3) by one 16-byte load.
+    auto vq = [&](const float* vecp, int j) {
+        return reinterpret_cast<const float4*>(vecp + qd * (NC + 4))[j];
     };
     auto row_sum = [&](float x) {  // over the row's four threads
         x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -171,21 +184,22 @@ __global__ void __launch_bounds__(DK * 4, 1)
 #pragma unroll
                 for (int i = 0; i < DK / 32; ++i) sm.kh[tt][lane + 32 * i] = kk[i] * rk;
 #pragma unroll
-                for (int i = 0; i < DV / 32; ++i) sm.v[tt][lane + 32 * i] = ld_in(v + (row * H + h) * DV + lane + 32 * i);
+                for (int i = 0; i < DV / 32; ++i)
+                    sm.v[tt][vidx<DV>(lane + 32 * i)] = ld_in(v + (row * H + h) * DV + lane + 32 * i);
                 if (lane == 0) sm.beta[tt] = beta[row * H + h];
             }
             __syncthreads();
             for (int tt = 0; tt < rows; ++tt) {
                 const float a = sm.al[tt][c], kc = sm.kh[tt][c], be = sm.beta[tt];
-                float P[NC], x[NC];
+                col_sum(S, a * kc);  // P^T kh, P = Diag(alpha) S
 #pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    P[i] = a * S[i];
-                    x[i] = P[i] * kc;
+                for (int j = 0; j < NC / 4; ++j) {
+                    const float4 vv = vq(sm.v[tt], j), pk = vq(sm.vec, j);
+                    S[4 * j] = fmaf(be * kc, vv.x - pk.x, a * S[4 * j]);
+                    S[4 * j + 1] = fmaf(be * kc, vv.y - pk.y, a * S[4 * j + 1]);
+                    S[4 * j + 2] = fmaf(be * kc, vv.z - pk.z, a * S[4 * j + 2]);
+                    S[4 * j + 3] = fmaf(be * kc, vv.w - pk.w, a * S[4 * j + 3]);
                 }
-                col_sum(x);
-#pragma unroll
-                for (int i = 0; i < NC; ++i) S[i] = fmaf(be * kc, sm.v[tt][4 * i + qd] - sm.vec[4 * i + qd], P[i]);
             }
         }
         // -------- 2. chunks in reverse
@@ -226,8 +240,8 @@ __global__ void __launch_bounds__(DK * 4, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < DV / 32; ++i) {
-                    sm.v[tt][lane + 32 * i] = ld_in(v + ov + lane + 32 * i);
-                    sm.dout[tt][lane + 32 * i] = ld_in(dout + ov + lane + 32 * i);
+                    sm.v[tt][vidx<DV>(lane + 32 * i)] = ld_in(v + ov + lane + 32 * i);
+                    sm.dout[tt][vidx<DV>(lane + 32 * i)] = ld_in(dout + ov + lane + 32 * i);
                 }
                 if (lane == 0) {
                     sm.rk[tt] = rk;
@@ -242,16 +256,16 @@ __global__ void __launch_bounds__(DK * 4, 1)
 #pragma unroll
                 for (int i = 0; i < NC; i += 4) *reinterpret_cast<float4*>(sp + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
                 const float a = sm.al[tt][c], kc = sm.kh[tt][c], be = sm.beta[tt];
-                float P[NC], x[NC];
+                col_sum(S, a * kc);  // P^T kh, P = Diag(alpha) S
+                if (tid < DV) sm.r[tt][vidx<DV>(tid)] = sm.v[tt][vidx<DV>(tid)] - sm.vec[vidx<DV>(tid)];
 #pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    P[i] = a * S[i];
-                    x[i] = P[i] * kc;
+                for (int j = 0; j < NC / 4; ++j) {
+                    const float4 vv = vq(sm.v[tt], j), pk = vq(sm.vec, j);
+                    S[4 * j] = fmaf(be * kc, vv.x - pk.x, a * S[4 * j]);
+                    S[4 * j + 1] = fmaf(be * kc, vv.y - pk.y, a * S[4 * j + 1]);
+                    S[4 * j + 2] = fmaf(be * kc, vv.z - pk.z, a * S[4 * j + 2]);
+                    S[4 * j + 3] = fmaf(be * kc, vv.w - pk.w, a * S[4 * j + 3]);
                 }
-                col_sum(x);
-                if (tid < DV) sm.r[tt][tid] = sm.v[tt][tid] - sm.vec[tid];
-#pragma unroll
-                for (int i = 0; i < NC; ++i) S[i] = fmaf(be * kc, sm.v[tt][4 * i + qd] - sm.vec[4 * i + qd], P[i]);
             }
             __syncthreads();  // sm.r complete
             // tokens in reverse; each step's S_{t-1} loads during the step before
@@ -272,26 +286,36 @@ __global__ void __launch_bounds__(DK * 4, 1)
                 for (int i = 0; i < NC; ++i) Sp[i] = nxt[i];
                 if (tt > 0) load_prev(tt - 1);
                 const float a = sm.al[tt][c], kc = sm.kh[tt][c], qc = sm.qh[tt][c], be = sm.beta[tt];
-                float dqh = 0.f, u = 0.f, x[NC];
+                float dqh = 0.f, u = 0.f;
 #pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    const float ri = sm.r[tt][4 * i + qd], di = sm.dout[tt][4 * i + qd];
-                    const float St = fmaf(be * kc, ri, a * Sp[i]);
-                    dS[i] = fmaf(scale * qc, di, dS[i]);
-                    dqh = fmaf(St, di, dqh);
-                    u = fmaf(dS[i], ri, u);
-                    x[i] = dS[i] * kc;
+                for (int j = 0; j < NC / 4; ++j) {
+                    const float4 r4 = vq(sm.r[tt], j), d4 = vq(sm.dout[tt], j);
+                    const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * j + e;
+                        const float St = fmaf(be * kc, rr[e], a * Sp[i]);
+                        dS[i] = fmaf(scale * qc, dd[e], dS[i]);
+                        dqh = fmaf(St, dd[e], dqh);
+                        u = fmaf(dS[i], rr[e], u);
+                    }
                 }
-                col_sum(x);  // sm.vec = dS^T kh
+                col_sum(dS, kc);  // sm.vec = dS^T kh
                 float dkh2 = 0.f, dal = 0.f;
 #pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    const float dr = be * sm.vec[4 * i + qd];
-                    const float P = a * Sp[i];
-                    const float dP = fmaf(-kc, dr, dS[i]);
-                    dkh2 = fmaf(-P, dr, dkh2);
-                    dal = fmaf(dP, Sp[i], dal);
-                    dS[i] = a * dP;
+                for (int j = 0; j < NC / 4; ++j) {
+                    const float4 c4 = vq(sm.vec, j);
+                    const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * j + e;
+                        const float dr = be * cs[e];
+                        const float P = a * Sp[i];
+                        const float dP = fmaf(-kc, dr, dS[i]);
+                        dkh2 = fmaf(-P, dr, dkh2);
+                        dal = fmaf(dP, Sp[i], dal);
+                        dS[i] = a * dP;
+                    }
                 }
                 dqh = row_sum(dqh);
                 u = row_sum(u);
@@ -303,7 +327,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
                     dq[ok] = scale * dqh;         // dqh; normalised below
                     dg[ok] = dal * a;
                 }
-                if (tid < DV) dv[(row * H + h) * DV + tid] = be * sm.vec[tid];
+                if (tid < DV) dv[(row * H + h) * DV + tid] = be * sm.vec[vidx<DV>(tid)];
                 float bp = qd == 0 ? kc * u : 0.f;  // this warp's rows' share of dbeta
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) bp += __shfl_xor_sync(0xffffffffu, bp, o);
