@@ -277,11 +277,15 @@ kda_status kda_decode(const void* q, const void* k, const void* v, kda_dtype qkv
  * device), 256-byte aligned, caller-owned scratch; it holds the state at every
  * chunk start and, per CTA, the states of one chunk.
  *
- * Computation: one CTA per (sequence, head) chain at a time, fp32 state in
- * registers, fp32 arithmetic on the CUDA cores: the forward recomputed with
- * checkpoints at chunk starts, then every chunk in reverse (its states recomputed,
- * then its tokens in reverse).  Two launches (the schedule kernel, the backward).
- * Statuses as kda_fwd (malformed cu_seqlens: the device error word, kda_fwd_check).
+ * Computation: one CTA per (sequence, head, 32 value columns) at a time (the value
+ * columns never mix in the recurrence), fp32 state in registers, fp32 arithmetic
+ * on the CUDA cores: the forward recomputed with checkpoints at chunk starts, then
+ * every chunk in reverse (its states recomputed, then its tokens in reverse).  The
+ * sums over value columns (dq, dk, dg, dbeta) are added tile by tile into the
+ * zeroed outputs, so their last bits may differ between runs.  Launches: the
+ * schedule kernel, four memsets of those outputs, the backward, a kernel applying
+ * the L2 normalisations' derivatives.  Statuses as kda_fwd (malformed cu_seqlens:
+ * the device error word, kda_fwd_check).
  */
 size_t kda_bwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs);
 kda_status kda_bwd(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
