@@ -137,3 +137,39 @@ def test_fwd_ex_gate_dtypes(lib):
     assert call(0, 5) == 2      # unknown gate dtype
     assert call(0, 0, wsb=16) == 4   # valid dtypes reach the workspace check
     assert call(0, 1, wsb=16) == 4
+
+
+def _bwd(lib, **kw):
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails host checks
+    args = dict(q=p, k=p, v=p, dt=0, g=p, beta=p, h0=None, cu=None, N=1, B=1, T=64, H=2, dk=64,
+                dv=64, scale=0.125, do=p, dhT=None, dq=p, dk_=p, dv_=p, dg=p, db=p, dh0=None,
+                ws=ctypes.c_void_p(1 << 20), wsb=1 << 40, stream=None)
+    args.update(kw)
+    a = args
+    return lib.kda_bwd(a["q"], a["k"], a["v"], a["dt"], a["g"], a["beta"], a["h0"], a["cu"], a["N"],
+                       a["B"], a["T"], a["H"], a["dk"], a["dv"], a["scale"], a["do"], a["dhT"], a["dq"],
+                       a["dk_"], a["dv_"], a["dg"], a["db"], a["dh0"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_bwd_host_validation(lib):
+    assert lib.kda_bwd_workspace_size(1, 8192, 32, 128, 128, 1) > 0
+    assert lib.kda_bwd_workspace_size(1, 8192, 32, 96, 128, 1) == 0
+    assert _bwd(lib, dk=96) == 2                      # unsupported head dim
+    assert _bwd(lib, dt=7) == 2                       # unknown dtype
+    assert _bwd(lib, scale=float("nan")) == 1
+    assert _bwd(lib, B=2, N=1) == 1                   # fixed length needs N == B
+    assert _bwd(lib, do=None) == 1                    # an input gradient is missing
+    assert _bwd(lib, dq=None) == 1                    # an output is missing
+    assert _bwd(lib, dg=ctypes.c_void_p((1 << 20) + 4)) == 3       # misaligned
+    assert _bwd(lib, wsb=16) == 4                     # workspace too small
+    assert _bwd(lib, ws=ctypes.c_void_p((1 << 20) + 128)) == 4     # workspace misaligned
+    assert _bwd(lib, N=0, B=0, T=0) == 0              # nothing to do: no launch
+
+
+def test_python_bwd_fails_loudly_without_cuda():
+    import torch
+
+    import gated_delta_rule_25_gb300 as kda
+    x = torch.zeros(1, 4, 1, 64)
+    with pytest.raises(ValueError):
+        kda.bwd(x, x, x, x.float(), torch.zeros(1, 4, 1), do=x)
