@@ -626,10 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // float4 of F^T's row m and one of the tile's row m: conflict-free and broadcast),
 // and the four partial blocks are added with Z_k through shared memory.
 constexpr int kScanCols = 16, kScanThreads = 512, kScanK = 4;
+constexpr int kPrevLd = kScanCols + 4;  // padded rows: the output threads' row-wise writes hit distinct banks
 struct __align__(16) ScanSmem {
     float FT[2][kCDK * kCDK];
-    float prev[kCDK][kScanCols];
-    float part[kScanK][kCDK][kScanCols];
+    float prev[kCDK][kPrevLd];
+    // partial 4 x 4 blocks: [quarter][column group][row group][4 float4], the float4 of
+    // block row r at position r ^ ((row group / 2) & 3), so that the 8 threads of a
+    // quarter warp store to distinct banks
+    float part[kScanK][kScanCols / 4][kCDK / 4][16];
     uint64_t full[2];
     int abort;
 };
@@ -650,7 +654,8 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
     const float* FT = reinterpret_cast<const float*>(ws + W.seg_f);
     const int tid = threadIdx.x;
     const int kq = tid >> 7, rg = tid & 31, cg = (tid >> 5) & 3;  // m quarter; rows 4 rg .., columns 4 cg ..
-    const int orow = tid >> 2, ocol = 4 * (tid & 3);                // the output float4 of this thread
+    const int orow = tid & (DK - 1), ocol = 4 * (tid >> 7);          // the output float4 of this thread
+    const int swz = (rg >> 1) & 3, oswz = ((orow >> 2) >> 1) & 3;
     uint32_t issued[2] = {0, 0};
     if (tid == 0) {
         ptx::mbar_init(&sm.full[0], 1);
@@ -682,11 +687,16 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
         if (!ok) break;
         float acc[4][4] = {};
         const float* ft = sm.FT[b] + kq * kM * DK + 4 * rg;
-#pragma unroll 8
+        const float* pv = &sm.prev[kq * kM][4 * cg];
+        // the loads of m + 1 are in flight while m's 16 products run
+        float4 f = *reinterpret_cast<const float4*>(ft), p = *reinterpret_cast<const float4*>(pv);
+#pragma unroll 4
         for (int m = 0; m < kM; ++m) {
-            const float4 f = *reinterpret_cast<const float4*>(ft + m * DK);
-            const float4 p = *reinterpret_cast<const float4*>(&sm.prev[kq * kM + m][4 * cg]);
             const float fr[4] = {f.x, f.y, f.z, f.w}, pc[4] = {p.x, p.y, p.z, p.w};
+            if (m + 1 < kM) {
+                f = *reinterpret_cast<const float4*>(ft + (m + 1) * DK);
+                p = *reinterpret_cast<const float4*>(pv + (m + 1) * kPrevLd);
+            }
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -694,14 +704,15 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<float4*>(&sm.part[kq][4 * rg + r][4 * cg]) =
+            *reinterpret_cast<float4*>(&sm.part[kq][cg][rg][4 * (r ^ swz)]) =
                 make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         __syncthreads();  // every partial block written; the previous start state and F buffer b read
         float4 v = z;
 #pragma unroll
         for (int q = 0; q < kScanK; ++q) {
-            const float4 p = *reinterpret_cast<const float4*>(&sm.part[q][orow][ocol]);
-            v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+            const float4 pp = *reinterpret_cast<const float4*>(
+                &sm.part[q][ocol >> 2][orow >> 2][4 * ((orow & 3) ^ oswz)]);
+            v.x += pp.x; v.y += pp.y; v.z += pp.z; v.w += pp.w;
         }
         *reinterpret_cast<float4*>(&sm.prev[orow][ocol]) = v;
         *reinterpret_cast<float4*>(Ek) = v;
