@@ -241,7 +241,7 @@ def test_malformed_cu_seqlens_reports_device_error(kda):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_fp32_inputs_run_u_and_w_on_tf32(kda, d):
-    """fp32 q, k, v (BASELINE config 1) compute u = X Diag(beta) v and w on tf32
+    """fp32 q, k, v (the cfg1 workload) compute u = X Diag(beta) v and w on tf32
     operands.  Against the fp64 oracle on the fp32 values, that path is more accurate
     than casting the same values to bf16 and running the bf16 path, which rounds v
     and kh gamma to bf16 operands (as fp32 inputs were computed before)."""
