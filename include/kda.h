@@ -76,7 +76,10 @@ typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
  * Bytes of device workspace kda_fwd needs for these sizes (0 on bad sizes).
  * B, T, H: batch, tokens per batch row, heads; num_seqs: N (== B when fixed length).
  * The workspace holds a schedule of chunks and the per-chunk factors of the
- * chunkwise form; its contents are scratch and need no initialisation.
+ * chunkwise form and, where few long chains may be cut into segments (dk = dv =
+ * 128, N * H <= 64), a region for the segments' start states and maps (up to 20 MB);
+ * a smaller workspace of at least the rest runs the chains whole.  Its contents are
+ * scratch and need no initialisation.
  */
 size_t kda_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs);
 
@@ -106,9 +109,12 @@ kda_status kda_fwd_check(const void* workspace, kda_stream_t stream, uint32_t* d
 const char* kda_status_string(kda_status status);
 
 /* Number of kernel launches kda_fwd enqueues for these sizes under the current
- * pipeline setting (for launch counts): 2 with the fused pipeline (schedule, fused),
- * 3 with the split one (schedule, factors, state), 4 when the split pipeline leaves
- * the choice of state kernel to the device (both launched). */
+ * pipeline setting, with a workspace of kda_fwd_workspace_size bytes (for launch
+ * counts): 2 with the fused pipeline (schedule, fused); with the split one 3
+ * (schedule, factors, state), 4 when it leaves the choice between the tiled and the
+ * 128-column state kernels to the device (both launched), 5 with segments chosen on
+ * the host (schedule, factors, pass A, scan, pass C), 6 when the device decides on
+ * segments (the tiled state kernel, then the three segment kernels). */
 int kda_fwd_launch_count(int B, int T, int H, int dk, int dv, int num_seqs);
 
 /*
