@@ -370,17 +370,10 @@ def run_decode(args):
     print(json.dumps(line), flush=True)
 
 
-def run_backward(args):
-    """--backward: times kda_bwd (the gradients of sum(o do) + sum(h_T dh_T)) on the
-    workload's inputs with random do and dh_T (CUDA events, inputs resident), then
-    checks two heads' gradients against the fp64 autograd oracle."""
-    import __graft_entry__
-    __graft_entry__.build()
-    import gated_delta_rule_25_gb300 as kda
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    salt = gen.fresh_salt()
-    x, desc = make_workload(args.workload, 0, salt)
+def measure_backward(kda, x, dev, steps: int, warmup: int, parity: bool, salt: int) -> dict:
+    """Times kda_bwd (the gradients of sum(o do) + sum(h_T dh_T)) on x with random do
+    and dh_T (CUDA events on the launching stream, inputs resident) and, with
+    `parity`, checks two heads' gradients against the fp64 autograd oracle."""
     xd = x.to(dev)
     rng = np.random.default_rng(salt)
     do = torch.from_numpy(rng.standard_normal(tuple(x.v.shape)).astype(np.float32)).to(x.v.dtype)
@@ -393,22 +386,18 @@ def run_backward(args):
     def step():
         return kda.bwd(**xd.tensors(), do=do_d, dhT=dhT_d, workspace=ws)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(0)
-    clocks.start()
-    time.sleep(0.2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         out = step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    parity = None
-    if not args.no_parity:
+    ms = e0.elapsed_time(e1) / steps
+    par = None
+    if parity:
         from oracle.backward import kda_backward_fp64
         from tests.metrics import rel_rmse
         hs = sorted({0, min(1, x.H - 1)})
@@ -418,20 +407,34 @@ def run_backward(args):
         if t["h0"] is not None:
             t["h0"] = t["h0"][:, hs].contiguous()
         ref = kda_backward_fp64(**t, do=do[:, :, hs].double(), dhT=dhT[:, hs].double())
-        names = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
-        parity = {"heads": hs}
-        for name, a, r in zip(names, out, ref):
+        par = {"heads": hs}
+        for name, a, r in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), out, ref):
             a = a.cpu()
             a = a[:, hs] if name == "dh0" else a[:, :, hs]
-            parity[name + "_rel_rmse"] = rel_rmse(a, r)
-    line = {
-        "metric": "KDA backward tokens/s (gradients of o and h_T for q, k, v, g, beta, h0)",
-        "value": x.tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32",
-        "data": "synthetic", "config": {"workload": desc, "name": args.workload, "tokens_per_step": x.tokens,
-                                        "heads": x.H, "dk": x.dk, "dv": x.dv, "salt": salt},
-        "gpu_launches": 2 * args.steps, "clocks": clk, "parity": parity,
-    }
+            par[name + "_rel_rmse"] = rel_rmse(a, r)
+    return {"metric": "KDA backward tokens/s (gradients of o and h_T for q, k, v, g, beta, h0)",
+            "value": x.tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "warmup": warmup, "dtype": "f32", "kernels_per_step": 3, "parity": par}
+
+
+def run_backward(args):
+    """--backward: the backward pass on the workload instead of the forward."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import gated_delta_rule_25_gb300 as kda
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    salt = gen.fresh_salt()
+    x, desc = make_workload(args.workload, 0, salt)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.2)
+    res = measure_backward(kda, x, dev, args.steps, args.warmup, not args.no_parity, salt)
+    clk = clocks.stop()
+    line = dict(res, n_gpus=1, higher_is_better=True, data="synthetic",
+                config={"workload": desc, "name": args.workload, "tokens_per_step": x.tokens,
+                        "heads": x.H, "dk": x.dk, "dv": x.dv, "salt": salt},
+                gpu_launches=3 * args.steps, clocks=clk)
     print(json.dumps(line), flush=True)
 
 
@@ -445,6 +448,8 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (kda_bwd) on the workload instead of the forward")
     ap.add_argument("--no-parity", action="store_true", help="--backward: skip the oracle check")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="forward runs: skip the backward pass's measurement in the JSON line")
     ap.add_argument("--pipeline", default="auto", choices=["auto", "fused", "split", "split-whole"],
                     help="auto (default): the library's choice for the sizes; fused: factor "
                          "production and state chains in one kernel; split: a factor kernel, "
@@ -633,6 +638,11 @@ def main():
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x)
+    # the backward pass on the same inputs (f3; a few steps, two heads against the
+    # autograd oracle), for workloads of up to 16,384 tokens
+    bwd = None
+    if world == 1 and not args.no_backward and x.tokens <= 16384:
+        bwd = measure_backward(kda, x, dev, 3, 1, True, salt)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -657,6 +667,7 @@ def main():
                 "outputs_match": e2e_ok},
         "parity": parity,
         "cpu_baseline": cpu,
+        "backward": bwd,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
