@@ -99,3 +99,28 @@ def test_bwd_many_chains(kda):
     x = gen.make_lengths(lens, seed=57, salt=SALT, H=1, d=64)
     assert x.num_seqs * x.H > 152
     _check(kda, x, seed=7)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "cfg3"])
+def test_bwd_full_size_sampled_heads(kda, name):
+    """The full cfg2 (8,192 tokens x 32 heads) and cfg3 (varlen) sizes through the GPU
+    backward; the oracle checks two heads (the heads are independent chains)."""
+    x = {"cfg2": gen.make_cfg2, "cfg3": gen.make_cfg3}[name](seed=58, salt=SALT)
+    rng = np.random.default_rng(8)
+    do = torch.from_numpy(rng.standard_normal(tuple(x.v.shape)).astype(np.float32)).to(x.v.dtype)
+    dhT = torch.from_numpy(rng.standard_normal((x.num_seqs, x.H, x.dk, x.dv)).astype(np.float32))
+    xd = x.to("cuda")
+    got = kda.bwd(**xd.tensors(), do=do.to("cuda"), dhT=dhT.to("cuda"), check=True)
+    torch.cuda.synchronize()
+    hs = [0, x.H - 1]
+    t = x.tensors()
+    for key in ("q", "k", "v", "g", "beta"):
+        t[key] = t[key][:, :, hs].contiguous()
+    t["h0"] = t["h0"][:, hs].contiguous()
+    ref = kda_backward_fp64(**t, do=do[:, :, hs].double(), dhT=dhT[:, hs].double())
+    errs = {}
+    for name_, a, r in zip(NAMES, got, ref):
+        a = a.cpu()
+        a = a[:, hs] if name_ == "dh0" else a[:, :, hs]
+        errs[name_] = rel_rmse(a, r)
+    assert all(e <= TOL for e in errs.values()), f"{x.name} salt={x.salt}: {errs}"
