@@ -61,6 +61,9 @@ def make_workload(name: str, seed: int, salt: int):
         x = gen.make_cfg2(seed=seed, salt=salt)
         x.g = x.g.to(torch.bfloat16)
         return x, WORKLOADS["cfg2"].replace("fp32 g/beta/h0", "bf16 g, fp32 beta/h0")
+    if name == "cfg2-d64":
+        x = gen.make_cfg2(seed=seed, salt=salt, d=64)
+        return x, WORKLOADS["cfg2"].replace("dk=dv=128", "dk=dv=64")
     if name == "cfg3":
         return gen.make_cfg3(seed=seed, salt=salt), WORKLOADS[name]
     if name == "cfg4":
@@ -456,7 +459,7 @@ def main():
                          "then the state kernels (few long chains cut into segments where "
                          "predicted faster); split-whole: split, chains never cut")
     ap.add_argument("--workload", default="cfg2",
-                    help="cfg2 (the headline workload), cfg2-gbf16 (bf16 gate), cfg3, cfg4, "
+                    help="cfg2 (the headline workload), cfg2-gbf16 (bf16 gate), cfg2-d64 (dk = dv = 64), cfg3, cfg4, "
                          "cfg5-{fixed|varlen}-H{16|32|64}-{total}, long-B{B}-H{H}-{T} "
                          "(few long fixed-length chains), "
                          "decode-N{sequences}-H{heads}")
