@@ -5,9 +5,11 @@
 //
 // The value columns of the state never mix in the recurrence (S[:, n] evolves from
 // kh, alpha, beta and v[n] alone), and neither do those of its gradient, so the
-// work item is one (sequence, head, 32-column tile): a persistent grid takes items
-// in steps of its size.  4 * dk threads per CTA: thread (c, qd) holds row c of the
-// tile's fp32 state S and of its gradient dS, columns qd, qd + 4, ... of the tile
+// work item is one (sequence, head, tile of NVT = 32 or 64 columns; 64 once 32-column
+// items would fill the SMs more than twice, so that each token's barriers are shared
+// by more work): a persistent grid takes items in steps of its size.  4 * dk threads
+// per CTA: thread (c, qd) holds row c of the tile's fp32 state S and of its gradient
+// dS, columns qd, qd + 4, ... of the tile
 // (interleaved, so that the four threads of a row read consecutive words of a
 // shared vector).  Per item:
 //   1. forward over the chain, the tile's state at the start of every 64-token
@@ -38,45 +40,51 @@ namespace kda {
 namespace {
 
 constexpr float kEps = 1e-6f;  // the L2-normalisation epsilon of the forward
-constexpr int kNVT = 32;       // value columns per work item
 
 __device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float ld_in(const float* p) { return *p; }
 
 // Vectors over a tile's columns are kept permuted and padded: column n at
-// vidx(n) = (n % 4) (NC + 4) + n / 4, so that the NC columns of thread qd (n = 4 i +
-// qd) are contiguous and the four threads of a row read them by 16-byte loads in
-// distinct banks.
-constexpr int kNC = kNVT / 4;
-constexpr int kVP = 4 * (kNC + 4);
-__device__ __forceinline__ int vidx(int n) { return (n & 3) * (kNC + 4) + (n >> 2); }
+// vidx(n) = (n % 4) (NC + 4) + n / 4 (NC = NVT / 4), so that the NC columns of
+// thread qd (n = 4 i + qd) are contiguous and the four threads of a row read them by
+// 16-byte loads in distinct banks.
+template <int NVT>
+__host__ __device__ constexpr int vpad() { return 4 * (NVT / 4 + 4); }
+template <int NVT>
+__device__ __forceinline__ int vidx(int n) { return (n & 3) * (NVT / 4 + 4) + (n >> 2); }
 
 // Shared memory of one CTA: the current chunk's per-token vectors and the
 // reduction scratch.
-template <int DK>
+template <int DK, int NVT>
 struct __align__(16) BwdSmem {
     float kh[kChunk][DK], qh[kChunk][DK], al[kChunk][DK];
-    float v[kChunk][kVP], dout[kChunk][kVP], r[kChunk][kVP];
-    float red[DK / 8][kNVT];  // per-warp partial column sums (natural order)
-    float vec[kVP];           // a finished column sum
+    float v[kChunk][vpad<NVT>()], dout[kChunk][vpad<NVT>()], r[kChunk][vpad<NVT>()];
+    float red[DK / 8][NVT];  // per-warp partial column sums (natural order)
+    float vec[vpad<NVT>()];  // a finished column sum
     float bpart[kChunk][DK / 8];
     float beta[kChunk];
 };
+
+// Value columns per work item for these sizes (on this device).
+int bwd_nvt(const Dims& d) {
+    const long long items32 = (long long)d.N * d.H * (d.dv / 32);
+    return d.dv >= 64 && items32 > 2LL * num_sms() ? 64 : 32;
+}
 
 // Workspace: the forward's schedule (header, sequence table, chunk table), then the
 // checkpoints (per (chunk, head): the state at the chunk's start) and each CTA's
 // scratch (the tile's states S_{t-1} of one chunk).
 struct BwdLayout {
     size_t ckpt, scratch, total;
-    __host__ __device__ BwdLayout(const Dims& d, int grid) {
+    __host__ __device__ BwdLayout(const Dims& d, int grid, int nvt) {
         const WsLayout W(d);
         ckpt = align256(W.plist);
         scratch = ckpt + size_t(W.cmax) * d.H * d.dk * d.dv * 4;
-        total = scratch + size_t(grid) * kChunk * d.dk * kNVT * 4;
+        total = scratch + size_t(grid) * kChunk * d.dk * nvt * 4;
     }
 };
 
-template <int DK, int DV, typename TIn>
+template <int DK, int DV, int NVT, typename TIn>
 __global__ void __launch_bounds__(DK * 4, 1)
     bwd_kernel(Dims d, const int32_t* __restrict__ cu, const TIn* __restrict__ q, const TIn* __restrict__ k,
                const TIn* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
@@ -84,11 +92,11 @@ __global__ void __launch_bounds__(DK * 4, 1)
                float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
                float* __restrict__ dg, float* __restrict__ dbeta, float* __restrict__ dh0,
                uint8_t* __restrict__ ws) {
-    constexpr int NT = DK * 4, NC = kNC, NW = NT / 32, NTILE = DV / kNVT;
+    constexpr int NT = DK * 4, NC = NVT / 4, NW = NT / 32, NTILE = DV / NVT;
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    BwdSmem<DK>& sm = *reinterpret_cast<BwdSmem<DK>*>(smem_raw);
+    BwdSmem<DK, NVT>& sm = *reinterpret_cast<BwdSmem<DK, NVT>*>(smem_raw);
     const WsLayout W(d);
-    const BwdLayout L(d, (int)gridDim.x);
+    const BwdLayout L(d, (int)gridDim.x, NVT);
     const Header* hdr = reinterpret_cast<const Header*>(ws + W.header);
     if (hdr->error) return;  // malformed cu_seqlens (reported in the error word)
     const int32_t* seq_first = reinterpret_cast<const int32_t*>(ws + W.seq_first);
@@ -97,7 +105,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
     const int H = d.H;
     const size_t st = size_t(DK) * DV;
     float* ckpt_all = reinterpret_cast<float*>(ws + L.ckpt);
-    float* scr = reinterpret_cast<float*>(ws + L.scratch) + size_t(blockIdx.x) * kChunk * DK * kNVT;
+    float* scr = reinterpret_cast<float*>(ws + L.scratch) + size_t(blockIdx.x) * kChunk * DK * NVT;
 
     // Sum over the state's rows of f x[i] (column 4 i + qd of the tile), for every
     // column: the result lands in sm.vec.  Inside a warp (8 rows) a butterfly: at each
@@ -127,11 +135,11 @@ __global__ void __launch_bounds__(DK * 4, 1)
 #pragma unroll
         for (int i = 0; i < NC / 8; ++i) sm.red[warp][4 * (slot0 + i) + qd] = w[i];
         __syncthreads();
-        if (tid < kNVT) {
+        if (tid < NVT) {
             float s = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < NW; ++w2) s += sm.red[w2][tid];
-            sm.vec[vidx(tid)] = s;
+            sm.vec[vidx<NVT>(tid)] = s;
         }
         __syncthreads();
     };
@@ -149,7 +157,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
     auto fwd_step = [&](float (&S)[NC], int tt, bool keep_r) {
         const float a = sm.al[tt][c], kc = sm.kh[tt][c], be = sm.beta[tt];
         col_sum(S, a * kc);  // P^T kh, P = Diag(alpha) S
-        if (keep_r && tid < kNVT) sm.r[tt][vidx(tid)] = sm.v[tt][vidx(tid)] - sm.vec[vidx(tid)];
+        if (keep_r && tid < NVT) sm.r[tt][vidx<NVT>(tid)] = sm.v[tt][vidx<NVT>(tid)] - sm.vec[vidx<NVT>(tid)];
 #pragma unroll
         for (int j = 0; j < NC / 4; ++j) {
             const float4 vv = vq(sm.v[tt], j), pk = vq(sm.vec, j);
@@ -187,8 +195,11 @@ __global__ void __launch_bounds__(DK * 4, 1)
                 sm.kh[tt][lane + 32 * i] = kk[i] * rk;
                 if (full) sm.qh[tt][lane + 32 * i] = qq[i] * rq;
             }
-            sm.v[tt][vidx(lane)] = ld_in(v + ov + lane);  // kNVT == 32: one column per lane
-            if (full) sm.dout[tt][vidx(lane)] = ld_in(dout + ov + lane);
+#pragma unroll
+            for (int i = 0; i < NVT / 32; ++i) {
+                sm.v[tt][vidx<NVT>(lane + 32 * i)] = ld_in(v + ov + lane + 32 * i);
+                if (full) sm.dout[tt][vidx<NVT>(lane + 32 * i)] = ld_in(dout + ov + lane + 32 * i);
+            }
             if (lane == 0) sm.beta[tt] = beta[row * H + h];
         }
         __syncthreads();
@@ -197,7 +208,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
     const int items = d.N * H * NTILE;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int chain = item / NTILE, tile = item - chain * NTILE;
-        const int s = chain / H, h = chain - s * H, col0 = tile * kNVT;
+        const int s = chain / H, h = chain - s * H, col0 = tile * NVT;
         int b, bos, eos;
         if (d.varlen) {
             b = 0;
@@ -239,7 +250,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
             load_chunk(b, t0, rows, h, col0, true);
             // the chunk's states S_{t-1} into the scratch, and r_t
             for (int tt = 0; tt < rows; ++tt) {
-                float* sp = scr + (size_t)tt * DK * kNVT + (size_t)c * kNVT + n0;
+                float* sp = scr + (size_t)tt * DK * NVT + (size_t)c * NVT + n0;
 #pragma unroll
                 for (int i = 0; i < NC; i += 4) *reinterpret_cast<float4*>(sp + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
                 fwd_step(S, tt, true);
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
             // tokens in reverse; each step's S_{t-1} loads during the step before
             float nxt[NC];
             auto load_prev = [&](int tt) {
-                const float* sp = scr + (size_t)tt * DK * kNVT + (size_t)c * kNVT + n0;
+                const float* sp = scr + (size_t)tt * DK * NVT + (size_t)c * NVT + n0;
 #pragma unroll
                 for (int i = 0; i < NC; i += 4) {
                     const float4 w4 = *reinterpret_cast<const float4*>(sp + i);
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(DK * 4, 1)
                     atomicAdd(dq + ok, scale * dqh);         // dqh; the same
                     atomicAdd(dg + ok, dal * a);
                 }
-                if (tid < kNVT) dv[(row * H + h) * DV + col0 + tid] = be * sm.vec[vidx(tid)];
+                if (tid < NVT) dv[(row * H + h) * DV + col0 + tid] = be * sm.vec[vidx<NVT>(tid)];
                 float bp = qd == 0 ? kc * u : 0.f;  // this warp's rows' share of dbeta
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) bp += __shfl_xor_sync(0xffffffffu, bp, o);
@@ -377,20 +388,20 @@ __global__ void __launch_bounds__(256) bwd_finish_kernel(Dims d, const TIn* __re
 }
 
 int bwd_grid(const Dims& d) {
-    const long long items = (long long)d.N * d.H * (d.dv / kNVT);
+    const long long items = (long long)d.N * d.H * (d.dv / bwd_nvt(d));
     const int sms = num_sms();
     return (int)(items < sms ? (items > 0 ? items : 1) : sms);
 }
 
-template <int DK, int DV, typename TIn>
+template <int DK, int DV, int NVT, typename TIn>
 cudaError_t launch_bwd_t(const Dims& d, const int32_t* cu, const void* q, const void* k, const void* v,
                          const float* g, const float* beta, const float* h0, const void* dout,
                          const float* dhT, float scale, float* dq, float* dk, float* dv, float* dg,
                          float* dbeta, float* dh0, uint8_t* ws, cudaStream_t stream) {
-    static_assert(DV % kNVT == 0 && kNVT == 32, "value tiles of one column per lane");
-    auto kern = bwd_kernel<DK, DV, TIn>;
-    const size_t smem = sizeof(BwdSmem<DK>);
-    static_assert(sizeof(BwdSmem<DK>) <= 227 * 1024, "backward shared memory");
+    static_assert(DV % NVT == 0 && NVT % 32 == 0, "value tiles of whole warps of columns");
+    auto kern = bwd_kernel<DK, DV, NVT, TIn>;
+    const size_t smem = sizeof(BwdSmem<DK, NVT>);
+    static_assert(sizeof(BwdSmem<DK, NVT>) <= 227 * 1024, "backward shared memory");
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const size_t tok = (size_t)d.B * d.T * d.H;
@@ -414,23 +425,27 @@ cudaError_t launch_bwd_t(const Dims& d, const int32_t* cu, const void* q, const 
 
 }  // namespace
 
-size_t bwd_workspace_bytes(const Dims& d) { return BwdLayout(d, bwd_grid(d)).total; }
+size_t bwd_workspace_bytes(const Dims& d) { return BwdLayout(d, bwd_grid(d), bwd_nvt(d)).total; }
 
 cudaError_t launch_bwd(const Dims& d, bool qkv_bf16, const int32_t* cu, const void* q, const void* k,
                        const void* v, const float* g, const float* beta, const float* h0, const void* dout,
                        const float* dhT, float scale, float* dq, float* dk, float* dv, float* dg,
                        float* dbeta, float* dh0, uint8_t* ws, cudaStream_t stream) {
     using bf = __nv_bfloat16;
-#define KDA_BWD_CASE(DK_, DV_)                                                                        \
-    if (d.dk == DK_ && d.dv == DV_)                                                                   \
-        return qkv_bf16 ? launch_bwd_t<DK_, DV_, bf>(d, cu, q, k, v, g, beta, h0, dout, dhT, scale, dq, dk, \
-                                                      dv, dg, dbeta, dh0, ws, stream)                  \
-                        : launch_bwd_t<DK_, DV_, float>(d, cu, q, k, v, g, beta, h0, dout, dhT, scale, dq,  \
-                                                         dk, dv, dg, dbeta, dh0, ws, stream);
-    KDA_BWD_CASE(64, 64)
-    KDA_BWD_CASE(64, 128)
-    KDA_BWD_CASE(128, 64)
-    KDA_BWD_CASE(128, 128)
+#define KDA_BWD_CASE(DK_, DV_, NVT_)                                                                  \
+    if (d.dk == DK_ && d.dv == DV_ && bwd_nvt(d) == NVT_)                                              \
+        return qkv_bf16 ? launch_bwd_t<DK_, DV_, NVT_, bf>(d, cu, q, k, v, g, beta, h0, dout, dhT, scale,   \
+                                                            dq, dk, dv, dg, dbeta, dh0, ws, stream)    \
+                        : launch_bwd_t<DK_, DV_, NVT_, float>(d, cu, q, k, v, g, beta, h0, dout, dhT,      \
+                                                               scale, dq, dk, dv, dg, dbeta, dh0, ws, stream);
+    KDA_BWD_CASE(64, 64, 32)
+    KDA_BWD_CASE(64, 64, 64)
+    KDA_BWD_CASE(64, 128, 32)
+    KDA_BWD_CASE(64, 128, 64)
+    KDA_BWD_CASE(128, 64, 32)
+    KDA_BWD_CASE(128, 64, 64)
+    KDA_BWD_CASE(128, 128, 32)
+    KDA_BWD_CASE(128, 128, 64)
 #undef KDA_BWD_CASE
     return cudaErrorInvalidValue;
 }
