@@ -75,7 +75,7 @@ struct SegRun {
     const int4* tasks;
     int ntasks;
     float* E;  // segment start states, row-major (and, before the scan, the middle segments' Z)
-    float* F;  // the middle segments' maps, transposed: F^T[m][r] = F[r][m]
+    float* F;  // the middle segments' maps, transposed: F^T[m][r] = F[r][m], rows of dk + kMapPad
 };
 
 // Where a task's chain starts and where its final state goes.
@@ -470,8 +470,10 @@ __device__ __forceinline__ void chain_role(const Dims& d, const float* __restric
                     const size_t slot = (size_t)(cur.w >> 4) * DK * DV;
                     if (kind == kTaskHead || kind == kTaskMapZ) dst = seg->E + slot;
                     if (kind == kTaskTail && !((cur.w >> 3) & 1)) dst = nullptr;  // the scan made it
-                    if (kind == kTaskMapF) {  // the map, transposed: F^T[n][c], 32 floats per thread
-                        float4* ft = reinterpret_cast<float4*>(seg->F + slot + (size_t)n * DK + 32 * g);
+                    if (kind == kTaskMapF) {  // the map, transposed: F^T[n][c] (padded rows), 32 floats per thread
+                        constexpr int LD = DK + kMapPad;
+                        float4* ft = reinterpret_cast<float4*>(seg->F + (size_t)(cur.w >> 4) * DK * LD +
+                                                               (size_t)n * LD + 32 * g);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             ft[e] = make_float4(S[4 * e], S[4 * e + 1], S[4 * e + 2], S[4 * e + 3]);

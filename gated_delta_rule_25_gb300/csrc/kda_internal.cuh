@@ -12,7 +12,8 @@
 //   (segments, when they may apply: dk = dv = 128 and N * H <= kSegPairs)
 //   seg_a, seg_c    int4[kSegTasks] each: the two chain passes' task lists
 //   seg_scan        int4[kSegPairs]: the scan's (pair, E slot, F slot, segments)
-//   seg_e, seg_f    fp32[slots][dk * dv] each: segment start states and maps
+//   seg_e, seg_f    fp32[slots][dk * dv] and [slots][dk * (dk + kMapPad)]: segment
+//                   start states and maps (F^T, rows padded)
 //
 // Per (chunk, head) factor block, every part a multiple of 256 bytes:
 //   WQ  [128 x dk] bf16, M-major operand layout: rows 0-63
@@ -98,6 +99,7 @@ struct FactorLayout {
 constexpr int kSegPairs = 64;    // (sequence, head) pairs, at most
 constexpr int kSegTasks = 1024;  // tasks of one pass, at most
 constexpr int kSegSlots = 160;   // segment start states (and maps), at most
+constexpr int kMapPad = 8;       // a map F^T is stored with rows of dk + kMapPad floats
 // Task kinds (int4 {first chunk, chunks, sequence * H + head, kind | last << 3 | slot << 4}).
 constexpr int kTaskWhole = 0;  // a whole chain: h0 -> outputs, h_T
 constexpr int kTaskHead = 1;   // segment 0: h0 -> outputs, end state to E[slot]
@@ -135,7 +137,7 @@ struct WsLayout {
         seg_c = off;     off += seg_slots ? size_t(kSegTasks) * 16 : 0;
         seg_scan = off;  off += seg_slots ? size_t(kSegPairs) * 16 : 0;
         seg_e = off;     off += size_t(seg_slots) * d.dk * d.dv * 4;
-        seg_f = off;     off += size_t(seg_slots) * d.dk * d.dv * 4;
+        seg_f = off;     off += size_t(seg_slots) * d.dk * (d.dk + kMapPad) * 4;
         total_seg = seg_slots ? off : total;
     }
 };

@@ -14,29 +14,46 @@ constexpr int kCDK = 128, kCDV = 128;  // the head dimensions segments apply to
 // start state of segment k + 1 is F_k E_k + Z_k (k = 1 .. segments - 2), E_1 being
 // the first segment's final state; Z_k is overwritten by the result.  The value
 // columns are independent, so each CTA takes one 16-column tile of one chain and
-// walks its segments in order, in fp32: F_k^T arrives in shared memory by one bulk
-// copy (two buffers: the maps do not depend on the scan, so the next one loads
-// while a step computes) and the tile stays in shared memory.  The sum over m is
-// split in four quarters over the CTA's 16 warps (enough warps to hide the shared
-// memory latency); in each quarter a thread accumulates a 4 x 4 block (per m, a
-// float4 of F^T's row m and one of the tile's row m: conflict-free and broadcast),
-// and the four partial blocks are added with Z_k through shared memory.
-constexpr int kScanCols = 16, kScanThreads = 512, kScanK = 4;
-constexpr int kPrevLd = kScanCols + 4;  // padded rows: the output threads' row-wise writes hit distinct banks
+// walks its segments in order.  F_k^T arrives in shared memory by one bulk copy (two
+// buffers: the maps do not depend on the scan, so the next one loads while a step
+// computes; its rows are padded to dk + 8 floats when the map task writes it, so
+// that the copy lands conflict-free for the fragment loads) and the tile stays in
+// shared memory (rows padded to 24 floats).  Each step is F_k E_k on the tensor cores
+// (mma.sync m16n8k8 on tf32 operands, each split into a tf32 high part and the
+// rounding remainder, three products per k-step: about fp32 accuracy), warp w taking
+// rows 16 w .. 16 w + 15 and both 8-column halves of the tile; Z_k, loaded a step
+// ahead, is added in fp32.
+constexpr int kScanCols = 16, kScanThreads = 256, kFBufs = 2;
+constexpr int kFLd = kCDK + kMapPad;     // padded row of F^T (136: bank offset 8 per row)
+constexpr int kPLd = kScanCols + 8;      // padded row of the tile (24: bank offset 24 per row)
 struct __align__(16) ScanSmem {
-    float FT[2][kCDK * kCDK];
-    float prev[kCDK][kPrevLd];
-    // partial 4 x 4 blocks: [quarter][column group][row group][4 float4], the float4 of
-    // block row r at position r ^ ((row group / 2) & 3), so that the 8 threads of a
-    // quarter warp store to distinct banks
-    float part[kScanK][kScanCols / 4][kCDK / 4][16];
-    uint64_t full[2];
+    float FT[kFBufs][kCDK * kFLd];
+    float prev[kCDK * kPLd];
+    uint64_t full[kFBufs];
     int abort;
 };
 
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// x = hi + lo with hi = x rounded to tf32 and lo the remainder rounded to tf32.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32_bits(x);
+    lo = tf32_bits(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t* __restrict__ ws) {
-    constexpr int DK = kCDK, DV = kCDV, kTiles = DV / kScanCols, kM = DK / kScanK;
-    constexpr uint32_t FB = DK * DK * 4;
+    constexpr int DK = kCDK, DV = kCDV, kTiles = DV / kScanCols;
+    constexpr uint32_t FB = DK * kFLd * 4;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     ScanSmem& sm = *reinterpret_cast<ScanSmem*>(smem_raw);
     const WsLayout W(d);
@@ -48,83 +65,102 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
     const int steps = e.w - 2;
     float* E = reinterpret_cast<float*>(ws + W.seg_e);
     const float* FT = reinterpret_cast<const float*>(ws + W.seg_f);
-    const int tid = threadIdx.x;
-    const int kq = tid >> 7, rg = tid & 31, cg = (tid >> 5) & 3;  // m quarter; rows 4 rg .., columns 4 cg ..
-    const int orow = tid & (DK - 1), ocol = 4 * (tid >> 7);          // the output float4 of this thread
-    const int swz = (rg >> 1) & 3, oswz = ((orow >> 2) >> 1) & 3;
-    uint32_t issued[2] = {0, 0};
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3, r0 = 16 * warp;  // fragment row group, k index; the warp's rows
+    uint32_t issued[kFBufs] = {};
     if (tid == 0) {
-        ptx::mbar_init(&sm.full[0], 1);
-        ptx::mbar_init(&sm.full[1], 1);
+        for (int bb = 0; bb < kFBufs; ++bb) ptx::mbar_init(&sm.full[bb], 1);
         sm.abort = 0;
         ptx::fence_mbar_init();
         // The maps and Z of the later steps into L2 now (pass A's factor reads may have
         // pushed them out), each by one of the chain's tile CTAs.
         const int tile = (int)blockIdx.x % kTiles;
-        for (int k = 3 + tile; k <= steps; k += kTiles) {
-            ptx::bulk_prefetch_l2(FT + (size_t)(e.z + k - 1) * DK * DK, FB);
-            ptx::bulk_prefetch_l2(E + (size_t)(e.y + k) * DK * DV, FB);
+        for (int k = kFBufs + 1 + tile; k <= steps; k += kTiles) {
+            ptx::bulk_prefetch_l2(FT + (size_t)(e.z + k - 1) * DK * kFLd, FB);
+            ptx::bulk_prefetch_l2(E + (size_t)(e.y + k) * DK * DV, DK * DV * 4);
         }
-        for (int k = 1; k <= 2 && k <= steps; ++k) {
+        for (int k = 1; k <= kFBufs && k <= steps; ++k) {
             ptx::mbar_arrive_expect_tx(&sm.full[k - 1], FB);
-            ptx::bulk_g2s(sm.FT[k - 1], FT + (size_t)(e.z + k - 1) * DK * DK, FB, &sm.full[k - 1]);
+            ptx::bulk_g2s(sm.FT[k - 1], FT + (size_t)(e.z + k - 1) * DK * kFLd, FB, &sm.full[k - 1]);
             ++issued[k - 1];
         }
     }
-    *reinterpret_cast<float4*>(&sm.prev[orow][ocol]) =
-        *reinterpret_cast<const float4*>(E + (size_t)e.y * DK * DV + (size_t)orow * DV + col0 + ocol);
+    for (int x = tid; x < DK * kScanCols; x += kScanThreads)
+        sm.prev[(x / kScanCols) * kPLd + x % kScanCols] =
+            E[(size_t)e.y * DK * DV + (size_t)(x / kScanCols) * DV + col0 + x % kScanCols];
     __syncthreads();
     bool ok = true;
+    // this lane's outputs: rows r0 + gq (+ 8), columns 8 nt + 2 tq (+ 1); Z of the next
+    // step is loaded while a step computes
+    float2 zn[2][2];
+    auto load_z = [&](int k) {
+        const float* Ek = E + (size_t)(e.y + k) * DK * DV + col0;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                zn[nt][h] = *reinterpret_cast<const float2*>(Ek + (size_t)(r0 + gq + 8 * h) * DV + 8 * nt + 2 * tq);
+    };
+    if (steps >= 1) load_z(1);
     for (int k = 1; k <= steps; ++k) {
-        const int b = (k - 1) & 1;
-        float* Ek = E + (size_t)(e.y + k) * DK * DV + (size_t)orow * DV + col0 + ocol;
-        const float4 z = *reinterpret_cast<const float4*>(Ek);
-        ok = __syncthreads_and(ptx::mbar_wait_or_abort(&sm.full[b], ((k - 1) >> 1) & 1u, &sm.abort));
+        const int b = (k - 1) % kFBufs;
+        float* Ek = E + (size_t)(e.y + k) * DK * DV + col0;
+        float2 z[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) z[nt][h] = zn[nt][h];
+        if (k < steps) load_z(k + 1);
+        ok = __syncthreads_and(ptx::mbar_wait_or_abort(&sm.full[b], ((k - 1) / kFBufs) & 1u, &sm.abort));
         if (!ok) break;
-        float acc[4][4] = {};
-        const float* ft = sm.FT[b] + kq * kM * DK + 4 * rg;
-        const float* pv = &sm.prev[kq * kM][4 * cg];
-        // the loads of m + 1 are in flight while m's 16 products run
-        float4 f = *reinterpret_cast<const float4*>(ft), p = *reinterpret_cast<const float4*>(pv);
+        const float* F = sm.FT[b];
+        float acc[2][4] = {};
 #pragma unroll 4
-        for (int m = 0; m < kM; ++m) {
-            const float fr[4] = {f.x, f.y, f.z, f.w}, pc[4] = {p.x, p.y, p.z, p.w};
-            if (m + 1 < kM) {
-                f = *reinterpret_cast<const float4*>(ft + (m + 1) * DK);
-                p = *reinterpret_cast<const float4*>(pv + (m + 1) * kPrevLd);
+        for (int kk = 0; kk < DK / 8; ++kk) {
+            const int m0 = 8 * kk;
+            // A = F (rows r, k = m): F[r][m] = F^T[m][r]
+            const float af[4] = {F[(m0 + tq) * kFLd + r0 + gq], F[(m0 + tq) * kFLd + r0 + gq + 8],
+                                 F[(m0 + tq + 4) * kFLd + r0 + gq], F[(m0 + tq + 4) * kFLd + r0 + gq + 8]};
+            uint32_t ahi[4], alo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) split_tf32(af[j], ahi[j], alo[j]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                // B = the tile (k = m, n = column)
+                const float b0f = sm.prev[(m0 + tq) * kPLd + 8 * nt + gq];
+                const float b1f = sm.prev[(m0 + tq + 4) * kPLd + 8 * nt + gq];
+                uint32_t b0h, b0l, b1h, b1l;
+                split_tf32(b0f, b0h, b0l);
+                split_tf32(b1f, b1h, b1l);
+                mma_tf32_16x8x8(acc[nt], alo, b0h, b1h);
+                mma_tf32_16x8x8(acc[nt], ahi, b0l, b1l);
+                mma_tf32_16x8x8(acc[nt], ahi, b0h, b1h);
             }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(fr[r], pc[c], acc[r][c]);
         }
+        __syncthreads();  // every warp has read the previous start state and F buffer b
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<float4*>(&sm.part[kq][cg][rg][4 * (r ^ swz)]) =
-                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-        __syncthreads();  // every partial block written; the previous start state and F buffer b read
-        float4 v = z;
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int q = 0; q < kScanK; ++q) {
-            const float4 pp = *reinterpret_cast<const float4*>(
-                &sm.part[q][ocol >> 2][orow >> 2][4 * ((orow & 3) ^ oswz)]);
-            v.x += pp.x; v.y += pp.y; v.z += pp.z; v.w += pp.w;
-        }
-        *reinterpret_cast<float4*>(&sm.prev[orow][ocol]) = v;
-        *reinterpret_cast<float4*>(Ek) = v;
-        if (tid == 0 && k + 2 <= steps) {  // the map after next into the buffer just read
+            for (int h = 0; h < 2; ++h) {
+                const int row = r0 + gq + 8 * h, col = 8 * nt + 2 * tq;
+                const float2 v = make_float2(acc[nt][2 * h] + z[nt][h].x, acc[nt][2 * h + 1] + z[nt][h].y);
+                sm.prev[row * kPLd + col] = v.x;
+                sm.prev[row * kPLd + col + 1] = v.y;
+                *reinterpret_cast<float2*>(Ek + (size_t)row * DV + col) = v;
+            }
+        if (tid == 0 && k + kFBufs <= steps) {  // the map kFBufs steps ahead into the buffer just read
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive_expect_tx(&sm.full[b], FB);
-            ptx::bulk_g2s(sm.FT[b], FT + (size_t)(e.z + k + 1) * DK * DK, FB, &sm.full[b]);
+            ptx::bulk_g2s(sm.FT[b], FT + (size_t)(e.z + k + kFBufs - 1) * DK * kFLd, FB, &sm.full[b]);
             ++issued[b];
         }
-        __syncthreads();  // the new start state complete; the partial blocks read
+        __syncthreads();  // the new start state complete
     }
     if (!ok && tid == 0) {  // a copy did not land in time: report, and let those in flight land
         atomicOr(&hdr->error, kDevErrTimeout);
         volatile int never = 0;
-        for (int b = 0; b < 2; ++b)
-            if (issued[b]) ptx::mbar_wait_or_abort(&sm.full[b], (issued[b] - 1) & 1u, &never);
+        for (int bb = 0; bb < kFBufs; ++bb)
+            if (issued[bb]) ptx::mbar_wait_or_abort(&sm.full[bb], (issued[bb] - 1) & 1u, &never);
     }
 }
 
