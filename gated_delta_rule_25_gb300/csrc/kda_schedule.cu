@@ -31,7 +31,7 @@ __host__ __device__ inline float tiled_time(int longest, long long steps, int H,
 // Both passes must fit one round of CTAs, and the start states the slots.  Time
 // (measured on GB300): 2.5 us per step of the longest task of each pass plus about
 // 10 us per pass (a task's start and end: tensor memory, barriers, its first
-// copies, its final state), and for the scan about 5 us plus 2.9 us per serial step.
+// copies, its final state), and for the scan about 5 us plus 2.6 us per serial step.
 struct SegCount {
     int tasks_a, slots, nseg_max, tail_max;
     __host__ __device__ void add(int n, int L, int H) {  // one sequence of n > 0 chunks
@@ -47,7 +47,7 @@ struct SegCount {
         const int cap = sms < kSegTasks - empty_tasks ? sms : kSegTasks - empty_tasks;
         if (nseg_max < 3 || tasks_a > cap || slots > slot_cap) return -1.f;
         const int head = L < longest ? L : longest;
-        return kStep128 * (float)(head + tail_max) + 2.f * 10.f + 5.f + 2.9f * (float)(nseg_max - 2);
+        return kStep128 * (float)(head + tail_max) + 2.f * 10.f + 5.f + 2.6f * (float)(nseg_max - 2);
     }
 };
 

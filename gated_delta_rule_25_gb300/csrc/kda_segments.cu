@@ -18,7 +18,8 @@ constexpr int kCDK = 128, kCDV = 128;  // the head dimensions segments apply to
 // buffers: the maps do not depend on the scan, so the next one loads while a step
 // computes; its rows are padded to dk + 8 floats when the map task writes it, so
 // that the copy lands conflict-free for the fragment loads) and the tile stays in
-// shared memory (rows padded to 24 floats).  Each step is F_k E_k on the tensor cores
+// shared memory (rows padded to 24 floats) already split into its tf32 high part and
+// remainder, written once per step instead of converted by every warp.  Each step is F_k E_k on the tensor cores
 // (mma.sync m16n8k8 on tf32 operands, each split into a tf32 high part and the
 // rounding remainder, three products per k-step: about fp32 accuracy), warp w taking
 // rows 16 w .. 16 w + 15 and both 8-column halves of the tile; Z_k, loaded a step
@@ -28,7 +29,7 @@ constexpr int kFLd = kCDK + kMapPad;     // padded row of F^T (136: bank offset 
 constexpr int kPLd = kScanCols + 8;      // padded row of the tile (24: bank offset 24 per row)
 struct __align__(16) ScanSmem {
     float FT[kFBufs][kCDK * kFLd];
-    float prev[kCDK * kPLd];
+    uint32_t phi[kCDK * kPLd], plo[kCDK * kPLd];  // the tile: tf32 high part, remainder
     uint64_t full[kFBufs];
     int abort;
 };
@@ -85,9 +86,11 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
             ++issued[k - 1];
         }
     }
-    for (int x = tid; x < DK * kScanCols; x += kScanThreads)
-        sm.prev[(x / kScanCols) * kPLd + x % kScanCols] =
-            E[(size_t)e.y * DK * DV + (size_t)(x / kScanCols) * DV + col0 + x % kScanCols];
+    for (int x = tid; x < DK * kScanCols; x += kScanThreads) {
+        const int at = (x / kScanCols) * kPLd + x % kScanCols;
+        split_tf32(E[(size_t)e.y * DK * DV + (size_t)(x / kScanCols) * DV + col0 + x % kScanCols], sm.phi[at],
+                   sm.plo[at]);
+    }
     __syncthreads();
     bool ok = true;
     // this lane's outputs: rows r0 + gq (+ 8), columns 8 nt + 2 tq (+ 1); Z of the next
@@ -114,27 +117,30 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
         ok = __syncthreads_and(ptx::mbar_wait_or_abort(&sm.full[b], ((k - 1) / kFBufs) & 1u, &sm.abort));
         if (!ok) break;
         const float* F = sm.FT[b];
-        float acc[2][4] = {};
-#pragma unroll 4
-        for (int kk = 0; kk < DK / 8; ++kk) {
-            const int m0 = 8 * kk;
-            // A = F (rows r, k = m): F[r][m] = F^T[m][r]
-            const float af[4] = {F[(m0 + tq) * kFLd + r0 + gq], F[(m0 + tq) * kFLd + r0 + gq + 8],
-                                 F[(m0 + tq + 4) * kFLd + r0 + gq], F[(m0 + tq + 4) * kFLd + r0 + gq + 8]};
-            uint32_t ahi[4], alo[4];
+        // three accumulators per column half and k parity (the three products of a
+        // k-step; even and odd k-steps), so that the dependent chains of tensor-core
+        // operations are a sixth as long
+        float acc[2][2][3][4] = {};
+#pragma unroll 2
+        for (int k2 = 0; k2 < DK / 16; ++k2) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) split_tf32(af[j], ahi[j], alo[j]);
+            for (int par = 0; par < 2; ++par) {
+                const int m0 = 16 * k2 + 8 * par;
+                // A = F (rows r, k = m): F[r][m] = F^T[m][r]
+                const float af[4] = {F[(m0 + tq) * kFLd + r0 + gq], F[(m0 + tq) * kFLd + r0 + gq + 8],
+                                     F[(m0 + tq + 4) * kFLd + r0 + gq], F[(m0 + tq + 4) * kFLd + r0 + gq + 8]};
+                uint32_t ahi[4], alo[4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                // B = the tile (k = m, n = column)
-                const float b0f = sm.prev[(m0 + tq) * kPLd + 8 * nt + gq];
-                const float b1f = sm.prev[(m0 + tq + 4) * kPLd + 8 * nt + gq];
-                uint32_t b0h, b0l, b1h, b1l;
-                split_tf32(b0f, b0h, b0l);
-                split_tf32(b1f, b1h, b1l);
-                mma_tf32_16x8x8(acc[nt], alo, b0h, b1h);
-                mma_tf32_16x8x8(acc[nt], ahi, b0l, b1l);
-                mma_tf32_16x8x8(acc[nt], ahi, b0h, b1h);
+                for (int j = 0; j < 4; ++j) split_tf32(af[j], ahi[j], alo[j]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    // B = the tile (k = m, n = column), already split
+                    const int at0 = (m0 + tq) * kPLd + 8 * nt + gq, at1 = at0 + 4 * kPLd;
+                    const uint32_t b0h = sm.phi[at0], b0l = sm.plo[at0], b1h = sm.phi[at1], b1l = sm.plo[at1];
+                    mma_tf32_16x8x8(acc[nt][par][0], alo, b0h, b1h);
+                    mma_tf32_16x8x8(acc[nt][par][1], ahi, b0l, b1l);
+                    mma_tf32_16x8x8(acc[nt][par][2], ahi, b0h, b1h);
+                }
             }
         }
         __syncthreads();  // every warp has read the previous start state and F buffer b
@@ -143,9 +149,14 @@ __global__ void __launch_bounds__(kScanThreads) seg_scan_kernel(Dims d, uint8_t*
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int row = r0 + gq + 8 * h, col = 8 * nt + 2 * tq;
-                const float2 v = make_float2(acc[nt][2 * h] + z[nt][h].x, acc[nt][2 * h + 1] + z[nt][h].y);
-                sm.prev[row * kPLd + col] = v.x;
-                sm.prev[row * kPLd + col + 1] = v.y;
+                const int i0 = 2 * h, i1 = 2 * h + 1;
+                auto sum = [&](int i) {
+                    return (acc[nt][0][2][i] + acc[nt][1][2][i]) +
+                           ((acc[nt][0][0][i] + acc[nt][0][1][i]) + (acc[nt][1][0][i] + acc[nt][1][1][i]));
+                };
+                const float2 v = make_float2(sum(i0) + z[nt][h].x, sum(i1) + z[nt][h].y);
+                split_tf32(v.x, sm.phi[row * kPLd + col], sm.plo[row * kPLd + col]);
+                split_tf32(v.y, sm.phi[row * kPLd + col + 1], sm.plo[row * kPLd + col + 1]);
                 *reinterpret_cast<float2*>(Ek + (size_t)row * DV + col) = v;
             }
         if (tid == 0 && k + kFBufs <= steps) {  // the map kFBufs steps ahead into the buffer just read
