@@ -19,11 +19,11 @@ constexpr int kCDK = 128, kCDV = 128;  // the head dimensions segments apply to
 // computes; its rows are padded to dk + 8 floats when the map task writes it, so
 // that the copy lands conflict-free for the fragment loads) and the tile stays in
 // shared memory (rows padded to 24 floats) already split into its tf32 high part and
-// remainder, written once per step instead of converted by every warp.  Each step is F_k E_k on the tensor cores
-// (mma.sync m16n8k8 on tf32 operands, each split into a tf32 high part and the
-// rounding remainder, three products per k-step: about fp32 accuracy), warp w taking
-// rows 16 w .. 16 w + 15 and both 8-column halves of the tile; Z_k, loaded a step
-// ahead, is added in fp32.
+// remainder, written once per step instead of converted by every warp.  Each step is
+// F_k E_k on the tensor cores (mma.sync m16n8k8 on tf32 operands, each split into a
+// tf32 high part and the rounding remainder, three products per k-step: about fp32
+// accuracy), warp w taking rows 16 w .. 16 w + 15 and both 8-column halves of the
+// tile; Z_k, loaded a step ahead, is added in fp32.
 constexpr int kScanCols = 16, kScanThreads = 256, kFBufs = 2;
 constexpr int kFLd = kCDK + kMapPad;     // padded row of F^T (136: bank offset 8 per row)
 constexpr int kPLd = kScanCols + 8;      // padded row of the tile (24: bank offset 24 per row)
