@@ -1,4 +1,4 @@
-"""Kimi Delta Attention prefill forward for GB300 (sm_103a).
+"""Kimi Delta Attention prefill forward (and its backward) for GB300 (sm_103a).
 
 A thin binding over the C ABI in ``include/kda.h`` (``_lib/libkda.so``).  This
 module only checks and marshals arguments; every step of the computation runs in
@@ -6,7 +6,9 @@ the library's CUDA kernels.  PyTorch provides device memory and the current
 stream.  There is no CPU path: without the built library every call raises.
 
     o, hT = fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, scale=None)
+    dq, dk, dv, dg, dbeta, dh0 = bwd(q, k, v, g, beta, h0, cu_seqlens, scale, do=do, dhT=dhT)
     o, h  = decode(q, k, v, g, beta, state=None, scale=None)   # one token per sequence
+    set_pipeline("auto" | "fused" | "split" | "split-whole")  # the forward's kernels
 
 q, k: [B, T, H, dk]; v: [B, T, H, dv] (bf16 or fp32, same dtype); g: [B, T, H, dk]
 fp32, or bf16 with bf16 q/k/v (log of the per-channel decay, <= 0); beta: [B, T, H] fp32 in [0, 1];
